@@ -1,0 +1,327 @@
+/*
+ * oracle.c -- plain, slow, fp64 CPU oracle for the softcapped LM-head
+ * cross-entropy path.  TEST INFRASTRUCTURE ONLY: only the tests, the smoke
+ * check and the benchmark's cpu_baseline / reference leg may load this.  It
+ * shares no code, header, table or helper with the CUDA library.
+ *
+ * What it computes (each function names the passage it follows):
+ *
+ *   z_ij   = sum_k h_ik W_jk                         (tied LM head)
+ *   s_ij   = c * tanh(z_ij / c)                      (tanh logit softcap)
+ *   lse_i  = log sum_j exp(s_ij)                     (log-sum-exp)
+ *   nll_i  = lse_i - s_{i,t_i}                       (next-token NLL)
+ *   bpb    = sum_i nll_i / (ln 2 * sum_i bytes_i)    (bits per byte)
+ *   dz_ij  = w * (p_ij - [j == t_i]) * (1 - tanh^2(z_ij / c)),
+ *            p_ij = exp(s_ij - lse_i)
+ *   dh     = dZ W,  dW = dZ^T h                      (training backward)
+ *   W_deq  = bf16_rne(q * scale)                     (per-group int4 head)
+ *
+ * Sources (page title, section):
+ *  - "parameter-golf: Parameter Golf: The OpenAI Repo Where Model Size Becomes
+ *    the Game", section "The Baseline Is a Map, Not the Destination": the
+ *    training step is logits = model(x); loss = criterion(logits, y).
+ *  - "OpenAI launched Parameter Golf" (tproger news), section "Rules and
+ *    metric": the score is bits per byte on FineWeb validation, i.e. the
+ *    compression measured in bytes, independent of the tokenizer.
+ *  - "parameter-golf README", Leaderboard, row "Naive Baseline": 9 layers,
+ *    512 dim, 1024 vocab, TiedEmbeddings -> the head is the embedding W.
+ *  - "HYDRA Golf" site, stack list: "fused softcapped CE kernel"; and
+ *    "parameter-golf README", Leaderboard, row "PR1736 + PolarNS + MIN_LR +
+ *    SparseAttnGate + FusedCE + Warm-A TTT": "fused softcapped CE".  The pages
+ *    do not print the softcap formula; this oracle takes the tanh form
+ *    s = c*tanh(z/c) (the plainest reading of "softcapped" logits).
+ *  - "parameter-golf README", Leaderboard, row "Sliding Window Eval": stride
+ *    64 evaluation, realised here as a row mask.
+ *  - "HYDRA Golf" site, stack list: "LQER asymmetric int4, per-group
+ *    compression"; the symmetric per-group-64 fp16-scale reading is used.
+ *
+ * No blocking, fusion or reordering: every function is the definition
+ * written out with plain loops (OpenMP over independent rows only), with the
+ * log-sum-exp taken about the row maximum for range safety.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_OK 0
+#define ORACLE_EINVAL 1
+#define ORACLE_EDATA 4
+
+/* ---- number formats, from their IEEE / bfloat16 definitions ------------ */
+
+/* bfloat16 is the upper half of an IEEE binary32: widening is exact. */
+double oracle_bf16_to_f64(uint16_t b) {
+  uint32_t u = ((uint32_t)b) << 16;
+  float f;
+  memcpy(&f, &u, sizeof f);
+  return (double)f;
+}
+
+/* IEEE binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+double oracle_f16_to_f64(uint16_t b) {
+  int sign = (b >> 15) & 1;
+  int e = (b >> 10) & 31;
+  int m = b & 1023;
+  double v;
+  if (e == 0) {
+    v = ldexp((double)m, -24);                 /* zero or subnormal */
+  } else if (e == 31) {
+    v = (m == 0) ? INFINITY : NAN;
+  } else {
+    v = ldexp((double)(1024 + m), e - 25);     /* (1.m) * 2^(e-15) */
+  }
+  return sign ? -v : v;
+}
+
+/* Round a double to the nearest bfloat16 (ties to even) and return its bits.
+ * bfloat16: 8 significant bits, exponent range of binary32 (normals down to
+ * 2^-126, subnormals in steps of 2^-133), overflow to infinity. */
+uint16_t oracle_f64_to_bf16_rne(double x) {
+  if (isnan(x)) return 0x7FC0;
+  uint16_t sign = signbit(x) ? 0x8000 : 0;
+  double a = fabs(x);
+  if (a == 0.0) return sign;
+  if (isinf(a)) return sign | 0x7F80;
+  int k;
+  frexp(a, &k);                       /* a = f * 2^k, f in [0.5, 1) */
+  int e = k - 1;                      /* a in [2^e, 2^(e+1)) */
+  int qexp = (e < -126) ? -133 : e - 7;
+  double q = ldexp(a, -qexp);         /* exact: power-of-two scaling */
+  double r = nearbyint(q);            /* default mode: nearest, ties even */
+  double v = ldexp(r, qexp);
+  if (v >= ldexp(1.0, 128)) return sign | 0x7F80;
+  float f = (float)v;                 /* exact: <= 8 significant bits */
+  uint32_t u;
+  memcpy(&u, &f, sizeof u);
+  return sign | (uint16_t)(u >> 16);
+}
+
+void oracle_bf16_to_f64_array(const uint16_t* in, double* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_f64(in[i]);
+}
+
+/* ---- forward: softcapped cross-entropy of the tied head ---------------- */
+
+/* One row's forward.  s must hold V doubles of scratch. */
+static void fwd_row(const double* hi, const double* W, int64_t V, int64_t d,
+                    double c, int64_t t, double* s, double* nll_out,
+                    double* lse_out) {
+  double m = -INFINITY;
+  for (int64_t j = 0; j < V; ++j) {
+    const double* wj = W + j * d;
+    double z = 0.0;
+    for (int64_t k = 0; k < d; ++k) z += hi[k] * wj[k];
+    s[j] = c * tanh(z / c);
+    if (s[j] > m) m = s[j];
+  }
+  double sum = 0.0;
+  for (int64_t j = 0; j < V; ++j) sum += exp(s[j] - m);
+  double lse = m + log(sum);
+  *lse_out = lse;
+  *nll_out = lse - s[t];
+}
+
+/* Forward over all rows (rows == NULL) or over the n_rows listed in rows.
+ * Masked rows (mask[i] == 0) get nll = 0 and lse = 0.  A target outside
+ * [0, V) on an unmasked row returns ORACLE_EDATA. */
+int oracle_fwd_f64(const double* h, const double* W, int64_t N, int64_t V,
+                   int64_t d, const int64_t* tgt, const uint8_t* mask,
+                   double c, const int64_t* rows, int64_t n_rows,
+                   double* nll, double* lse) {
+  if (!h || !W || !tgt || !nll || !lse || N <= 0 || V <= 0 || d <= 0 ||
+      !(c > 0.0))
+    return ORACLE_EINVAL;
+  int64_t n_out = rows ? n_rows : N;
+  for (int64_t r = 0; r < n_out; ++r) {
+    int64_t i = rows ? rows[r] : r;
+    if (i < 0 || i >= N) return ORACLE_EINVAL;
+    if (mask && !mask[i]) continue;
+    if (tgt[i] < 0 || tgt[i] >= V) return ORACLE_EDATA;
+  }
+  int err = 0;
+#pragma omp parallel
+  {
+    double* s = (double*)malloc((size_t)V * sizeof(double));
+    if (!s) {
+#pragma omp atomic write
+      err = 1;
+    }
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_out; ++r) {
+      if (!s) continue;
+      int64_t i = rows ? rows[r] : r;
+      if (mask && !mask[i]) {
+        nll[r] = 0.0;
+        lse[r] = 0.0;
+        continue;
+      }
+      fwd_row(h + i * d, W, V, d, c, tgt[i], s, &nll[r], &lse[r]);
+    }
+    free(s);
+  }
+  return err ? ORACLE_EINVAL : ORACLE_OK;
+}
+
+/* ---- bits per byte ----------------------------------------------------- */
+
+/* sum of nll over unmasked rows in index order, sum of bytes, row count;
+ * bpb = sum_nll / (ln 2 * sum_bytes).  Returns NAN bpb if sum_bytes == 0. */
+double oracle_bpb(const double* nll, const int32_t* bytes, const uint8_t* mask,
+                  int64_t N, double* sum_nll_out, int64_t* sum_bytes_out,
+                  int64_t* n_out) {
+  double sn = 0.0;
+  int64_t sb = 0, n = 0;
+  for (int64_t i = 0; i < N; ++i) {
+    if (mask && !mask[i]) continue;
+    sn += nll[i];
+    sb += bytes[i];
+    n += 1;
+  }
+  if (sum_nll_out) *sum_nll_out = sn;
+  if (sum_bytes_out) *sum_bytes_out = sb;
+  if (n_out) *n_out = n;
+  if (sb == 0) return NAN;
+  return sn / (log(2.0) * (double)sb);
+}
+
+/* ---- backward ---------------------------------------------------------- */
+
+/* dz for one row given its lse: dz_j = w (p_j - [j==t]) (1 - tanh^2(z_j/c)).
+ * Chain rule of nll = lse - s_t through s = c tanh(z/c):
+ *   d nll / d s_j = p_j - [j == t],   d s_j / d z_j = 1 - tanh^2(z_j / c). */
+static void dz_row(const double* hi, const double* W, int64_t V, int64_t d,
+                   double c, int64_t t, double lse, double w, double* dz) {
+  for (int64_t j = 0; j < V; ++j) {
+    const double* wj = W + j * d;
+    double z = 0.0;
+    for (int64_t k = 0; k < d; ++k) z += hi[k] * wj[k];
+    double th = tanh(z / c);
+    double s = c * th;
+    double p = exp(s - lse);
+    double g = p - (j == t ? 1.0 : 0.0);
+    dz[j] = w * g * (1.0 - th * th);
+  }
+}
+
+/* Gradient of L = sum over unmasked rows of w * nll_i.
+ * lse: as returned by oracle_fwd_f64 (all N rows).  dh [N, d] (may be NULL),
+ * dW [V, d] (may be NULL), both overwritten (not accumulated). */
+int oracle_bwd_f64(const double* h, const double* W, int64_t N, int64_t V,
+                   int64_t d, const int64_t* tgt, const uint8_t* mask,
+                   double c, const double* lse, double w, double* dh,
+                   double* dW) {
+  if (!h || !W || !tgt || !lse || N <= 0 || V <= 0 || d <= 0 || !(c > 0.0))
+    return ORACLE_EINVAL;
+  for (int64_t i = 0; i < N; ++i) {
+    if (mask && !mask[i]) continue;
+    if (tgt[i] < 0 || tgt[i] >= V) return ORACLE_EDATA;
+  }
+  double* dZ = (double*)calloc((size_t)N * (size_t)V, sizeof(double));
+  if (!dZ) return ORACLE_EINVAL;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t i = 0; i < N; ++i) {
+    if (mask && !mask[i]) continue;   /* masked rows: dz = 0 */
+    dz_row(h + i * d, W, V, d, c, tgt[i], lse[i], w, dZ + i * V);
+  }
+  if (dh) {
+#pragma omp parallel for schedule(static)
+    for (int64_t i = 0; i < N; ++i) {
+      for (int64_t k = 0; k < d; ++k) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < V; ++j) acc += dZ[i * V + j] * W[j * d + k];
+        dh[i * d + k] = acc;
+      }
+    }
+  }
+  if (dW) {
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < V; ++j) {
+      for (int64_t k = 0; k < d; ++k) {
+        double acc = 0.0;
+        for (int64_t i = 0; i < N; ++i) acc += dZ[i * V + j] * h[i * d + k];
+        dW[j * d + k] = acc;
+      }
+    }
+  }
+  free(dZ);
+  return ORACLE_OK;
+}
+
+/* dh for the n_rows listed rows only (full-size sampled checks); lse_rows
+ * holds those rows' lse in the same order. */
+int oracle_dh_rows_f64(const double* h, const double* W, int64_t N, int64_t V,
+                       int64_t d, const int64_t* tgt, const uint8_t* mask,
+                       double c, const int64_t* rows, int64_t n_rows,
+                       const double* lse_rows, double w, double* dh_rows) {
+  if (!h || !W || !tgt || !rows || !lse_rows || !dh_rows || !(c > 0.0))
+    return ORACLE_EINVAL;
+  int err = 0;
+#pragma omp parallel
+  {
+    double* dz = (double*)malloc((size_t)V * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t r = 0; r < n_rows; ++r) {
+      int64_t i = rows[r];
+      double* out = dh_rows + r * d;
+      if (!dz || i < 0 || i >= N) {
+#pragma omp atomic write
+        err = 1;
+        continue;
+      }
+      if (mask && !mask[i]) {
+        for (int64_t k = 0; k < d; ++k) out[k] = 0.0;
+        continue;
+      }
+      if (tgt[i] < 0 || tgt[i] >= V) {
+#pragma omp atomic write
+        err = 4;
+        continue;
+      }
+      dz_row(h + i * d, W, V, d, c, tgt[i], lse_rows[r], w, dz);
+      for (int64_t k = 0; k < d; ++k) {
+        double acc = 0.0;
+        for (int64_t j = 0; j < V; ++j) acc += dz[j] * W[j * d + k];
+        out[k] = acc;
+      }
+    }
+    free(dz);
+  }
+  return err;
+}
+
+/* ---- per-group int4 head ----------------------------------------------- */
+
+/* Wq: [V, d/2] bytes, element 2m in the low nibble of byte m and 2m+1 in
+ * the high nibble, each a two's-complement value in [-8, 7].
+ * scales: [V, d/group] IEEE binary16 bits.
+ * out[v, k] = bf16_rne(q[v, k] * scale[v, k / group])  (bf16 bits).
+ * The product is formed exactly in double before the single rounding. */
+int oracle_dequant_int4(const uint8_t* Wq, const uint16_t* scales, int64_t V,
+                        int64_t d, int64_t group, uint16_t* out) {
+  if (!Wq || !scales || !out || V <= 0 || d <= 0 || group <= 0 ||
+      d % 2 != 0 || d % group != 0)
+    return ORACLE_EINVAL;
+  int64_t ng = d / group;
+  for (int64_t v = 0; v < V; ++v) {
+    for (int64_t k = 0; k < d; ++k) {
+      uint8_t byte = Wq[v * (d / 2) + k / 2];
+      int nib = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      int q = (nib >= 8) ? nib - 16 : nib;
+      double sc = oracle_f16_to_f64(scales[v * ng + k / group]);
+      out[v * d + k] = oracle_f64_to_bf16_rne((double)q * sc);
+    }
+  }
+  return ORACLE_OK;
+}
+
+int oracle_num_threads(void) {
+#ifdef _OPENMP
+  return omp_get_max_threads();
+#else
+  return 1;
+#endif
+}
