@@ -1,0 +1,173 @@
+/*
+ * lmhead_ce.h -- C ABI of the fused tied-LM-head + softcapped cross-entropy
+ * library for B300 (sm_103a).
+ *
+ * The operation (notation: N rows, d model dim, V vocab, c softcap):
+ *   z = h W^T                   tied LM head: W is the [V, d] embedding table
+ *   s = c * tanh(z / c)         tanh logit softcap
+ *   lse_i = ln sum_j exp(s_ij)  log-sum-exp over the vocabulary
+ *   nll_i = lse_i - s_{i,t_i}   next-token negative log-likelihood
+ *   bpb = sum nll / (ln 2 * sum bytes)       bits per byte
+ *   dh = w G W,  dW (+)= w G^T h,  G_ij = (p_ij - [j == t_i]) (1 - (s_ij/c)^2),
+ *   p_ij = exp(s_ij - lse_i), w = grad_scale.
+ * Sources (page title, section):
+ *   - "parameter-golf: ... Where Model Size Becomes the Game", "The Baseline
+ *     Is a Map, Not the Destination": the step is logits = model(x);
+ *     loss = criterion(logits, y); loss.backward().
+ *   - "parameter-golf README", leaderboard row "Naive Baseline": tied
+ *     embeddings (the head's W is the input embedding table).
+ *   - "HYDRA Golf" site stack list ("fused softcapped CE kernel") and
+ *     "parameter-golf README" leaderboard row "PR1736 + PolarNS + MIN_LR +
+ *     SparseAttnGate + FusedCE + Warm-A TTT" ("fused softcapped CE").  The
+ *     pages give no softcap formula; the tanh form above is used.
+ *   - tproger news "OpenAI launched Parameter Golf", section "Rules and
+ *     metric": bits per byte on FineWeb validation (bytes, not tokens).
+ *   - "parameter-golf README", leaderboard row "Sliding Window Eval": stride
+ *     64 sliding-window scoring, expressed here as a row mask.
+ *   - "HYDRA Golf" site stack list: per-group int4 head ("LQER asymmetric
+ *     int4, per-group compression"); this library reads it as symmetric,
+ *     group 64 along d, fp16 scales.
+ *
+ * Conventions for every entry point:
+ *   - All pointers are DEVICE pointers unless a comment says host.  The caller
+ *     owns every buffer; the library allocates nothing.
+ *   - bf16 arrays are passed as uint16_t bit patterns (lmce_bf16).
+ *   - h is [N, d] row-major with row stride ldh elements; W is [V, d]
+ *     row-major (stride d).  Base addresses and row strides must be 16-byte
+ *     aligned (ldh % 8 == 0).  d must be a multiple of 64 with d <= 512.
+ *     N and V are arbitrary (>= 1); tails are handled inside the kernels.
+ *   - targets are int64 in [0, V) on every unmasked row.
+ *   - row_mask (nullable) is [N] uint8: 0 = row not scored (nll = 0, lse = 0,
+ *     dh row = 0, no contribution to dW or the bpb sums).
+ *   - ws is a device workspace of at least lmce_workspace_bytes(...) bytes,
+ *     16-byte aligned, zero-filled once by the caller (or by
+ *     lmce_workspace_init) before its first use.  It carries a sticky device
+ *     status word; concurrent calls must use distinct workspaces.
+ *   - stream is a cudaStream_t (passed as void*; NULL = default stream).  All
+ *     work is asynchronous on it; only lmce_status synchronises.
+ *   - Return values: LMCE_OK, or an error detected on the host before any
+ *     launch (nothing was enqueued), or LMCE_ECUDA for a launch failure.
+ *     Errors found by the kernels (a target out of range, a bounded wait that
+ *     expired) are reported later through lmce_status.
+ */
+#ifndef LMHEAD_CE_H_
+#define LMHEAD_CE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define LMCE_API __attribute__((visibility("default")))
+#else
+#define LMCE_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t lmce_bf16; /* bfloat16 bit pattern */
+typedef uint16_t lmce_f16;  /* IEEE binary16 bit pattern */
+
+enum lmce_status_code {
+  LMCE_OK = 0,
+  LMCE_EINVAL = 1,   /* null pointer, bad shape or stride, misalignment, N or V < 1, short workspace */
+  LMCE_ENOTSUP = 2,  /* d not a multiple of 64 or > 512, softcap outside (0, lmce_softcap_max(V)], no sm_103 device */
+  LMCE_ECUDA = 3,    /* CUDA runtime / launch failure; text via lmce_last_cuda_error() */
+  LMCE_EDATA = 4,    /* device-detected: target outside [0, V) on a scored row; or sum of bytes == 0 */
+  LMCE_ETIMEOUT = 5  /* device-detected: a bounded in-kernel wait expired (the kernel returned early) */
+};
+
+/* Workspace flags. */
+#define LMCE_WS_MASKED 1u /* room for row-mask compaction (masked forward) */
+#define LMCE_WS_INT4 2u   /* room for the dequantised bf16 copy of an int4 head */
+
+/* Accumulator of the bits-per-byte sums (device memory for bpb_reduce). */
+typedef struct lmce_bpb_acc {
+  double sum_nll;      /* sum of nll over scored rows (nats) */
+  long long sum_bytes; /* sum of bytes over scored rows */
+  long long n_scored;  /* number of scored rows */
+} lmce_bpb_acc;
+
+/* Bytes of workspace needed for problems of up to N rows, V vocab, d dims,
+ * for the uses named in flags (LMCE_WS_*). */
+LMCE_API size_t lmce_workspace_bytes(int64_t N, int64_t V, int64_t d, unsigned flags);
+
+/* Zero the workspace's status word (asynchronous on stream). */
+LMCE_API int lmce_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/* Largest accepted softcap for vocab V.  The kernels sum e^s without a
+ * running maximum (|s| < c bounds every term), which is exact in fp32 range
+ * while V e^c stays finite and e^-c stays normal. */
+LMCE_API float lmce_softcap_max(int64_t V);
+
+/* Forward.  Defining passages: see the header comment (tied head, tanh
+ * softcap, log-sum-exp, next-token NLL).
+ * Inputs: h [N, d] bf16 (row stride ldh), W [V, d] bf16, tgt [N] int64,
+ * row_mask [N] uint8 or NULL, softcap c.
+ * Outputs: nll [N] fp32; lse [N] fp32 or NULL (needed by the backward).
+ * With a row mask only the scored rows are computed (they are compacted into
+ * the workspace first); requires a workspace sized with LMCE_WS_MASKED. */
+LMCE_API int lmhead_ce_fwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+                  const int64_t* tgt, const uint8_t* row_mask, float softcap, float* nll, float* lse, void* ws,
+                  size_t ws_bytes, void* stream);
+
+/* Backward of L = grad_scale * sum over scored rows of nll_i.
+ * Inputs as lmhead_ce_fwd plus lse [N] fp32 from the forward.
+ * Outputs (each nullable, at least one non-NULL):
+ *   dh [N, d] bf16 (row stride ldh), overwritten; masked rows get 0.
+ *   dW [V, d] fp32: accumulate_dW != 0 adds into it, else overwrites.
+ * grad_scale: dL/dnll of each scored row (1/M for a mean over M rows). */
+LMCE_API int lmhead_ce_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+                  const int64_t* tgt, const uint8_t* row_mask, float softcap, const float* lse, float grad_scale,
+                  lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes, void* stream);
+
+/* Forward with the head stored as per-group int4 (symmetric, two's-complement
+ * nibbles; element 2m of a row in the low nibble of byte m) with one fp16
+ * scale per group of `group` elements along d.  Wq [V, d/2] uint8, scales
+ * [V, d/group] fp16.  The head is dequantised on the device into the
+ * workspace (W_deq = bf16_rne(q * scale), bit-exact) and the bf16 forward
+ * runs on it.  Needs a workspace sized with LMCE_WS_INT4 (| LMCE_WS_MASKED
+ * with a row mask).  group must divide d and be a multiple of 16. */
+LMCE_API int lmhead_ce_fwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
+                       int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
+                       float* nll, float* lse, void* ws, size_t ws_bytes, void* stream);
+
+/* Backward for the int4 head: dh only (the quantised head is frozen).
+ * Same layout rules as lmhead_ce_fwd_int4 and lmhead_ce_bwd. */
+LMCE_API int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
+                       int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
+                       const float* lse, float grad_scale, lmce_bf16* dh, void* ws, size_t ws_bytes, void* stream);
+
+/* Bits-per-byte sums (tproger news, "Rules and metric").  Adds, over rows with
+ * row_mask != 0 (all rows if NULL), sum nll (fp64), sum bytes and the row
+ * count into *acc (device memory).  Deterministic: fixed grid, fixed
+ * summation tree, one ordered update of *acc. */
+LMCE_API int bpb_reduce(const float* nll, const int32_t* bytes, const uint8_t* row_mask, int64_t N, lmce_bpb_acc* acc,
+               void* ws, size_t ws_bytes, void* stream);
+
+/* Host helper: *bpb_out = acc->sum_nll / (ln 2 * acc->sum_bytes).  acc is a
+ * HOST copy.  Returns LMCE_EDATA when sum_bytes == 0. */
+LMCE_API int lmce_bpb(const lmce_bpb_acc* acc, double* bpb_out);
+
+/* Dequantise an int4 head into out [V, d] bf16 (the same device routine the
+ * int4 entry points use; exposed for bit-exactness tests). */
+LMCE_API int lmhead_int4_dequant(const uint8_t* Wq, const lmce_f16* scales, int64_t V, int64_t d, int group, lmce_bf16* out,
+                        void* stream);
+
+/* Synchronise stream, then read and clear the workspace's device status
+ * word.  *code receives LMCE_OK, LMCE_EDATA or LMCE_ETIMEOUT (the most
+ * severe recorded).  Returns LMCE_ECUDA if the synchronisation fails. */
+LMCE_API int lmce_status(void* ws, void* stream, int* code);
+
+/* Text of the last CUDA error seen by this library (thread-local). */
+LMCE_API const char* lmce_last_cuda_error(void);
+
+/* Short text for a status code. */
+LMCE_API const char* lmce_strerror(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LMHEAD_CE_H_ */

@@ -1,0 +1,426 @@
+// lmce_api.cu -- host side of the C ABI declared in include/lmhead_ce.h:
+// argument validation (every host-detectable error returns before any
+// launch), workspace layout, TMA tensor maps and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include "../../include/lmhead_ce.h"
+#include "aux_kernels.cuh"
+#include "bwd_kernel.cuh"
+#include "fwd_kernel.cuh"
+
+namespace {
+
+thread_local std::string g_last_err;
+
+int cuda_fail(cudaError_t e, const char* what) {
+  g_last_err = std::string(what) + ": " + cudaGetErrorString(e);
+  return LMCE_ECUDA;
+}
+
+constexpr size_t kAlign = 256;
+size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Workspace layout (byte offsets).  Every sub-buffer is 256-byte aligned.
+struct Layout {
+  size_t status = 0;    // unsigned status word (sticky until lmce_status)
+  size_t bpb = 0;       // kBpbBlocks partials
+  size_t part = 0;      // forward: [2 VT][N_pad] fp32 partial sums
+  size_t st = 0;        // forward: [N_pad] fp32 target logits
+  size_t blkcnt = 0;    // masked: per-block counts / offsets
+  size_t nscored = 0;   // masked: live row count
+  size_t idx = 0;       // masked: [N] int32 compacted -> original row
+  size_t tgt_c = 0;     // masked: [N] int64 compacted targets
+  size_t h_c = 0;       // masked: [N, d] bf16 compacted rows
+  size_t wdeq = 0;      // int4: [V, d] bf16 dequantised head
+  size_t bwd = 0;       // backward scratch
+  size_t total = 0;
+};
+
+Layout make_layout(int64_t N, int64_t V, int64_t d, unsigned flags) {
+  Layout L;
+  size_t o = 0;
+  L.status = o;
+  o = up(o + 64);
+  L.bpb = o;
+  o = up(o + sizeof(lmce::BpbPartial) * lmce::kBpbBlocks);
+  const int64_t N_pad = cdiv(N, lmce::fwdk::BM) * lmce::fwdk::BM;
+  const int64_t VT = cdiv(V, lmce::fwdk::BN);
+  L.part = o;
+  o = up(o + sizeof(float) * 2 * VT * N_pad);
+  L.st = o;
+  o = up(o + sizeof(float) * N_pad);
+  if (flags & LMCE_WS_MASKED) {
+    L.blkcnt = o;
+    o = up(o + sizeof(int) * cdiv(N, lmce::kCompactRows));
+    L.nscored = o;
+    o = up(o + sizeof(int));
+    L.idx = o;
+    o = up(o + sizeof(int) * N);
+    L.tgt_c = o;
+    o = up(o + sizeof(int64_t) * N);
+    L.h_c = o;
+    o = up(o + 2 * N * d);
+  }
+  if (flags & LMCE_WS_INT4) {
+    L.wdeq = o;
+    o = up(o + 2 * V * d);
+  }
+  L.bwd = o;
+  o = up(o + lmce::bwdk::scratch_bytes(N, V, d));
+  L.total = o;
+  return L;
+}
+
+struct DevInfo {
+  int dev = 0;
+  int sms = 0;
+};
+
+// Per-device one-time set-up: SM count, architecture check, kernel
+// attributes.  Thread-safe.
+int dev_info(DevInfo* out) {
+  static std::mutex mu;
+  static bool ready[64] = {};
+  static int sms[64] = {};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= 64) return LMCE_ENOTSUP;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ready[dev]) {
+    int major = 0, minor = 0, n = 0;
+    if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if ((e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+      return cuda_fail(e, "cudaDeviceGetAttribute");
+    if (major != 10 || minor != 3) {
+      g_last_err = "device is not sm_103 (compute capability 10.3)";
+      return LMCE_ENOTSUP;
+    }
+    if ((e = cudaFuncSetAttribute(lmce::fwdk::fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  lmce::fwdk::SMEM_BYTES)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
+    if (int rc = lmce::bwdk::setup_attributes(); rc != 0) return rc;
+    sms[dev] = n;
+    ready[dev] = true;
+  }
+  out->dev = dev;
+  out->sms = sms[dev];
+  return LMCE_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+}  // namespace
+
+namespace lmce {
+
+// 2-D bf16 tensor map over a row-major [outer, inner] array with row pitch
+// `pitch_bytes`, box = box_inner x box_outer elements, 128-byte swizzle,
+// out-of-bounds elements read as zero.
+int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+                  uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) {
+    g_last_err = "cuTensorMapEncodeTiled unavailable";
+    return LMCE_ECUDA;
+  }
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_err = "cuTensorMapEncodeTiled failed with CUresult " + std::to_string(static_cast<int>(r));
+    return LMCE_ECUDA;
+  }
+  return LMCE_OK;
+}
+
+void set_last_error(const std::string& s) { g_last_err = s; }
+
+}  // namespace lmce
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+float softcap_max(int64_t V) {
+  // e^{-c} must stay a normal float (c < 87.3) and V e^{c} finite (c + ln V < 88.7);
+  // keep a margin of 2 on both.
+  const double a = 85.0;
+  const double b = 86.0 - std::log(static_cast<double>(V));
+  return static_cast<float>(a < b ? a : b);
+}
+
+// Shared shape / pointer checks of the forward and backward.
+int check_common(const void* h, int64_t ldh, const void* W, int64_t N, int64_t V, int64_t d, const int64_t* tgt,
+                 float softcap, void* ws) {
+  if (!h || !W || !tgt || !ws) return LMCE_EINVAL;
+  if (N < 1 || V < 1 || d < 1) return LMCE_EINVAL;
+  if (N > (int64_t(1) << 30) || V > (int64_t(1) << 30)) return LMCE_EINVAL;
+  if (d % 64 != 0 || d > 512) return LMCE_ENOTSUP;
+  if (ldh < d || ldh % 8 != 0) return LMCE_EINVAL;
+  if (!aligned16(h) || !aligned16(W) || !aligned16(ws)) return LMCE_EINVAL;
+  if (!(softcap > 0.0f) || !(softcap <= softcap_max(V))) return LMCE_ENOTSUP;
+  return LMCE_OK;
+}
+
+int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+             const int64_t* tgt, const uint8_t* mask, float c, float* nll, float* lse, void* ws, size_t ws_bytes,
+             void* stream, unsigned extra_flags) {
+  if (int rc = check_common(h, ldh, W, N, V, d, tgt, c, ws); rc) return rc;
+  if (!nll) return LMCE_EINVAL;
+  const Layout L = make_layout(N, V, d, (mask ? LMCE_WS_MASKED : 0u) | extra_flags);
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  unsigned* status = reinterpret_cast<unsigned*>(w + L.status);
+
+  const lmce_bf16* hx = h;
+  int64_t ldx = ldh;
+  const int* nrows_dev = nullptr;
+  const int* idx = nullptr;
+  const int64_t* tg = tgt;
+  if (mask) {
+    const int nblk = static_cast<int>(cdiv(N, lmce::kCompactRows));
+    int* blkcnt = reinterpret_cast<int*>(w + L.blkcnt);
+    int* nsc = reinterpret_cast<int*>(w + L.nscored);
+    int* idxp = reinterpret_cast<int*>(w + L.idx);
+    int64_t* tgc = reinterpret_cast<int64_t*>(w + L.tgt_c);
+    lmce_bf16* hc = reinterpret_cast<lmce_bf16*>(w + L.h_c);
+    lmce::compact_count_kernel<<<nblk, lmce::kCompactThreads, 0, s>>>(mask, static_cast<int>(N), blkcnt);
+    lmce::compact_scan_kernel<<<1, lmce::kCompactThreads, 0, s>>>(blkcnt, nblk, nsc);
+    lmce::compact_write_kernel<<<nblk, lmce::kCompactThreads, 0, s>>>(mask, static_cast<int>(N), blkcnt, tgt, idxp,
+                                                                      tgc, nll, lse);
+    const int vec = static_cast<int>(d / 8);
+    const int gblocks = static_cast<int>(std::min<int64_t>(cdiv(N * vec, 256), int64_t(di.sms) * 8));
+    lmce::gather_rows_kernel<<<gblocks, 256, 0, s>>>(reinterpret_cast<const uint4*>(h), ldh / 8, idxp, nsc, vec,
+                                                     reinterpret_cast<uint4*>(hc));
+    hx = hc;
+    ldx = d;
+    nrows_dev = nsc;
+    idx = idxp;
+    tg = tgc;
+  }
+
+  CUtensorMap tm_h, tm_w;
+  if (int rc = lmce::make_map_bf16(&tm_h, hx, d, N, ldx * 2, lmce::fwdk::KB, lmce::fwdk::BM); rc) return rc;
+  if (int rc = lmce::make_map_bf16(&tm_w, W, d, V, d * 2, lmce::fwdk::KB, lmce::fwdk::BN); rc) return rc;
+
+  lmce::fwdk::Params p{};
+  p.N = static_cast<int>(N);
+  p.n_rows = nrows_dev;
+  p.V = static_cast<int>(V);
+  p.d = static_cast<int>(d);
+  p.KC = static_cast<int>(d / 64);
+  p.VT = static_cast<int>(cdiv(V, lmce::fwdk::BN));
+  p.N_pad = static_cast<int>(cdiv(N, lmce::fwdk::BM) * lmce::fwdk::BM);
+  p.tgt = tg;
+  p.inv_c = 1.0f / c;
+  p.c = c;
+  const float cl2e = c * lmce::kLog2e;
+  const float coef[6] = {lmce::kTanhC0, lmce::kTanhC1, lmce::kTanhC2, lmce::kTanhC3, lmce::kTanhC4, lmce::kTanhC5};
+  for (int i = 0; i < 6; ++i) p.k[i] = cl2e * coef[i];
+  p.part = reinterpret_cast<float*>(w + L.part);
+  p.st = reinterpret_cast<float*>(w + L.st);
+  p.status = status;
+
+  const int64_t T_max = cdiv(N, lmce::fwdk::BM) * p.VT;
+  const int grid = static_cast<int>(std::min<int64_t>(T_max, di.sms));
+  lmce::fwdk::fwd_kernel<<<grid, lmce::fwdk::THREADS, lmce::fwdk::SMEM_BYTES, s>>>(tm_h, tm_w, p);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "fwd_kernel launch");
+  const int fblocks = static_cast<int>(std::min<int64_t>(cdiv(N, 256), int64_t(di.sms) * 4));
+  lmce::fwd_finalize_kernel<<<fblocks, 256, 0, s>>>(p.part, 2 * p.VT, p.N_pad, p.st, tg, nrows_dev,
+                                                    static_cast<int>(N), static_cast<int>(V), idx, nll, lse, status);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "fwd_finalize launch");
+  return LMCE_OK;
+}
+
+int dequant_impl(const uint8_t* Wq, const lmce_f16* scales, int64_t V, int64_t d, int group, lmce_bf16* out,
+                 cudaStream_t s, int sms) {
+  const int64_t total = V * (d / 16);
+  const int blocks = static_cast<int>(std::min<int64_t>(cdiv(total, 256), int64_t(sms) * 8));
+  lmce::dequant_int4_kernel<<<blocks, 256, 0, s>>>(Wq, reinterpret_cast<const __half*>(scales),
+                                                   static_cast<int>(V), static_cast<int>(d), group,
+                                                   reinterpret_cast<__nv_bfloat16*>(out));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "dequant_int4 launch");
+  return LMCE_OK;
+}
+
+int check_int4(const uint8_t* Wq, const lmce_f16* scales, int group, int64_t V, int64_t d) {
+  if (!Wq || !scales) return LMCE_EINVAL;
+  if (V < 1 || d < 1) return LMCE_EINVAL;
+  if (group < 16 || group % 16 != 0 || d % group != 0) return LMCE_EINVAL;
+  if ((reinterpret_cast<uintptr_t>(Wq) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scales) & 1u) != 0)
+    return LMCE_EINVAL;
+  return LMCE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t lmce_workspace_bytes(int64_t N, int64_t V, int64_t d, unsigned flags) {
+  if (N < 1 || V < 1 || d < 1) return 0;
+  return make_layout(N, V, d, flags).total;
+}
+
+float lmce_softcap_max(int64_t V) { return V < 1 ? 0.0f : softcap_max(V); }
+
+int lmce_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < 64) return LMCE_EINVAL;
+  cudaError_t e = cudaMemsetAsync(ws, 0, 64, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return LMCE_OK;
+}
+
+int lmhead_ce_fwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+                  const int64_t* tgt, const uint8_t* row_mask, float softcap, float* nll, float* lse, void* ws,
+                  size_t ws_bytes, void* stream) {
+  return fwd_impl(h, ldh, W, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, 0u);
+}
+
+int lmhead_ce_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+                  const int64_t* tgt, const uint8_t* row_mask, float softcap, const float* lse, float grad_scale,
+                  lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes, void* stream) {
+  if (int rc = check_common(h, ldh, W, N, V, d, tgt, softcap, ws); rc) return rc;
+  if (!lse || (!dh && !dW)) return LMCE_EINVAL;
+  if (dh && !aligned16(dh)) return LMCE_EINVAL;
+  if (dW && !aligned16(dW)) return LMCE_EINVAL;
+  if (!std::isfinite(grad_scale)) return LMCE_EINVAL;
+  const Layout L = make_layout(N, V, d, row_mask ? LMCE_WS_MASKED : 0u);
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  char* w = static_cast<char*>(ws);
+  return lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, grad_scale, dh, dW, accumulate_dW,
+                            reinterpret_cast<unsigned*>(w + L.status), w + L.bwd, di.sms,
+                            static_cast<cudaStream_t>(stream));
+}
+
+int lmhead_ce_fwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
+                       int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
+                       float* nll, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  if (int rc = check_int4(Wq, scales, group, V, d); rc) return rc;
+  if (!ws || !aligned16(ws)) return LMCE_EINVAL;
+  const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_INT4 | (row_mask ? LMCE_WS_MASKED : 0u));
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  lmce_bf16* wdeq = reinterpret_cast<lmce_bf16*>(static_cast<char*>(ws) + L.wdeq);
+  if (int rc = check_common(h, ldh, wdeq, N, V, d, tgt, softcap, ws); rc) return rc;
+  if (!nll) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  if (int rc = dequant_impl(Wq, scales, V, d, group, wdeq, static_cast<cudaStream_t>(stream), di.sms); rc)
+    return rc;
+  return fwd_impl(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, LMCE_WS_INT4);
+}
+
+int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
+                       int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
+                       const float* lse, float grad_scale, lmce_bf16* dh, void* ws, size_t ws_bytes, void* stream) {
+  if (int rc = check_int4(Wq, scales, group, V, d); rc) return rc;
+  if (!ws || !aligned16(ws) || !dh) return LMCE_EINVAL;
+  const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_INT4 | (row_mask ? LMCE_WS_MASKED : 0u));
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  lmce_bf16* wdeq = reinterpret_cast<lmce_bf16*>(static_cast<char*>(ws) + L.wdeq);
+  if (int rc = check_common(h, ldh, wdeq, N, V, d, tgt, softcap, ws); rc) return rc;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  if (int rc = dequant_impl(Wq, scales, V, d, group, wdeq, static_cast<cudaStream_t>(stream), di.sms); rc)
+    return rc;
+  return lmhead_ce_bwd(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, lse, grad_scale, dh, nullptr, 0, ws,
+                       ws_bytes, stream);
+}
+
+int bpb_reduce(const float* nll, const int32_t* bytes, const uint8_t* row_mask, int64_t N, lmce_bpb_acc* acc,
+               void* ws, size_t ws_bytes, void* stream) {
+  if (!nll || !bytes || !acc || !ws || N < 1) return LMCE_EINVAL;
+  if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(acc) & 7u) != 0) return LMCE_EINVAL;
+  const Layout L = make_layout(1, 1, 64, 0u);
+  if (ws_bytes < L.bpb + sizeof(lmce::BpbPartial) * lmce::kBpbBlocks) return LMCE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  auto* part = reinterpret_cast<lmce::BpbPartial*>(static_cast<char*>(ws) + L.bpb);
+  lmce::bpb_partial_kernel<<<lmce::kBpbBlocks, lmce::kBpbThreads, 0, s>>>(nll, bytes, row_mask, N, part);
+  lmce::bpb_final_kernel<<<1, lmce::kBpbBlocks, 0, s>>>(part, reinterpret_cast<lmce::BpbPartial*>(acc));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bpb_reduce launch");
+  return LMCE_OK;
+}
+
+int lmce_bpb(const lmce_bpb_acc* acc, double* bpb_out) {
+  if (!acc || !bpb_out) return LMCE_EINVAL;
+  if (acc->sum_bytes == 0) return LMCE_EDATA;
+  *bpb_out = acc->sum_nll / (std::log(2.0) * static_cast<double>(acc->sum_bytes));
+  return LMCE_OK;
+}
+
+int lmhead_int4_dequant(const uint8_t* Wq, const lmce_f16* scales, int64_t V, int64_t d, int group, lmce_bf16* out,
+                        void* stream) {
+  if (int rc = check_int4(Wq, scales, group, V, d); rc) return rc;
+  if (!out || !aligned16(out)) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  return dequant_impl(Wq, scales, V, d, group, out, static_cast<cudaStream_t>(stream), di.sms);
+}
+
+int lmce_status(void* ws, void* stream, int* code) {
+  if (!ws || !code) return LMCE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  unsigned v = 0;
+  e = cudaMemcpy(&v, ws, sizeof v, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status)");
+  const unsigned zero = 0;
+  e = cudaMemcpy(ws, &zero, sizeof zero, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpy(status clear)");
+  *code = (v & lmce::ST_ETIMEOUT) ? LMCE_ETIMEOUT : (v & lmce::ST_EDATA) ? LMCE_EDATA : LMCE_OK;
+  return LMCE_OK;
+}
+
+const char* lmce_last_cuda_error(void) { return g_last_err.c_str(); }
+
+const char* lmce_strerror(int code) {
+  switch (code) {
+    case LMCE_OK: return "ok";
+    case LMCE_EINVAL: return "invalid argument";
+    case LMCE_ENOTSUP: return "unsupported shape, softcap or device";
+    case LMCE_ECUDA: return "CUDA error";
+    case LMCE_EDATA: return "invalid data (target out of range or no bytes)";
+    case LMCE_ETIMEOUT: return "device wait timed out";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"
