@@ -1,0 +1,368 @@
+#!/usr/bin/env python
+"""Benchmark of the fused tied-LM-head + softcapped cross-entropy path.
+
+One step = the whole hot path over one batch of the training-micro-batch
+workload (N = 65536 tokens = 32 x 2048, d = 512, V = 8192, softcap 30, Zipf
+targets, mean loss): forward (nll, lse) -> bits-per-byte reduction ->
+backward dh -> backward dW (fp32, accumulated).  Inputs are synthetic
+(seeded numpy PCG64, shaped like the pages' models) and resident in HBM when
+the timed region starts; L2 is flushed (a 256 MB write) between steps.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
+on its own GPU (weak scaling, no data-path collective); the time is the max
+over ranks.  --impl reference times the fp64 CPU oracle on the host cores on
+a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+CFG = 3
+SOFTCAP = 30.0
+WORKLOAD = "training micro-batch: N=65536 (32x2048) d=512 V=8192 softcap=30 Zipf(1.1) targets, mean loss, " \
+           "fwd + bpb_reduce + bwd dh + bwd dW (fp32 +=)"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------- helpers
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason sampling during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            m = json.load(f)
+        return float(m["bf16_tflops"]), float(m.get("bf16_tflops_sustained", m["bf16_tflops"])), \
+            float(m["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1800.0, 1400.0, 6400.0, "fallback"
+
+
+def flops_per_token(V, d):
+    """Algorithmic tensor FLOPs per token of each launch (2 per MAC)."""
+    return {"fwd": 2 * V * d,          # z = h W^T
+            "bwd_dh": 4 * V * d,       # z recomputed + dh = G W
+            "bwd_dW": 4 * V * d}       # z recomputed + dW = G^T h
+
+
+# ---------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import lm_head_softcapped_lmhead_b300 as lm
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    import synth_inputs as si
+
+    inp = si.make_inputs(CFG, seed=1000 + CFG + 7919 * rank)
+    N, V, d = inp["N"], inp["V"], inp["d"]
+    grad_scale = 1.0 / N
+    h_host = torch.from_numpy(inp["h"].view(np.int16)).view(torch.bfloat16).pin_memory()
+    t_host = torch.from_numpy(inp["tgt"]).pin_memory()
+    b_host = torch.from_numpy(inp["nbytes"]).pin_memory()
+    h = h_host.to(dev)
+    W = torch.from_numpy(inp["W"].view(np.int16)).view(torch.bfloat16).to(dev)
+    tgt = t_host.to(dev)
+    nbytes = b_host.to(dev)
+    ws = lm.workspace(N, V, d, device=dev)
+    nll = torch.empty(N, device=dev)
+    lse = torch.empty(N, device=dev)
+    dh = torch.empty_like(h)
+    dW = torch.zeros((V, d), device=dev)
+    acc = lm.bpb_acc(dev)
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(events=None):
+        ev = events or [None] * 5
+        if ev[0] is not None:
+            ev[0].record(stream)
+        lm.lmhead_ce_fwd(h, W, tgt, SOFTCAP, nll, lse, ws=ws, stream=stream)
+        if ev[1] is not None:
+            ev[1].record(stream)
+        lm.bpb_reduce(nll, nbytes, acc, ws=ws, stream=stream)
+        if ev[2] is not None:
+            ev[2].record(stream)
+        lm.lmhead_ce_bwd(h, W, tgt, SOFTCAP, lse, grad_scale, dh=dh, ws=ws, stream=stream)
+        if ev[3] is not None:
+            ev[3].record(stream)
+        lm.lmhead_ce_bwd(h, W, tgt, SOFTCAP, lse, grad_scale, dW=dW, accumulate_dW=True, ws=ws, stream=stream)
+        if ev[4] is not None:
+            ev[4].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+        flush.zero_()
+    torch.cuda.synchronize()
+    if lm.lmce_status(ws, stream) != lm.LMCE_OK:
+        raise RuntimeError("device status after warm-up is not OK")
+
+    sampler = ClockSampler(local_rank)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    launches0 = lm.lmce_launch_count()
+    t_wall0 = time.perf_counter()
+    for k in range(args.steps):
+        step(evs[k])
+        flush.zero_()
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall0
+    launches = lm.lmce_launch_count() - launches0
+    barrier()
+    clocks = sampler.stop()
+    if lm.lmce_status(ws, stream) != lm.LMCE_OK:
+        raise RuntimeError("device status after the timed steps is not OK")
+
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
+    part_ms = {"fwd": [e[0].elapsed_time(e[1]) for e in evs],
+               "bpb_reduce": [e[1].elapsed_time(e[2]) for e in evs],
+               "bwd_dh": [e[2].elapsed_time(e[3]) for e in evs],
+               "bwd_dW": [e[3].elapsed_time(e[4]) for e in evs]}
+    total_ms = sum(step_ms)
+
+    # ---- end to end through the public API with host buffers ----
+    h_in = torch.empty_like(h)
+    t_in = torch.empty_like(tgt)
+    b_in = torch.empty_like(nbytes)
+    acc_host = torch.empty(3, dtype=torch.float64).pin_memory()
+    h2d = h_host.numel() * 2 + t_host.numel() * 8 + b_host.numel() * 4
+    d2h = acc_host.numel() * 8
+
+    def e2e_step():
+        h_in.copy_(h_host, non_blocking=True)
+        t_in.copy_(t_host, non_blocking=True)
+        b_in.copy_(b_host, non_blocking=True)
+        lm.lmhead_ce_fwd(h_in, W, t_in, SOFTCAP, nll, lse, ws=ws, stream=stream)
+        lm.bpb_reduce(nll, b_in, acc, ws=ws, stream=stream)
+        lm.lmhead_ce_bwd(h_in, W, t_in, SOFTCAP, lse, grad_scale, dh=dh, dW=dW, accumulate_dW=True, ws=ws,
+                         stream=stream)
+        acc_host.copy_(acc, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e_ms = []
+    for _ in range(max(3, args.steps // 2)):
+        flush.zero_()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        e_ms.append(e0.elapsed_time(e1))
+    e2e_total_ms = sum(e_ms)
+
+    # ---- max over ranks ----
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms, e2e_total_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms, e2e_total_ms = float(tt[0]), float(tt[1])
+    if rank != 0:
+        return None
+
+    tokens = N * world * args.steps
+    value = tokens / (total_ms / 1e3)
+    e2e_value = N * world * len(e_ms) / (e2e_total_ms / 1e3)
+    peak_burst, peak_sust, hbm, peak_src = measured_peaks()
+    fpt = flops_per_token(V, d)
+    avg = {k: statistics.mean(v) for k, v in part_ms.items()}
+    dom = max(("fwd", "bwd_dh", "bwd_dW"), key=lambda k: avg[k])
+    achieved = fpt[dom] * N / (avg[dom] / 1e3) / 1e12
+    ms_step = total_ms / args.steps
+    model_flops = 6 * V * d * N
+    exec_flops = 8 * V * d * N
+    line = {
+        "metric": "tokens/s for fused LM-head+softcapped CE fwd+bwd; % of bf16 tensor peak",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic (seeded PCG64; FineWeb-shaped: d=512, V=8192, seq 2048)",
+        "config": {"workload": WORKLOAD, "N": N, "V": V, "d": d, "softcap": SOFTCAP, "loss": "mean",
+                   "l2": "flushed between steps (256 MB write outside the timed events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_burst,
+                     "unit": "TFLOP/s", "frac": achieved / peak_burst, "peak_source": f"{peak_src} bf16 burst",
+                     "frac_of_sustained": achieved / peak_sust, "traffic": None,
+                     "flops_per_launch": fpt[dom] * N},
+        "kernels_ms": avg,
+        "mfu_6NVd": model_flops / (ms_step / 1e3) / 1e12 / peak_burst,
+        "tensor_frac_exec_8NVd": exec_flops / (ms_step / 1e3) / 1e12 / peak_burst,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_total_ms / len(e_ms)},
+        "gpu_launches": launches,
+        "clocks": clocks,
+        "wall_s_timed": t_wall,
+    }
+    return line
+
+
+# ---------------------------------------------------------------- oracle arm
+def oracle_sample_time(target_s: float):
+    """Times the fp64 CPU oracle on a bounded sample of the workload: the first
+    S rows of the same inputs, forward + bpb + backward (dh and dW over those
+    rows).  Returns (tokens/s, S, seconds, threads)."""
+    import oracle
+    import synth_inputs as si
+
+    inp = si.make_inputs(CFG)
+    W = oracle.widen_bf16(inp["W"])
+
+    def run(S):
+        h = oracle.widen_bf16(inp["h"][:S])
+        t = inp["tgt"][:S]
+        t0 = time.perf_counter()
+        nll, lse = oracle.fwd(h, W, t, SOFTCAP)
+        oracle.bpb(nll, inp["nbytes"][:S])
+        oracle.bwd(h, W, t, SOFTCAP, lse, 1.0 / inp["N"])
+        return time.perf_counter() - t0
+
+    probe = 16
+    tp = run(probe)
+    S = int(max(16, min(8192, probe * target_s / max(tp, 1e-3))))
+    ts = run(S)
+    return S / ts, S, ts, oracle.num_threads()
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    import oracle
+    oracle.build()
+    per_step = max(1.0, min(20.0, 150.0 / max(1, args.steps + args.warmup)))
+    rates = []
+    info = None
+    for k in range(args.warmup + args.steps):
+        r, S, ts, thr = oracle_sample_time(per_step)
+        if k >= args.warmup:
+            rates.append(r)
+            info = (S, ts, thr)
+    value = statistics.mean(rates)
+    S, ts, thr = info
+    sample = f"first {S} rows of the N=65536 batch per step (fwd + bpb + bwd dh, dW over those rows), fp64"
+    return {
+        "impl": "reference",
+        "metric": "tokens/s for fused LM-head+softcapped CE fwd+bwd; % of bf16 tensor peak",
+        "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": S / value * 1e3, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "f64", "data": "synthetic (seeded PCG64)",
+        "config": {"workload": WORKLOAD, "N": 65536, "V": 8192, "d": 512, "softcap": SOFTCAP},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": thr, "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse()
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if args.impl == "reference":
+        # The oracle needs no GPU and no process group: rank 0 alone works.
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    line = run_ours(args, rank, world, local_rank)
+    if line is not None and rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            r, S, ts, thr = oracle_sample_time(args.cpu_seconds)
+            line["cpu_baseline"] = {"value": r, "unit": "tokens/s", "cores": thr, "kind": "oracle",
+                                    "sample": f"first {S} rows of the batch: fwd + bpb + bwd (dh, dW), fp64, "
+                                              f"{ts:.1f} s"}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -163,6 +163,10 @@ LMCE_API int lmce_status(void* ws, void* stream, int* code);
 /* Text of the last CUDA error seen by this library (thread-local). */
 LMCE_API const char* lmce_last_cuda_error(void);
 
+/* Number of kernels this library has enqueued in this process so far (a
+ * diagnostic counter; monotonically increasing, thread-safe). */
+LMCE_API unsigned long long lmce_launch_count(void);
+
 /* Short text for a status code. */
 LMCE_API const char* lmce_strerror(int code);
 

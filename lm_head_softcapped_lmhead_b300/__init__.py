@@ -29,7 +29,7 @@ LMCE_WS_INT4 = 2
 EXPORTS = (
     "lmce_workspace_bytes", "lmce_workspace_init", "lmce_softcap_max", "lmhead_ce_fwd", "lmhead_ce_bwd",
     "lmhead_ce_fwd_int4", "lmhead_ce_bwd_int4", "bpb_reduce", "lmce_bpb", "lmhead_int4_dequant",
-    "lmce_status", "lmce_last_cuda_error", "lmce_strerror",
+    "lmce_status", "lmce_last_cuda_error", "lmce_strerror", "lmce_launch_count",
 )
 
 _lib = None
@@ -72,6 +72,7 @@ def lib():
             "lmce_status": ([P, P, ctypes.POINTER(ctypes.c_int)], I),
             "lmce_last_cuda_error": ([], ctypes.c_char_p),
             "lmce_strerror": ([I], ctypes.c_char_p),
+            "lmce_launch_count": ([], ctypes.c_ulonglong),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -87,6 +88,11 @@ def strerror(code: int) -> str:
 
 def last_cuda_error() -> str:
     return lib().lmce_last_cuda_error().decode()
+
+
+def lmce_launch_count() -> int:
+    """Kernels enqueued by the library so far in this process."""
+    return int(lib().lmce_launch_count())
 
 
 def _p(t):

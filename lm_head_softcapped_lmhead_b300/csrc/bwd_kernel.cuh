@@ -34,6 +34,7 @@ namespace lmce {
 int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
                   uint32_t box_inner, uint32_t box_outer);
 void set_last_error(const std::string& s);
+void count_launches(unsigned n);
 
 namespace bwdk {
 
@@ -675,6 +676,7 @@ inline int launch_mode(const CUtensorMap& tx, const CUtensorMap& ty, const Param
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  count_launches(1);
   cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_kernel<MODE>, tx, ty, p);
   if (e != cudaSuccess) {
     set_last_error(std::string("bwd_kernel launch: ") + cudaGetErrorString(e));
@@ -728,6 +730,7 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
     if (q.split > 1) {
       const long long n4 = V * d / 4;
       const int blocks = static_cast<int>(cdivll(n4, 256) < sms * 8 ? cdivll(n4, 256) : sms * 8);
+      count_launches(1);
       dw_split_reduce_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(scratch), q.split,
                                                     static_cast<long long>(q.V_pad) * d / 4, n4, w, accumulate,
                                                     reinterpret_cast<float4*>(dW));

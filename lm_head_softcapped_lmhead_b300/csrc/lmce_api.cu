@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <string>
 
@@ -19,6 +20,7 @@
 namespace {
 
 thread_local std::string g_last_err;
+std::atomic<unsigned long long> g_launches{0};
 
 int cuda_fail(cudaError_t e, const char* what) {
   g_last_err = std::string(what) + ": " + cudaGetErrorString(e);
@@ -163,6 +165,7 @@ int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
 }
 
 void set_last_error(const std::string& s) { g_last_err = s; }
+void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
 }  // namespace lmce
 
@@ -216,6 +219,7 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
     int* idxp = reinterpret_cast<int*>(w + L.idx);
     int64_t* tgc = reinterpret_cast<int64_t*>(w + L.tgt_c);
     lmce_bf16* hc = reinterpret_cast<lmce_bf16*>(w + L.h_c);
+    lmce::count_launches(4);
     lmce::compact_count_kernel<<<nblk, lmce::kCompactThreads, 0, s>>>(mask, static_cast<int>(N), blkcnt);
     lmce::compact_scan_kernel<<<1, lmce::kCompactThreads, 0, s>>>(blkcnt, nblk, nsc);
     lmce::compact_write_kernel<<<nblk, lmce::kCompactThreads, 0, s>>>(mask, static_cast<int>(N), blkcnt, tgt, idxp,
@@ -255,6 +259,7 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
 
   const int64_t T_max = cdiv(N, lmce::fwdk::BM) * p.VT;
   const int grid = static_cast<int>(std::min<int64_t>(T_max, di.sms));
+  lmce::count_launches(2);
   lmce::fwdk::fwd_kernel<<<grid, lmce::fwdk::THREADS, lmce::fwdk::SMEM_BYTES, s>>>(tm_h, tm_w, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fwd_kernel launch");
@@ -270,6 +275,7 @@ int dequant_impl(const uint8_t* Wq, const lmce_f16* scales, int64_t V, int64_t d
                  cudaStream_t s, int sms) {
   const int64_t total = V * (d / 16);
   const int blocks = static_cast<int>(std::min<int64_t>(cdiv(total, 256), int64_t(sms) * 8));
+  lmce::count_launches(1);
   lmce::dequant_int4_kernel<<<blocks, 256, 0, s>>>(Wq, reinterpret_cast<const __half*>(scales),
                                                    static_cast<int>(V), static_cast<int>(d), group,
                                                    reinterpret_cast<__nv_bfloat16*>(out));
@@ -371,6 +377,7 @@ int bpb_reduce(const float* nll, const int32_t* bytes, const uint8_t* row_mask, 
   if (ws_bytes < L.bpb + sizeof(lmce::BpbPartial) * lmce::kBpbBlocks) return LMCE_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto* part = reinterpret_cast<lmce::BpbPartial*>(static_cast<char*>(ws) + L.bpb);
+  lmce::count_launches(2);
   lmce::bpb_partial_kernel<<<lmce::kBpbBlocks, lmce::kBpbThreads, 0, s>>>(nll, bytes, row_mask, N, part);
   lmce::bpb_final_kernel<<<1, lmce::kBpbBlocks, 0, s>>>(part, reinterpret_cast<lmce::BpbPartial*>(acc));
   cudaError_t e = cudaGetLastError();
@@ -410,6 +417,8 @@ int lmce_status(void* ws, void* stream, int* code) {
 }
 
 const char* lmce_last_cuda_error(void) { return g_last_err.c_str(); }
+
+unsigned long long lmce_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 const char* lmce_strerror(int code) {
   switch (code) {
