@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
+    ap.add_argument("--profile", action="store_true",
+                    help="for profiler captures: exactly W warm-up steps, no clock sampling, no e2e leg")
     return ap.parse_args()
 
 
@@ -169,18 +171,28 @@ def run_ours(args, rank, world, local_rank):
             import torch.distributed as dist
             dist.barrier()
 
-    for _ in range(max(args.warmup, 3)):
+    # Warm-up: at least W steps and at least ~1 s of load, so that the clock
+    # sampler (started before it) sees the GPU busy for a while.
+    sampler = ClockSampler(local_rank)
+    if not args.profile:
+        sampler.start()
+        time.sleep(0.3)
+    n_warm = 0
+    t_w0 = time.perf_counter()
+    min_warm_s = 0.0 if args.profile else 1.0
+    while n_warm < max(args.warmup, 3) or time.perf_counter() - t_w0 < min_warm_s:
         step()
         flush.zero_()
+        n_warm += 1
+        if n_warm % 16 == 0:
+            torch.cuda.synchronize()
     torch.cuda.synchronize()
     if lm.lmce_status(ws, stream) != lm.LMCE_OK:
         raise RuntimeError("device status after warm-up is not OK")
 
-    sampler = ClockSampler(local_rank)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
-    sampler.start()
     launches0 = lm.lmce_launch_count()
     t_wall0 = time.perf_counter()
     for k in range(args.steps):
@@ -201,6 +213,8 @@ def run_ours(args, rank, world, local_rank):
                "bwd_dW": [e[3].elapsed_time(e[4]) for e in evs]}
     total_ms = sum(step_ms)
 
+    if args.profile:
+        return None
     # ---- end to end through the public API with host buffers ----
     h_in = torch.empty_like(h)
     t_in = torch.empty_like(tgt)
@@ -258,6 +272,7 @@ def run_ours(args, rank, world, local_rank):
         "metric": "tokens/s for fused LM-head+softcapped CE fwd+bwd; % of bf16 tensor peak",
         "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps, "warmup": max(args.warmup, 3),
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "warmup_steps_run": n_warm,
         "dtype": "bf16", "data": "synthetic (seeded PCG64; FineWeb-shaped: d=512, V=8192, seq 2048)",
         "config": {"workload": WORKLOAD, "N": N, "V": V, "d": d, "softcap": SOFTCAP, "loss": "mean",
                    "l2": "flushed between steps (256 MB write outside the timed events)",
@@ -272,7 +287,7 @@ def run_ours(args, rank, world, local_rank):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_total_ms / len(e_ms)},
         "gpu_launches": launches,
-        "clocks": clocks,
+        "clocks": dict(clocks, window="sampled every 100 ms over the warm-up (>= 1 s) and the timed steps"),
         "wall_s_timed": t_wall,
     }
     return line

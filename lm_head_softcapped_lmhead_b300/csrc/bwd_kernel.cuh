@@ -31,8 +31,8 @@
 #include "softcap_math.cuh"
 
 namespace lmce {
-int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
-                  uint32_t box_inner, uint32_t box_outer);
+int make_map_bf16_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t rows, uint64_t pitch_bytes,
+                     uint32_t box_rows, uint32_t box_chunks);
 void set_last_error(const std::string& s);
 void count_launches(unsigned n);
 
@@ -44,19 +44,25 @@ constexpr int BM = 128;   // stationary block (TMEM lanes)
 constexpr int BT = 128;   // streamed tile (z columns; K of the accumulation)
 constexpr int KB = 64;    // K elements per chunk
 constexpr int MAX_KC = 8; // d <= 512
-constexpr int YSTAGES = 4;
+constexpr int YSTAGES = 3;  // Z ring: stages of two 64-column chunks (32 KB, one TMA load each)
 constexpr int EPI_WARPS = 8;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int THREADS = 320;
 constexpr uint32_t CHUNK = 128 * KB * 2;  // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t ZSTAGE = 2 * CHUNK;     // 32 KB
+// The A CTA loads its Y tile in 4 slabs of 32 rows x d (one TMA load per
+// slab, up to 32 KB); inside a slab the d / 64 chunks of 32 x 64 follow each
+// other (4 KB apart).
+constexpr int SLAB_ROWS = 32;
+constexpr int NSLAB = BT / SLAB_ROWS;
+constexpr uint32_t SLAB_CHUNK = SLAB_ROWS * KB * 2;  // 4 KB
 // Z CTA layout
 constexpr uint32_t Z_X = 0;
-constexpr uint32_t Z_Y = Z_X + MAX_KC * CHUNK;          // ring of YSTAGES chunks
-constexpr uint32_t Z_SIDE = Z_Y + YSTAGES * CHUNK;      // DW: per-warp row data (64 lse2 + 64 hit)
-constexpr uint32_t Z_END = Z_SIDE + 8 * 64 * 8;
+constexpr uint32_t Z_Y = Z_X + MAX_KC * CHUNK;          // ring of YSTAGES two-chunk stages
+constexpr uint32_t Z_END = Z_Y + YSTAGES * ZSTAGE;
 // A CTA layout
-constexpr uint32_t A_Y = 0;                             // one full Y tile: MAX_KC chunks
+constexpr uint32_t A_Y = 0;                             // one full Y tile: NSLAB slabs
 constexpr uint32_t A_P = A_Y + MAX_KC * CHUNK;          // 2 P slots of 128 x 128 bf16
 constexpr uint32_t P_SLOT = 2 * CHUNK;                  // 32 KB
 constexpr uint32_t A_END = A_P + 2 * P_SLOT;
@@ -76,7 +82,9 @@ struct Params {
   const int64_t* tgt;   // [N]
   const uint8_t* mask;  // [N] or null
   const float* lse;     // [N]
-  float inv_c, cl2e, w;
+  float inv_c, cl2e, w;  // w: the drain's scale (-grad_scale: the tiles hold -G)
+  float zlim2;
+  float q[kTanhTerms];  // -C_i / c^(2i+1)
   __nv_bfloat16* dh;    // DH output [N, ldh]
   long long ldh;
   float* dW;            // DW output [V, d]
@@ -86,105 +94,169 @@ struct Params {
   unsigned* status;
 };
 
-// Gradient for 32 columns of one lane-row.  DH: column = vocab, per-thread
-// lse2 / rel (target column relative to the chunk, or -1).  Writes 16 packed
-// bf16x2 words.  Columns >= lim are forced to 0.
+// The epilogue forms the NEGATED gradient tile, P = -G (or -G^T), because
+// with nth = -tanh(z/c) both exponent and derivative are one FFMA2 each:
+//   a = cl2e * tanh - lse2 = fma(nth, -cl2e, -lse2),  p = 2^a,
+//   w = tanh^2 - 1 = fma(nth, nth, -1) = -(1 - tanh^2),
+//   -G = (p - [j == t]) * w.
+// The drain multiplies the accumulator by -grad_scale.
+struct EpiConst {
+  float2 q[kTanhTerms];  // -C_i / c^(2i+1): z * Q(z^2) = -tanh(z/c)
+  float2 ncl2e;   // -c log2(e)
+  float2 m1;      // -1
+  float zlim2;    // (kTanhXmax c)^2
+  float inv_c, cl2e;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+
+// Slow path for chunks whose |z| may exceed the polynomial range: exact-form
+// tanh per element, same sign convention.  Kept out of line (arguments and
+// result by value) so the compiler branches to it instead of predicating it
+// into every chunk; only the call site copies the chunk to the stack.
+struct Chunk32 {
+  uint32_t v[32];
+};
+struct Packed16 {
+  uint32_t v[16];
+};
+struct SlowArgs {
+  float lse2_col[32];  // per-column lse2 (DW) -- unused when per_col == 0
+  int hit_col[32];     // per-column target lane (DW)
+};
+__device__ __noinline__ Packed16 g_chunk_slow(Chunk32 r, float inv_c, float cl2e, int per_col, SlowArgs cols,
+                                              float lse2_row, int rel, int my_lane, int lim) {
+  Packed16 out;
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    float g[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float th = tanh_any(__uint_as_float(r.v[j + e]) * inv_c);
+      const float l2 = per_col ? cols.lse2_col[j + e] : lse2_row;
+      float pp = ex2_approx(fmaf(th, cl2e, -l2));
+      const bool hit = per_col ? (cols.hit_col[j + e] == my_lane) : (j + e == rel);
+      if (hit) pp -= 1.0f;
+      g[e] = (j + e < lim) ? pp * fmaf(th, th, -1.0f) : 0.f;
+    }
+    out.v[j / 2] = pack_bf16x2(g[0], g[1]);
+  }
+  return out;
+}
+
+// DH mode: 32 vocab columns of this thread's row (lse2 = lse log2 e of the
+// row, rel = target column inside the chunk or -1, lim = valid columns).
 template <bool kHit>
-__device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], float inv_c, float cl2e, float lse2, int rel,
-                                           int lim, uint32_t (&out)[16]) {
-  float xmax = 0.f;
-  float g[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float x = __uint_as_float(r[j]) * inv_c;
-    xmax = fmaxf(xmax, fabsf(x));
-    const float th = tanh_poly(x);
-    const float p = ex2_approx(fmaf(th, cl2e, -lse2));
-    const float tau = fmaf(-th, th, 1.0f);
-    g[j] = (kHit && j == rel) ? (p - 1.0f) * tau : p * tau;
-  }
-  if (__any_sync(0xffffffffu, xmax > kTanhXmax)) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float x = __uint_as_float(r[j]) * inv_c;
-      const float th = tanh_any(x);
-      const float p = ex2_approx(fmaf(th, cl2e, -lse2));
-      const float tau = fmaf(-th, th, 1.0f);
-      g[j] = (j == rel) ? (p - 1.0f) * tau : p * tau;
-    }
-  }
-  if (lim < 32) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) g[j] = (j < lim) ? g[j] : 0.f;
-  }
+__device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiConst& k, float lse2, int rel, int lim,
+                                           uint32_t (&out)[16]) {
+  const float2 nl = make_float2(-lse2, -lse2);
+  float2 su = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    __nv_bfloat162 b = __floats2bfloat162_rn(g[2 * j], g[2 * j + 1]);
-    out[j] = *reinterpret_cast<uint32_t*>(&b);
+    const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    const float2 u = __fmul2_rn(z, z);
+    su = __fadd2_rn(su, u);
+    const float2 nth = poly_z2(z, u, k.q);
+    const float2 a = __ffma2_rn(nth, k.ncl2e, nl);
+    float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+    if (kHit) {
+      pp.x -= (2 * j == rel) ? 1.0f : 0.0f;
+      pp.y -= (2 * j + 1 == rel) ? 1.0f : 0.0f;
+    }
+    float2 g = __fmul2_rn(pp, __ffma2_rn(nth, nth, k.m1));
+    if (lim < 32) {
+      g.x = (2 * j < lim) ? g.x : 0.f;
+      g.y = (2 * j + 1 < lim) ? g.y : 0.f;
+    }
+    out[j] = pack_bf16x2(g.x, g.y);
+  }
+  if (__any_sync(0xffffffffu, !(su.x + su.y <= k.zlim2))) {
+    Chunk32 c;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c.v[j] = r[j];
+    SlowArgs none;
+    const Packed16 o = g_chunk_slow(c, k.inv_c, k.cl2e, 0, none, lse2, rel, -1, lim);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) out[j] = o.v[j];
   }
 }
 
-// DW: column = row i of the tile with lse2[i] and hit[i] (lane index of the
-// target inside this vocab block, or -1) from shared memory; lane = vocab.
-__device__ __forceinline__ void g_chunk_dw(const uint32_t (&r)[32], float inv_c, float cl2e, const float* lse2,
-                                           const int* hit, int my_lane, uint32_t (&out)[16]) {
-  float xmax = 0.f;
-  float g[32];
-#pragma unroll
-  for (int j = 0; j < 32; ++j) {
-    const float x = __uint_as_float(r[j]) * inv_c;
-    xmax = fmaxf(xmax, fabsf(x));
-    const float th = tanh_poly(x);
-    const float p = ex2_approx(fmaf(th, cl2e, -lse2[j]));
-    const float tau = fmaf(-th, th, 1.0f);
-    g[j] = (hit[j] == my_lane) ? (p - 1.0f) * tau : p * tau;
-  }
-  if (__any_sync(0xffffffffu, xmax > kTanhXmax)) {
-#pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      const float x = __uint_as_float(r[j]) * inv_c;
-      const float th = tanh_any(x);
-      const float p = ex2_approx(fmaf(th, cl2e, -lse2[j]));
-      const float tau = fmaf(-th, th, 1.0f);
-      g[j] = (hit[j] == my_lane) ? (p - 1.0f) * tau : p * tau;
-    }
-  }
+// DW mode: lane = vocab row of the block, 32 columns = rows of the tile.
+// Lane j holds, for column j of the chunk, -lse log2(e) (nl_col, -inf for rows
+// that do not count) and the block lane of that row's target (hit_col, -1 if
+// outside the block); every lane reads them with shuffles.
+template <bool kHit>
+__device__ __forceinline__ void g_chunk_dw(const uint32_t (&r)[32], const EpiConst& k, float nl_col, int hit_col,
+                                           int my_lane, uint32_t (&out)[16]) {
+  float2 su = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
-    __nv_bfloat162 b = __floats2bfloat162_rn(g[2 * j], g[2 * j + 1]);
-    out[j] = *reinterpret_cast<uint32_t*>(&b);
+    const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    const float2 u = __fmul2_rn(z, z);
+    su = __fadd2_rn(su, u);
+    const float2 nth = poly_z2(z, u, k.q);
+    const float2 nl = make_float2(__shfl_sync(0xffffffffu, nl_col, 2 * j), __shfl_sync(0xffffffffu, nl_col, 2 * j + 1));
+    const float2 a = __ffma2_rn(nth, k.ncl2e, nl);
+    float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+    if (kHit) {
+      pp.x -= (__shfl_sync(0xffffffffu, hit_col, 2 * j) == my_lane) ? 1.0f : 0.0f;
+      pp.y -= (__shfl_sync(0xffffffffu, hit_col, 2 * j + 1) == my_lane) ? 1.0f : 0.0f;
+    }
+    const float2 g = __fmul2_rn(pp, __ffma2_rn(nth, nth, k.m1));
+    out[j] = pack_bf16x2(g.x, g.y);
+  }
+  if (__any_sync(0xffffffffu, !(su.x + su.y <= k.zlim2))) {
+    Chunk32 c;
+    SlowArgs cols;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+      c.v[j] = r[j];
+      cols.lse2_col[j] = -__shfl_sync(0xffffffffu, nl_col, j);
+      cols.hit_col[j] = __shfl_sync(0xffffffffu, hit_col, j);
+    }
+    const Packed16 o = g_chunk_slow(c, k.inv_c, k.cl2e, 1, cols, 0.f, -1, my_lane, 32);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) out[j] = o.v[j];
   }
 }
 
-// Tile range of unit u: the stationary block and the streamed tiles.
+// Split-major order: clusters running at the same time share a row range
+// of the streamed operand, which then stays in L2.
 __device__ __forceinline__ void unit_range(const Params& p, int u, int& blk, int& t0, int& t1) {
-  blk = u / p.split;
-  const int s = u % p.split;
+  blk = u % p.n_blocks;
+  const int s = u / p.n_blocks;
   t0 = static_cast<int>(static_cast<long long>(s) * p.n_tiles / p.split);
   t1 = static_cast<int>(static_cast<long long>(s + 1) * p.n_tiles / p.split);
 }
 
 template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
-    bwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y, const Params p) {
+    bwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
+               const __grid_constant__ CUtensorMap tm_ys, const Params p) {
+  // tm_x: X blocks, box 64 x 128 x KC (the whole 128 x d block in one load);
+  // tm_y: Y tiles, box 64 x 128 x 2 (two chunks); tm_ys: Y slabs, box
+  // 64 x 32 x KC.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   // Z CTA barriers
   uint64_t* zy_full = bars + 0;     // [YSTAGES]
-  uint64_t* zy_empty = bars + 4;    // [YSTAGES]
-  uint64_t* x_full = bars + 8;
-  uint64_t* x_empty = bars + 9;
-  uint64_t* acc_full = bars + 10;   // [2]  Z: z tiles; A: [0] = accumulator done
-  uint64_t* acc_empty = bars + 12;  // [2]  Z: z tiles; A: [0] = accumulator drained
-  uint64_t* p_empty = bars + 14;    // [2]  in Z, arrived by A's MMA commit
+  uint64_t* zy_empty = bars + 6;    // [YSTAGES]
+  uint64_t* x_full = bars + 12;
+  uint64_t* x_empty = bars + 13;
+  uint64_t* acc_full = bars + 14;   // [2]  Z: z tiles; A: [0] = accumulator done
+  uint64_t* acc_empty = bars + 16;  // [2]  Z: z tiles; A: [0] = accumulator drained
+  uint64_t* p_empty = bars + 18;    // [2]  in Z, arrived by A's MMA commit
   // A CTA barriers
-  uint64_t* p_full = bars + 16;     // [2]  in A, arrived by Z's epilogue warps
-  uint64_t* ay_full = bars + 18;    // [2]  halves of the Y tile
-  uint64_t* ay_empty = bars + 20;   // [2]
-  uint64_t* mma_done = bars + 22;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 196);
+  uint64_t* p_full = bars + 20;     // [2]  in A: A's expect_tx + the bytes of Z's st.async
+  uint64_t* ay_full = bars + 22;    // [NSLAB] slabs of the Y tile
+  uint64_t* ay_empty = bars + 26;   // [NSLAB]
+  uint64_t* mma_done = bars + 30;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 248);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 252);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -204,7 +276,9 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(acc_full + i, 1);
       mbar_init(acc_empty + i, EPI_WARPS);
       mbar_init(p_empty + i, 1);
-      mbar_init(p_full + i, EPI_WARPS);
+      mbar_init(p_full + i, 1);
+    }
+    for (int i = 0; i < NSLAB; ++i) {
       mbar_init(ay_full + i, 1);
       mbar_init(ay_empty + i, 1);
     }
@@ -232,7 +306,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         int stage = 0;
         uint32_t phase = 0, xph = 0;
         bool first = true, ok = true;
-        uint32_t pend = 0, pend_ph[YSTAGES] = {0, 0, 0, 0};
+        uint32_t pend = 0, pend_ph[YSTAGES] = {0, 0, 0};
+        const int npair = (p.KC + 1) / 2;
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
@@ -243,13 +318,15 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           first = false;
           mbar_expect_tx(x_full, p.KC * CHUNK);
-          for (int kc = 0; kc < p.KC; ++kc) tma_load_2d(smem + Z_X + kc * CHUNK, &tm_x, x_full, kc * KB, blk * BM);
+          tma_load_3d(smem + Z_X, &tm_x, x_full, 0, blk * BM, 0);
           for (int t = t0; t < t1 && ok; ++t) {
-            for (int kc = 0; kc < p.KC; ++kc) {
+            for (int pr = 0; pr < npair; ++pr) {
               ok = mbar_wait(zy_empty + stage, phase ^ 1u, abort_flag, p.status);
               if (!ok) break;
-              mbar_expect_tx(zy_full + stage, CHUNK);
-              tma_load_2d(smem + Z_Y + stage * CHUNK, &tm_y, zy_full + stage, kc * KB, t * BT);
+              // A pair past an odd KC reads zeros for its second chunk; the
+              // load still delivers the full box.
+              mbar_expect_tx(zy_full + stage, ZSTAGE);
+              tma_load_3d(smem + Z_Y + stage * ZSTAGE, &tm_y, zy_full + stage, 0, t * BT, 2 * pr);
               pend |= 1u << stage;
               pend_ph[stage] = phase;
               if (++stage == YSTAGES) {
@@ -283,16 +360,20 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (!ok) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BT);
-            for (int kc = 0; kc < p.KC; ++kc) {
+            for (int pr = 0; pr < (p.KC + 1) / 2; ++pr) {
               ok = mbar_wait(zy_full + stage, phase, abort_flag, p.status);
               if (!ok) break;
               tc_fence_after();
-              const uint32_t xa = smem_u32(smem + Z_X + kc * CHUNK);
-              const uint32_t ya = smem_u32(smem + Z_Y + stage * CHUNK);
+              for (int c = 0; c < 2; ++c) {
+                const int kc = 2 * pr + c;
+                if (kc >= p.KC) break;
+                const uint32_t xa = smem_u32(smem + Z_X + kc * CHUNK);
+                const uint32_t ya = smem_u32(smem + Z_Y + stage * ZSTAGE + c * CHUNK);
 #pragma unroll
-              for (int k = 0; k < KB / 16; ++k)
-                umma_bf16(d_tmem, sdesc_sw128(xa + k * 32, 16, 1024), sdesc_sw128(ya + k * 32, 16, 1024), IDESC_Z,
-                          (kc | k) != 0 ? 1u : 0u);
+                for (int k = 0; k < KB / 16; ++k)
+                  umma_bf16(d_tmem, sdesc_sw128(xa + k * 32, 16, 1024), sdesc_sw128(ya + k * 32, 16, 1024), IDESC_Z,
+                            (kc | k) != 0 ? 1u : 0u);
+              }
               umma_commit(zy_empty + stage);
               if (++stage == YSTAGES) {
                 stage = 0;
@@ -316,9 +397,22 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int q = warp & 3;    // lanes 32q .. 32q+31
       const int hc = warp >> 2;  // columns 64hc .. 64hc+63 (one K chunk of P)
       const int m = q * 32 + lane;  // row of the P tile (= TMEM lane)
-      // DW: warp-private copy of the row data of its 64 columns.
-      float* side_lse = reinterpret_cast<float*>(smem + Z_SIDE) + warp * 128;
-      int* side_hit = reinterpret_cast<int*>(side_lse + 64);
+      EpiConst kc;
+#pragma unroll
+      for (int i = 0; i < kTanhTerms; ++i) kc.q[i] = make_float2(p.q[i], p.q[i]);
+      kc.ncl2e = make_float2(-p.cl2e, -p.cl2e);
+      kc.m1 = make_float2(-1.0f, -1.0f);
+      kc.zlim2 = p.zlim2;
+      kc.inv_c = p.inv_c;
+      kc.cl2e = p.cl2e;
+      const float kNegInf = __int_as_float(0xff800000);
+      // DW: row data of the warp's 64 columns (lane j holds columns j and
+      // 32 + j): -lse log2(e) (-inf for rows that do not count) and the block
+      // lane of the row's target.  pf_* is the next tile's, fetched early.
+      float cur_nl[2] = {kNegInf, kNegInf};
+      int cur_hit[2] = {-1, -1};
+      float pf_nl[2] = {kNegInf, kNegInf};
+      int pf_hit[2] = {-1, -1};
       const uint32_t peer_p = mapa_shared(smem_u32(smem + A_P), 1);
       const uint32_t peer_pfull = mapa_shared(smem_u32(p_full), 1);
       int acc = 0, slot = 0;
@@ -328,39 +422,50 @@ __global__ void __launch_bounds__(THREADS, 1)
         int blk, t0, t1;
         unit_range(p, u, blk, t0, t1);
         // DH: this thread's row data.
-        float lse2 = __int_as_float(0x7f800000);  // +inf: row contributes nothing
+        float nl_row = kNegInf;
         long long trow = -1;
         if (MODE == DH) {
           const int row = blk * BM + m;
           if (row < p.N && (!p.mask || p.mask[row])) {
             const long long tt = p.tgt[row];
-            lse2 = p.lse[row] * kLog2e;
+            nl_row = -p.lse[row] * kLog2e;
             if (tt >= 0 && tt < p.V) trow = tt;
             else atomicOr(p.status, ST_EDATA);
           }
         }
-        const int my_vocab_lane = m;  // DW: vocab index inside the block
+        const long long vbase = static_cast<long long>(blk) * BM;
+        // DW: row data of tile t is fetched into registers one tile ahead.
+        auto fetch_dw = [&](int t) {
+#pragma unroll
+          for (int k = 0; k < 2; ++k) {
+            const int row = t * BT + hc * 64 + k * 32 + lane;
+            float nl = kNegInf;
+            int hl = -1;
+            if (row < p.N) {
+              const uint8_t mk = p.mask ? p.mask[row] : uint8_t(1);
+              const long long tt = p.tgt[row];
+              const float l = p.lse[row];
+              if (mk) {
+                nl = -l * kLog2e;
+                if (tt < 0 || tt >= p.V) atomicOr(p.status, ST_EDATA);
+                else if (tt >= vbase && tt < vbase + BM) hl = static_cast<int>(tt - vbase);
+              }
+            }
+            pf_nl[k] = nl;
+            pf_hit[k] = hl;
+          }
+        };
+        if (MODE == DW && t0 < t1) fetch_dw(t0);
         for (int t = t0; t < t1; ++t) {
+          bool hit_any[2] = {false, false};
           if (MODE == DW) {
-            // Rows of this warp's 64 columns: lse * log2(e) and the lane
-            // (vocab inside the block) of their target, or -1.
 #pragma unroll
             for (int k = 0; k < 2; ++k) {
-              const int col = hc * 64 + k * 32 + lane;
-              const int row = t * BT + col;
-              float l2 = __int_as_float(0x7f800000);
-              int hl = -1;
-              if (row < p.N && (!p.mask || p.mask[row])) {
-                const long long tt = p.tgt[row];
-                l2 = p.lse[row] * kLog2e;
-                if (tt < 0 || tt >= p.V) atomicOr(p.status, ST_EDATA);
-                else if (tt >= static_cast<long long>(blk) * BM && tt < static_cast<long long>(blk) * BM + BM)
-                  hl = static_cast<int>(tt - static_cast<long long>(blk) * BM);
-              }
-              side_lse[k * 32 + lane] = l2;
-              side_hit[k * 32 + lane] = hl;
+              cur_nl[k] = pf_nl[k];
+              cur_hit[k] = pf_hit[k];
+              hit_any[k] = __any_sync(0xffffffffu, pf_hit[k] >= 0);
             }
-            __syncwarp();
+            if (t + 1 < t1) fetch_dw(t + 1);
           }
           ok = mbar_wait(acc_full + acc, aph, abort_flag, p.status);
           if (!ok) break;
@@ -370,41 +475,44 @@ __global__ void __launch_bounds__(THREADS, 1)
           const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BT + hc * 64);
           const uint32_t dst_row = peer_p + static_cast<uint32_t>(slot) * P_SLOT + static_cast<uint32_t>(hc) * CHUNK +
                                    static_cast<uint32_t>(m) * 128u;
-#pragma unroll 1
-          for (int ch = 0; ch < 2; ++ch) {
-            uint32_t r[32];
-            tmem_ld32(tb + ch * 32, r);
-            tmem_ld_wait();
-            reg_fence32(r);
+          const uint32_t pfull_slot = peer_pfull + static_cast<uint32_t>(slot) * 8u;
+          // One 32-column chunk: gradient, pack, four swizzled 16-byte DSMEM stores.
+          auto do_chunk = [&](const uint32_t (&r)[32], int ch) {
             uint32_t packed[16];
-            const int c0 = hc * 64 + ch * 32;  // column inside the tile
             if (MODE == DH) {
-              const int cbase = t * BT + c0;   // vocab index
+              const int cbase = t * BT + hc * 64 + ch * 32;  // vocab index
               const int lim = min(32, p.V - cbase);
               const long long relw = trow - cbase;
               const int rel = (relw >= 0 && relw < 32) ? static_cast<int>(relw) : -1;
               if (__any_sync(0xffffffffu, rel >= 0))
-                g_chunk_dh<true>(r, p.inv_c, p.cl2e, lse2, rel, lim, packed);
+                g_chunk_dh<true>(r, kc, -nl_row, rel, lim, packed);
               else
-                g_chunk_dh<false>(r, p.inv_c, p.cl2e, lse2, -1, lim, packed);
+                g_chunk_dh<false>(r, kc, -nl_row, -1, lim, packed);
             } else {
-              g_chunk_dw(r, p.inv_c, p.cl2e, side_lse + ch * 32, side_hit + ch * 32, my_vocab_lane, packed);
+              if (hit_any[ch])
+                g_chunk_dw<true>(r, kc, cur_nl[ch], cur_hit[ch], m, packed);
+              else
+                g_chunk_dw<false>(r, kc, cur_nl[ch], cur_hit[ch], m, packed);
             }
-            // 4 x 16-byte units of this 32-column chunk, 128B-swizzled.
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
               const uint32_t unit = static_cast<uint32_t>(ch * 4 + v);
               const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
-              st_cluster_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+              st_async_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3], pfull_slot);
             }
-          }
+          };
+          uint32_t ra[32], rc[32];
+          tmem_ld32(tb, ra);
+          tmem_ld_wait();
+          reg_fence32(ra);
+          tmem_ld32(tb + 32, rc);  // in flight while chunk 0 is processed
+          do_chunk(ra, 0);
+          tmem_ld_wait();
+          reg_fence32(rc);
+          do_chunk(rc, 1);
           tc_fence_before();
-          fence_proxy_async_cluster();
           __syncwarp();
-          if (lane == 0) {
-            mbar_arrive(acc_empty + acc);
-            mbar_arrive_cluster(peer_pfull + static_cast<uint32_t>(slot) * 8u);
-          }
+          if (lane == 0) mbar_arrive(acc_empty + acc);
           acc ^= 1;
           if (acc == 0) aph ^= 1u;
           slot ^= 1;
@@ -416,30 +524,28 @@ __global__ void __launch_bounds__(THREADS, 1)
     // =========================== A CTA ===========================
     if (warp == TMA_WARP) {
       if (lane == 0) {
-        uint32_t yph = 0;  // shared by both halves: each completes once per tile
+        // The Y tile arrives in NSLAB slabs of 32 rows x d, one load each.
+        uint32_t yph = 0;
         bool ok = true;
-        uint32_t pend = 0, pend_ph[2] = {0, 0};
+        uint32_t pend = 0, pend_ph[NSLAB] = {0, 0, 0, 0};
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
           for (int t = t0; t < t1 && ok; ++t) {
-            for (int half = 0; half < 2 && ok; ++half) {
-              const int kc0 = half == 0 ? 0 : (p.KC + 1) / 2;
-              const int kc1 = half == 0 ? (p.KC + 1) / 2 : p.KC;
-              if (kc1 == kc0) continue;
-              ok = mbar_wait(ay_empty + half, yph ^ 1u, abort_flag, p.status);
+            for (int sl = 0; sl < NSLAB; ++sl) {
+              ok = mbar_wait(ay_empty + sl, yph ^ 1u, abort_flag, p.status);
               if (!ok) break;
-              mbar_expect_tx(ay_full + half, (kc1 - kc0) * CHUNK);
-              for (int kc = kc0; kc < kc1; ++kc) tma_load_2d(smem + A_Y + kc * CHUNK, &tm_y, ay_full + half, kc * KB, t * BT);
-              pend |= 1u << half;
-              pend_ph[half] = yph;
+              mbar_expect_tx(ay_full + sl, p.KC * SLAB_CHUNK);
+              tma_load_3d(smem + A_Y + sl * p.KC * SLAB_CHUNK, &tm_ys, ay_full + sl, 0, t * BT + sl * SLAB_ROWS, 0);
+              pend |= 1u << sl;
+              pend_ph[sl] = yph;
             }
             yph ^= 1u;
           }
         }
         if (!ok) {
           const unsigned long long t0 = globaltimer_ns();
-          for (int s = 0; s < 2; ++s)
+          for (int s = 0; s < NSLAB; ++s)
             if (pend & (1u << s))
               while (!mbar_try_wait(smem_u32(ay_full + s), pend_ph[s]) && globaltimer_ns() - t0 < kWaitLimitNs) {
               }
@@ -453,6 +559,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         // The accumulator's d columns in two N halves of nh0 and nh1 chunks.
         const int nh0 = (p.KC + 1) / 2;
         const int nh1 = p.KC - nh0;
+        // Each P slot completes when all its bytes (st.async from the Z CTA)
+        // have landed: arm both slots for their first use.
+        mbar_expect_tx(p_full + 0, P_SLOT);
+        mbar_expect_tx(p_full + 1, P_SLOT);
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
@@ -463,25 +573,30 @@ __global__ void __launch_bounds__(THREADS, 1)
           for (int t = t0; t < t1 && ok; ++t) {
             ok = mbar_wait<true>(p_full + slot, sph, abort_flag, p.status);
             if (!ok) break;
-            tc_fence_after();
+            mbar_expect_tx(p_full + slot, P_SLOT);  // arm the slot's next use
             fence_proxy_async_smem();
+            tc_fence_after();
             const uint32_t pa = smem_u32(smem + A_P + slot * P_SLOT);
-            for (int half = 0; half < 2; ++half) {
-              const int nh = half == 0 ? nh0 : nh1;
-              if (nh == 0) continue;
-              ok = mbar_wait(ay_full + half, yph, abort_flag, p.status);
-              if (!ok) break;
-              tc_fence_after();
-              const uint32_t idesc = idesc_bf16_f32(128, 64 * nh, false, true);
-              const uint32_t yb = smem_u32(smem + A_Y + half * nh0 * CHUNK);
-              const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(half * 64 * nh0);
-#pragma unroll 1
-              for (int ks = 0; ks < BT / 16; ++ks) {
-                const uint64_t ad = sdesc_sw128(pa + (ks >> 2) * CHUNK + (ks & 3) * 32, 16, 1024);
-                const uint64_t bd = sdesc_sw128(yb + ks * 2048, CHUNK, 1024);
-                umma_bf16(d_tmem, ad, bd, idesc, (t != t0 || ks != 0) ? 1u : 0u);
+            for (int ks = 0; ks < BT / 16 && ok; ++ks) {
+              const int sl = ks / (SLAB_ROWS / 16);
+              if (ks % (SLAB_ROWS / 16) == 0) {
+                ok = mbar_wait(ay_full + sl, yph, abort_flag, p.status);
+                if (!ok) break;
+                tc_fence_after();
               }
-              umma_commit(ay_empty + half);
+              const uint64_t ad = sdesc_sw128(pa + (ks >> 2) * CHUNK + (ks & 3) * 32, 16, 1024);
+              for (int half = 0; half < 2; ++half) {
+                const int nh = half == 0 ? nh0 : nh1;
+                if (nh == 0) continue;
+                const uint32_t idesc = idesc_bf16_f32(128, 64 * nh, false, true);
+                // MN-major B: N = 64 nh columns of d in chunks 4 KB apart inside
+                // the slab; K-step ks covers rows 16 (ks % 2) .. +15 of slab sl.
+                const uint32_t yb = smem_u32(smem + A_Y + sl * p.KC * SLAB_CHUNK + half * nh0 * SLAB_CHUNK);
+                const uint64_t bd = sdesc_sw128(yb + (ks % (SLAB_ROWS / 16)) * 2048, SLAB_CHUNK, 1024);
+                umma_bf16(tmem_base + static_cast<uint32_t>(half * 64 * nh0), ad, bd, idesc,
+                          (t != t0 || ks != 0) ? 1u : 0u);
+              }
+              if (ks % (SLAB_ROWS / 16) == SLAB_ROWS / 16 - 1) umma_commit(ay_empty + sl);
             }
             if (!ok) break;
             umma_commit_mc(p_empty + slot, static_cast<uint16_t>(1u << 0));  // P slot free (Z CTA)
@@ -545,7 +660,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                   dst[v] = a;
                 }
               } else {
-                const int s = u % p.split;
+                const int s = u / p.n_blocks;
                 float4* dst = reinterpret_cast<float4*>(
                     p.dw_part + (static_cast<long long>(s) * p.V_pad + row) * p.d + col);
 #pragma unroll
@@ -663,7 +778,8 @@ inline int max_clusters(int sms) {
 }
 
 template <int MODE>
-inline int launch_mode(const CUtensorMap& tx, const CUtensorMap& ty, const Params& p, int clusters, cudaStream_t s) {
+inline int launch_mode(const CUtensorMap& tx, const CUtensorMap& ty, const CUtensorMap& tys, const Params& p,
+                       int clusters, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters);
   cfg.blockDim = dim3(THREADS);
@@ -677,7 +793,7 @@ inline int launch_mode(const CUtensorMap& tx, const CUtensorMap& ty, const Param
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   count_launches(1);
-  cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_kernel<MODE>, tx, ty, p);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, bwd_kernel<MODE>, tx, ty, tys, p);
   if (e != cudaSuccess) {
     set_last_error(std::string("bwd_kernel launch: ") + cudaGetErrorString(e));
     return 3;
@@ -688,9 +804,14 @@ inline int launch_mode(const CUtensorMap& tx, const CUtensorMap& ty, const Param
 inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long N, long long V, long long d,
                   const int64_t* tgt, const uint8_t* mask, float c, const float* lse, float w, uint16_t* dh, float* dW,
                   int accumulate, unsigned* status, void* scratch, int sms, cudaStream_t s) {
-  CUtensorMap tm_h, tm_w;
-  if (int rc = make_map_bf16(&tm_h, h, d, N, ldh * 2, KB, 128); rc) return rc;
-  if (int rc = make_map_bf16(&tm_w, W, d, V, d * 2, KB, 128); rc) return rc;
+  const uint32_t kc = static_cast<uint32_t>(d / KB);
+  CUtensorMap tm_hx, tm_wx, tm_hy, tm_wy, tm_hs, tm_ws;
+  if (int rc = make_map_bf16_3d(&tm_hx, h, d, N, ldh * 2, BM, kc); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_wx, W, d, V, d * 2, BM, kc); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_hy, h, d, N, ldh * 2, BT, 2); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_wy, W, d, V, d * 2, BT, 2); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_hs, h, d, N, ldh * 2, SLAB_ROWS, kc); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_ws, W, d, V, d * 2, SLAB_ROWS, kc); rc) return rc;
   const int clusters_max = max_clusters(sms);
   Params p{};
   p.N = static_cast<int>(N);
@@ -702,7 +823,9 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
   p.lse = lse;
   p.inv_c = 1.0f / c;
   p.cl2e = c * kLog2e;
-  p.w = w;
+  p.w = -w;  // the P tiles hold -G
+  p.zlim2 = (kTanhXmax * c) * (kTanhXmax * c);
+  scaled_tanh_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
   p.status = status;
   if (dh) {
     Params q = p;
@@ -713,7 +836,7 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
     q.dh = reinterpret_cast<__nv_bfloat16*>(dh);
     q.ldh = ldh;
     const int cl = static_cast<int>(q.n_units < clusters_max ? q.n_units : clusters_max);
-    if (int rc = launch_mode<DH>(tm_h, tm_w, q, cl, s); rc) return rc;
+    if (int rc = launch_mode<DH>(tm_hx, tm_wy, tm_ws, q, cl, s); rc) return rc;
   }
   if (dW) {
     Params q = p;
@@ -726,13 +849,13 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
     q.V_pad = static_cast<int>(cdivll(V, BM) * BM);
     q.dw_part = static_cast<float*>(scratch);
     const int cl = static_cast<int>(q.n_units < clusters_max ? q.n_units : clusters_max);
-    if (int rc = launch_mode<DW>(tm_w, tm_h, q, cl, s); rc) return rc;
+    if (int rc = launch_mode<DW>(tm_wx, tm_hy, tm_hs, q, cl, s); rc) return rc;
     if (q.split > 1) {
       const long long n4 = V * d / 4;
       const int blocks = static_cast<int>(cdivll(n4, 256) < sms * 8 ? cdivll(n4, 256) : sms * 8);
       count_launches(1);
       dw_split_reduce_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(scratch), q.split,
-                                                    static_cast<long long>(q.V_pad) * d / 4, n4, w, accumulate,
+                                                    static_cast<long long>(q.V_pad) * d / 4, n4, p.w, accumulate,
                                                     reinterpret_cast<float4*>(dW));
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) {

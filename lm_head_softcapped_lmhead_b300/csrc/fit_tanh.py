@@ -9,8 +9,8 @@ and the worst relative error, in exact arithmetic and evaluated in fp32).
 """
 import numpy as np
 
-XMAX = 0.625
-DEG = 5
+XMAX = 0.3
+DEG = 3
 
 
 def g(u):

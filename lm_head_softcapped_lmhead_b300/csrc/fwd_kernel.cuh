@@ -11,24 +11,30 @@
 // softcapped CE kernel").
 //
 // Design (one CTA per SM, persistent):
-//  * work = tiles (row block of 128 rows) x (vocab tile of 256); CTA b takes
+//  * work = tiles (row block of 128 rows) x (vocab tile of 128); CTA b takes
 //    the contiguous tile range [b T / G, (b+1) T / G) in row-block-major
-//    order, so a CTA keeps one h block resident across its vocab tiles.
-//  * warp 8 (one lane) issues TMA: the h block (d/64 chunks of 128 x 64 bf16,
-//    128B-swizzled) once per row block, W tiles in 256 x 64 chunks through a
-//    3-stage ring.
-//  * warp 9 (one lane) issues tcgen05.mma M=128 N=256 K=16 into one of two
-//    TMEM accumulators (2 x 256 fp32 columns = all 512).
+//    order ("segments" of one row block).
+//  * the h block of the current row block lives in TMEM (256 of the 512
+//    columns, bf16 packed two per column) and is the A operand of every MMA;
+//    shared memory is a 3-stage ring of 64 KB TMA loads (four 64-column
+//    chunks of 128 rows each) that carries first the h block (copied to
+//    TMEM with tcgen05.cp) and then the W tiles.  TMA sustains only a few
+//    million loads per second per SM, so the loads are as large as the ring
+//    allows; 128+ KB stay in flight to cover the L2 latency under load.
+//  * warp 8 (one lane) issues the TMA loads; warp 9 (one lane) issues
+//    tcgen05.cp and tcgen05.mma (M=128, N=128, K=16) into one of two TMEM
+//    accumulators (columns 0-127 and 128-255).
 //  * warps 0-7: epilogue.  Warp w reads TMEM lanes 32 (w % 4) .. +31 (its 32
-//    rows) and columns 128 (w / 4) .. +127 of the tile.  Per logit:
-//    x = z / c, e = 2^(c log2(e) tanh(x)) with tanh from the minimax
-//    polynomial, summed in fp32.  No running max is needed: |s| < c, so
-//    S = sum e^s lies in (V e^-c, V e^c) and cannot overflow for the
+//    rows) and columns 64 (w / 4) .. +63 of the tile.  Per logit:
+//    e = 2^(c log2(e) tanh(z/c)) with tanh from the minimax polynomial,
+//    summed in fp32 over the segment.  No running max is needed: |s| < c,
+//    so S = sum e^s lies in (V e^-c, V e^c) and cannot overflow for the
 //    accepted c (the host rejects c > c_max(V)).
-//  * outputs per tile and half tile: the partial sum into
-//    part[2 vt + half][row]; the target logit s_t into st[row] by the one
-//    thread whose columns hold t.  A finalize kernel adds the partials in a
-//    fixed order (deterministic) and forms lse and nll.
+//  * outputs: per (segment, column half) the partial sum into
+//    part[2 s + half][row], s = the segment's first tile inside its row block
+//    (< VT); the target logit s_t into
+//    st[row] by the one thread whose columns hold t.  A finalize kernel adds
+//    the partials in a fixed order (deterministic) and forms lse and nll.
 #pragma once
 #include "ptx.cuh"
 #include "softcap_math.cuh"
@@ -37,77 +43,107 @@ namespace lmce {
 namespace fwdk {
 
 constexpr int BM = 128;        // rows per block (TMEM lanes, UMMA M)
-constexpr int BN = 256;        // vocab per tile (UMMA N)
+constexpr int BN = 128;        // vocab per tile (UMMA N)
 constexpr int KB = 64;         // K elements per chunk (one 128-byte swizzle row)
-constexpr int STAGES = 3;      // W ring depth
+constexpr int STAGES = 3;      // ring depth
+constexpr int SC = 4;          // 64-column chunks per stage (one 64 KB TMA load)
 constexpr int MAX_KC = 8;      // d <= 512
 constexpr int EPI_WARPS = 8;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int THREADS = 320;
-constexpr uint32_t X_CHUNK = BM * KB * 2;  // 16 KB
-constexpr uint32_t Y_CHUNK = BN * KB * 2;  // 32 KB
-constexpr uint32_t SMEM_X = 0;
-constexpr uint32_t SMEM_Y = SMEM_X + MAX_KC * X_CHUNK;
-constexpr uint32_t SMEM_BAR = SMEM_Y + STAGES * Y_CHUNK;
+constexpr uint32_t CHUNK = 128 * KB * 2;   // 16 KB: 128 rows x 64 bf16
+constexpr uint32_t STAGE = SC * CHUNK;     // 64 KB
+constexpr uint32_t SMEM_RING = 0;
+constexpr uint32_t SMEM_BAR = SMEM_RING + STAGES * STAGE;
 constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + barriers + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_X = 256;           // h block: columns 256-511
 constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, false);
 
 struct Params {
   int N;                // rows addressed by the h tensor map
+  int maxseg;           // partial-sum slots per row and column half
   const int* n_rows;    // optional device-side live row count (compacted rows)
   int V, d, KC, VT;     // vocab, model dim, d / 64, vocab tiles
   int N_pad;            // slot stride of `part`
   const int64_t* tgt;   // [N]
   float inv_c, c;
-  float k[6];           // c * log2(e) * tanh polynomial coefficients
-  float* part;          // [2 VT][N_pad] partial sums of e^s
+  float zlim2;          // (kTanhXmax * c)^2: range of the polynomial in z^2
+  float k[kTanhTerms];  // c log2(e) C_i / c^(2i+1): 2^(z P(z^2)) = e^(c tanh(z/c))
+  float* part;          // [2 maxseg][N_pad] partial sums of e^s
   float* st;            // [N] softcapped target logit
   unsigned* status;
 };
 
-// Sum over 32 columns of 2^(c log2e tanh(z/c)); `lim` = number of valid
-// columns (32 except in the last vocab tile).
-__device__ __forceinline__ float chunk_sum(const uint32_t (&r)[32], const Params& p, int lim) {
-  float xmax = 0.f;
-  float s0 = 0.f, s1 = 0.f, s2 = 0.f, s3 = 0.f;
+// Exact-form sum for chunks whose |z| may exceed the polynomial range.  Out
+// of line with by-value arguments, so it is a real branch rather than code
+// predicated into every chunk.
+struct ChunkF32 {
+  uint32_t v[32];
+};
+__device__ __noinline__ float chunk_sum_slow(ChunkF32 r, float c, float inv_c, int lim) {
+  float a0 = 0.f, a1 = 0.f;
+  const float cl2e = c * kLog2e;
 #pragma unroll
-  for (int j = 0; j < 32; j += 4) {
-    float e[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float x = __uint_as_float(r[j + u]) * p.inv_c;
-      xmax = fmaxf(xmax, fabsf(x));
-      e[u] = ex2_approx(x * tanh_poly_scaled(x * x, p.k));
-    }
-    if (lim < 32) {
-#pragma unroll
-      for (int u = 0; u < 4; ++u) e[u] = (j + u < lim) ? e[u] : 0.f;
-    }
-    s0 += e[0];
-    s1 += e[1];
-    s2 += e[2];
-    s3 += e[3];
+  for (int j = 0; j < 32; j += 2) {
+    const float e0 = ex2_approx(cl2e * tanh_any(__uint_as_float(r.v[j]) * inv_c));
+    const float e1 = ex2_approx(cl2e * tanh_any(__uint_as_float(r.v[j + 1]) * inv_c));
+    a0 += (j < lim) ? e0 : 0.f;
+    a1 += (j + 1 < lim) ? e1 : 0.f;
   }
-  float s = (s0 + s1) + (s2 + s3);
-  // Rare path (some |x| beyond the polynomial's range): recompute the chunk
-  // with the exact-form tanh for those elements.
-  if (__any_sync(0xffffffffu, xmax > kTanhXmax)) {
-    float a0 = 0.f, a1 = 0.f;
-    const float cl2e = p.c * kLog2e;
+  return a0 + a1;
+}
+
+// Sum over 32 columns of 2^(c log2e tanh(z/c)), packed fp32x2: per column
+// pair one FMUL2 (u = z^2), one FADD2 (range check), three FFMA2 + one FMUL2
+// (polynomial), two ex2 and one FADD2.  `lim` = number of valid columns (32
+// except in the last vocab tile).  If some |z| may exceed the polynomial's
+// range (sum of z^2 over the chunk > (kTanhXmax c)^2, a conservative test),
+// the warp recomputes the chunk with the exact-form tanh.
+__device__ __forceinline__ float chunk_sum(const uint32_t (&r)[32], const float2 (&k)[kTanhTerms], const Params& p,
+                                           int lim) {
+  float2 s0 = make_float2(0.f, 0.f), s1 = s0, su = s0;
 #pragma unroll
-    for (int j = 0; j < 32; j += 2) {
-      const float x0 = __uint_as_float(r[j]) * p.inv_c;
-      const float x1 = __uint_as_float(r[j + 1]) * p.inv_c;
-      float e0 = ex2_approx(cl2e * tanh_any(x0));
-      float e1 = ex2_approx(cl2e * tanh_any(x1));
-      a0 += (j < lim) ? e0 : 0.f;
-      a1 += (j + 1 < lim) ? e1 : 0.f;
+  for (int j = 0; j < 16; ++j) {
+    const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    const float2 u = __fmul2_rn(z, z);
+    su = __fadd2_rn(su, u);
+    const float2 a = poly_z2(z, u, k);
+    float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+    if (lim < 32) {
+      e.x = (2 * j < lim) ? e.x : 0.f;
+      e.y = (2 * j + 1 < lim) ? e.y : 0.f;
     }
-    s = a0 + a1;
+    if (j & 1)
+      s1 = __fadd2_rn(s1, e);
+    else
+      s0 = __fadd2_rn(s0, e);
+  }
+  float s = (s0.x + s0.y) + (s1.x + s1.y);
+  if (__any_sync(0xffffffffu, !(su.x + su.y <= p.zlim2))) {
+    ChunkF32 c;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c.v[j] = r[j];
+    s = chunk_sum_slow(c, p.c, p.inv_c, lim);
   }
   return s;
+}
+
+// Target logit: the thread whose target column falls in this chunk takes
+// z from its registers (predicated selects, only when some lane hits).
+__device__ __forceinline__ void pick_target(const uint32_t (&r)[32], long long rel, const Params& p, float& st_val,
+                                            bool& st_hit) {
+  const bool hit = (rel >= 0 && rel < 32);
+  if (__any_sync(0xffffffffu, hit)) {
+    float zt = 0.f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) zt = (rel == j) ? __uint_as_float(r[j]) : zt;
+    if (hit) {
+      st_val = p.c * tanh_any(zt * p.inv_c);
+      st_hit = true;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(THREADS, 1)
@@ -116,15 +152,15 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
-  uint64_t* y_full = bars;          // [STAGES]
-  uint64_t* y_empty = bars + 3;     // [STAGES]
-  uint64_t* x_full = bars + 6;
-  uint64_t* x_empty = bars + 7;
-  uint64_t* acc_full = bars + 8;    // [2]
-  uint64_t* acc_empty = bars + 10;  // [2]
-  uint64_t* mma_done = bars + 12;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 128);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 132);
+  uint64_t* full = bars;            // [STAGES]
+  uint64_t* empty = bars + 8;       // [STAGES]
+  uint64_t* acc_full = bars + 16;   // [2]
+  uint64_t* acc_empty = bars + 18;  // [2]
+  uint64_t* x_free = bars + 20;     // the previous segment's MMAs no longer read the h block
+  uint64_t* x_ready = bars + 22;    // the h block's tcgen05.cp have completed
+  uint64_t* mma_done = bars + 21;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 192);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 196);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -132,20 +168,22 @@ __global__ void __launch_bounds__(THREADS, 1)
   const int n_rows = p.n_rows ? min(*p.n_rows, p.N) : p.N;
   const int NB = (n_rows + BM - 1) / BM;
   const long long T = static_cast<long long>(NB) * p.VT;
-  const long long g_begin = static_cast<long long>(blockIdx.x) * T / gridDim.x;
-  const long long g_end = static_cast<long long>(blockIdx.x + 1) * T / gridDim.x;
+  const long long G = gridDim.x;
+  const long long g_begin = static_cast<long long>(blockIdx.x) * T / G;
+  const long long g_end = static_cast<long long>(blockIdx.x + 1) * T / G;
+  const int npair = (p.KC + SC - 1) / SC;  // ring stages per h block / W tile
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(y_full + i, 1);
-      mbar_init(y_empty + i, 1);
+      mbar_init(full + i, 1);
+      mbar_init(empty + i, 1);
     }
-    mbar_init(x_full, 1);
-    mbar_init(x_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(acc_full + i, 1);
       mbar_init(acc_empty + i, EPI_WARPS);
     }
+    mbar_init(x_free, 1);
+    mbar_init(x_ready, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -166,78 +204,107 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (warp == TMA_WARP) {
     if (lane == 0 && g_begin < g_end) {
+      // Ring order per tile: (at a new row block) the h block's stages, then
+      // the W tile's stages.  Chunks past d / 64 read zeros.
       int stage = 0;
-      uint32_t phase = 0, xph = 0;
+      uint32_t phase = 0;
       int prev_rb = -1;
-      uint32_t pend = 0;     // stages with a load in flight that nobody waited for
+      uint32_t pend = 0;
       uint32_t pend_ph[STAGES] = {0, 0, 0};
       bool ok = true;
+      auto put = [&](const CUtensorMap* m, int row0, int pr) -> bool {
+        if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, p.status)) return false;
+        mbar_expect_tx(full + stage, STAGE);
+        tma_load_3d(smem + SMEM_RING + stage * STAGE, m, full + stage, 0, row0, SC * pr);
+        pend |= 1u << stage;
+        pend_ph[stage] = phase;
+        if (++stage == STAGES) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        return true;
+      };
       for (long long g = g_begin; g < g_end && ok; ++g) {
         const int rb = static_cast<int>(g / p.VT);
         const int vt = static_cast<int>(g % p.VT);
         if (rb != prev_rb) {
-          if (prev_rb >= 0) {
-            ok = mbar_wait(x_empty, xph, abort_flag, p.status);
-            xph ^= 1u;
-            if (!ok) break;
-          }
-          mbar_expect_tx(x_full, p.KC * X_CHUNK);
-          for (int kc = 0; kc < p.KC; ++kc)
-            tma_load_2d(smem + SMEM_X + kc * X_CHUNK, &tm_h, x_full, kc * KB, rb * BM);
+          for (int pr = 0; pr < npair && ok; ++pr) ok = put(&tm_h, rb * BM, pr);
           prev_rb = rb;
         }
-        for (int kc = 0; kc < p.KC; ++kc) {
-          ok = mbar_wait(y_empty + stage, phase ^ 1u, abort_flag, p.status);
-          if (!ok) break;
-          mbar_expect_tx(y_full + stage, Y_CHUNK);
-          tma_load_2d(smem + SMEM_Y + stage * Y_CHUNK, &tm_w, y_full + stage, kc * KB, vt * BN);
-          pend |= 1u << stage;
-          pend_ph[stage] = phase;
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
+        for (int pr = 0; pr < npair && ok; ++pr) ok = put(&tm_w, vt * BN, pr);
       }
       if (!ok) {
         // Let every issued copy land before the CTA can exit (bounded).
-        const unsigned long long t0 = globaltimer_ns();
+        const long long t0 = clock64();
         for (int s = 0; s < STAGES; ++s)
           if (pend & (1u << s))
-            while (!mbar_try_wait(smem_u32(y_full + s), pend_ph[s]) && globaltimer_ns() - t0 < kWaitLimitNs) {
+            while (!mbar_try_wait(smem_u32(full + s), pend_ph[s]) && clock64() - t0 < kWaitLimitCycles) {
             }
       }
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0 && g_begin < g_end) {
       int stage = 0, acc = 0;
-      uint32_t phase = 0, aph = 0, xph = 0;
+      uint32_t phase = 0, aph = 0, xph = 0, rph = 0;
       int prev_rb = -1;
       bool ok = true;
       for (long long g = g_begin; g < g_end && ok; ++g) {
         const int rb = static_cast<int>(g / p.VT);
         if (rb != prev_rb) {
-          ok = mbar_wait(x_full, xph, abort_flag, p.status);
-          xph ^= 1u;
+          if (prev_rb >= 0) {
+            // The h block in TMEM is overwritten only after the previous
+            // segment's MMAs are done with it.
+            umma_commit(x_free);
+            ok = mbar_wait(x_free, xph, abort_flag, p.status);
+            xph ^= 1u;
+            if (!ok) break;
+          }
+          for (int pr = 0; pr < npair && ok; ++pr) {
+            ok = mbar_wait(full + stage, phase, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            for (int c = 0; c < SC; ++c) {
+              const int kc = SC * pr + c;
+              if (kc >= p.KC) break;
+              const uint32_t xa = smem_u32(smem + SMEM_RING + stage * STAGE + c * CHUNK);
+#pragma unroll
+              for (int k = 0; k < KB / 16; ++k)
+                tmem_cp_128x256b(tmem_base + TMEM_X + static_cast<uint32_t>(kc * 32 + k * 8),
+                                 sdesc_sw128(xa + k * 32, 16, 1024));
+            }
+            umma_commit(empty + stage);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
           if (!ok) break;
+          // The MMAs below read the copied block: wait for the copies.
+          umma_commit(x_ready);
+          ok = mbar_wait(x_ready, rph, abort_flag, p.status);
+          rph ^= 1u;
+          if (!ok) break;
+          tc_fence_after();
           prev_rb = rb;
         }
         ok = mbar_wait(acc_empty + acc, aph ^ 1u, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kc = 0; kc < p.KC; ++kc) {
-          ok = mbar_wait(y_full + stage, phase, abort_flag, p.status);
+        for (int pr = 0; pr < npair && ok; ++pr) {
+          ok = mbar_wait(full + stage, phase, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          const uint32_t xa = smem_u32(smem + SMEM_X + kc * X_CHUNK);
-          const uint32_t ya = smem_u32(smem + SMEM_Y + stage * Y_CHUNK);
+          for (int c = 0; c < SC; ++c) {
+            const int kc = SC * pr + c;
+            if (kc >= p.KC) break;
+            const uint32_t ya = smem_u32(smem + SMEM_RING + stage * STAGE + c * CHUNK);
 #pragma unroll
-          for (int k = 0; k < KB / 16; ++k) {
-            umma_bf16(d_tmem, sdesc_sw128(xa + k * 32, 16, 1024), sdesc_sw128(ya + k * 32, 16, 1024), IDESC,
-                      (kc | k) != 0 ? 1u : 0u);
+            for (int k = 0; k < KB / 16; ++k)
+              umma_bf16_ts(d_tmem, tmem_base + TMEM_X + static_cast<uint32_t>(kc * 32 + k * 8),
+                           sdesc_sw128(ya + k * 32, 16, 1024), IDESC, (kc | k) != 0 ? 1u : 0u);
           }
-          umma_commit(y_empty + stage);
+          umma_commit(empty + stage);
           if (++stage == STAGES) {
             stage = 0;
             phase ^= 1u;
@@ -245,26 +312,28 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (!ok) break;
         umma_commit(acc_full + acc);
-        const bool seg_end = (g + 1 == g_end) || ((g + 1) / p.VT != rb);
-        if (seg_end) umma_commit(x_empty);
         acc ^= 1;
         if (acc == 0) aph ^= 1u;
       }
-      // All issued MMAs complete before TMEM is released (bounded).
+      // All issued tcgen05 work completes before TMEM is released (bounded).
       umma_commit(mma_done);
-      const unsigned long long t0 = globaltimer_ns();
-      while (!mbar_try_wait(smem_u32(mma_done), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+      const long long t0 = clock64();
+      while (!mbar_try_wait(smem_u32(mma_done), 0) && clock64() - t0 < kWaitLimitCycles) {
       }
     }
   } else {
     // ---------------- epilogue warps ----------------
     const int q = warp & 3;    // TMEM lane quarter -> rows 32q .. 32q+31
-    const int hc = warp >> 2;  // column half of the tile
+    const int hc = warp >> 2;  // column half of the tile (64 columns)
+    float2 k2[kTanhTerms];
+#pragma unroll
+    for (int i = 0; i < kTanhTerms; ++i) k2[i] = make_float2(p.k[i], p.k[i]);
     int acc = 0;
     uint32_t aph = 0;
     int cur_rb = -1;
     int row = 0;
     long long t = -1;
+    float seg_sum = 0.f;
     for (long long g = g_begin; g < g_end; ++g) {
       const int rb = static_cast<int>(g / p.VT);
       const int vt = static_cast<int>(g % p.VT);
@@ -272,41 +341,46 @@ __global__ void __launch_bounds__(THREADS, 1)
         row = rb * BM + q * 32 + lane;
         t = (row < n_rows) ? p.tgt[row] : -1;
         cur_rb = rb;
+        seg_sum = 0.f;
       }
       if (!mbar_wait(acc_full + acc, aph, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + hc * 128);
-      const int col0 = vt * BN + hc * 128;
-      float sum = 0.f;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + hc * 64);
+      const int col0 = vt * BN + hc * 64;
       float st_val = 0.f;
       bool st_hit = false;
-#pragma unroll 1
-      for (int ch = 0; ch < 4; ++ch) {
-        uint32_t r[32];
-        tmem_ld32(tbase + ch * 32, r);
-        tmem_ld_wait();
-        reg_fence32(r);
-        const int cbase = col0 + ch * 32;
-        const int lim = min(32, p.V - cbase);
-        if (lim > 0) sum += chunk_sum(r, p, lim);
-        const long long rel = t - cbase;
-        const bool hit = (rel >= 0 && rel < 32);
-        if (__any_sync(0xffffffffu, hit)) {
-          float zt = 0.f;
-#pragma unroll
-          for (int j = 0; j < 32; ++j) zt = (rel == j) ? __uint_as_float(r[j]) : zt;
-          if (hit) {
-            st_val = p.c * tanh_any(zt * p.inv_c);
-            st_hit = true;
-          }
-        }
+      // Two 32-column chunks; the TMEM load of the second is in flight while
+      // the first is processed.
+      uint32_t ra[32], rc[32];
+      tmem_ld32(tbase, ra);
+      tmem_ld_wait();
+      reg_fence32(ra);
+      tmem_ld32(tbase + 32, rc);
+      {
+        const int lim = min(32, p.V - col0);
+        if (lim > 0) seg_sum += chunk_sum(ra, k2, p, lim);
+        pick_target(ra, t - col0, p, st_val, st_hit);
       }
+      tmem_ld_wait();
+      reg_fence32(rc);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty + acc);
+      if (lane == 0) mbar_arrive(acc_empty + acc);  // TMEM buffer free: both chunks are in registers
+      {
+        const int lim = min(32, p.V - (col0 + 32));
+        if (lim > 0) seg_sum += chunk_sum(rc, k2, p, lim);
+        pick_target(rc, t - (col0 + 32), p, st_val, st_hit);
+      }
       if (row < n_rows) {
-        p.part[static_cast<size_t>(2 * vt + hc) * p.N_pad + row] = sum;
         if (st_hit) p.st[row] = st_val;
+        const bool seg_end = (g + 1 == g_end) || ((g + 1) / p.VT != rb);
+        if (seg_end) {
+          // Slot: this segment's first tile inside row block rb (< VT, unique
+          // among the CTAs covering rb).
+          const long long g0 = static_cast<long long>(rb) * p.VT;
+          const int slot = static_cast<int>(g_begin > g0 ? g_begin - g0 : 0);
+          p.part[static_cast<size_t>(2 * slot + hc) * p.N_pad + row] = seg_sum;
+        }
       }
       acc ^= 1;
       if (acc == 0) aph ^= 1u;

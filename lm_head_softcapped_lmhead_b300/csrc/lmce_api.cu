@@ -56,7 +56,7 @@ Layout make_layout(int64_t N, int64_t V, int64_t d, unsigned flags) {
   o = up(o + sizeof(lmce::BpbPartial) * lmce::kBpbBlocks);
   const int64_t N_pad = cdiv(N, lmce::fwdk::BM) * lmce::fwdk::BM;
   const int64_t VT = cdiv(V, lmce::fwdk::BN);
-  L.part = o;
+  L.part = o;  // at most VT CTAs cover one row block: 2 VT slots per row
   o = up(o + sizeof(float) * 2 * VT * N_pad);
   L.st = o;
   o = up(o + sizeof(float) * N_pad);
@@ -164,6 +164,31 @@ int make_map_bf16(CUtensorMap* m, const void* base, uint64_t inner, uint64_t out
   return LMCE_OK;
 }
 
+// 3-D bf16 tensor map viewing a row-major [rows, d] array (row pitch
+// pitch_bytes, d a multiple of 64) as (d % 64, row, d / 64); box =
+// 64 x box_rows x box_chunks, 128-byte swizzle, out-of-bounds reads as zero.
+// One load of this box fills box_chunks consecutive [box_rows x 64] chunks.
+int make_map_bf16_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t rows, uint64_t pitch_bytes,
+                     uint32_t box_rows, uint32_t box_chunks) {
+  auto fn = encode_fn();
+  if (!fn) {
+    g_last_err = "cuTensorMapEncodeTiled unavailable";
+    return LMCE_ECUDA;
+  }
+  cuuint64_t dims[3] = {64, rows, d / 64};
+  cuuint64_t strides[2] = {pitch_bytes, 128};
+  cuuint32_t box[3] = {64, box_rows, box_chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_err = "cuTensorMapEncodeTiled (3-D) failed with CUresult " + std::to_string(static_cast<int>(r));
+    return LMCE_ECUDA;
+  }
+  return LMCE_OK;
+}
+
 void set_last_error(const std::string& s) { g_last_err = s; }
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
@@ -236,8 +261,8 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
   }
 
   CUtensorMap tm_h, tm_w;
-  if (int rc = lmce::make_map_bf16(&tm_h, hx, d, N, ldx * 2, lmce::fwdk::KB, lmce::fwdk::BM); rc) return rc;
-  if (int rc = lmce::make_map_bf16(&tm_w, W, d, V, d * 2, lmce::fwdk::KB, lmce::fwdk::BN); rc) return rc;
+  if (int rc = lmce::make_map_bf16_3d(&tm_h, hx, d, N, ldx * 2, lmce::fwdk::BM, lmce::fwdk::SC); rc) return rc;
+  if (int rc = lmce::make_map_bf16_3d(&tm_w, W, d, V, d * 2, lmce::fwdk::BN, lmce::fwdk::SC); rc) return rc;
 
   lmce::fwdk::Params p{};
   p.N = static_cast<int>(N);
@@ -250,21 +275,21 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
   p.tgt = tg;
   p.inv_c = 1.0f / c;
   p.c = c;
-  const float cl2e = c * lmce::kLog2e;
-  const float coef[6] = {lmce::kTanhC0, lmce::kTanhC1, lmce::kTanhC2, lmce::kTanhC3, lmce::kTanhC4, lmce::kTanhC5};
-  for (int i = 0; i < 6; ++i) p.k[i] = cl2e * coef[i];
+  p.zlim2 = (lmce::kTanhXmax * c) * (lmce::kTanhXmax * c);
+  lmce::scaled_tanh_coeffs(static_cast<double>(c) * 1.4426950408889634, 1.0 / static_cast<double>(c), p.k);
   p.part = reinterpret_cast<float*>(w + L.part);
   p.st = reinterpret_cast<float*>(w + L.st);
   p.status = status;
 
   const int64_t T_max = cdiv(N, lmce::fwdk::BM) * p.VT;
   const int grid = static_cast<int>(std::min<int64_t>(T_max, di.sms));
+  p.maxseg = p.VT;
   lmce::count_launches(2);
   lmce::fwdk::fwd_kernel<<<grid, lmce::fwdk::THREADS, lmce::fwdk::SMEM_BYTES, s>>>(tm_h, tm_w, p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fwd_kernel launch");
   const int fblocks = static_cast<int>(std::min<int64_t>(cdiv(N, 256), int64_t(di.sms) * 4));
-  lmce::fwd_finalize_kernel<<<fblocks, 256, 0, s>>>(p.part, 2 * p.VT, p.N_pad, p.st, tg, nrows_dev,
+  lmce::fwd_finalize_kernel<<<fblocks, 256, 0, s>>>(p.part, p.VT, grid, p.N_pad, p.st, tg, nrows_dev,
                                                     static_cast<int>(N), static_cast<int>(V), idx, nll, lse, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fwd_finalize launch");

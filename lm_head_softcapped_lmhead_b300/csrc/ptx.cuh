@@ -65,18 +65,24 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t pa
 
 // Bounded wait for the phase with parity `parity` of `bar`.  Returns false
 // (after raising the CTA's abort flag and the global status) if the wait
-// exceeds kWaitLimitNs or another role of the CTA has already aborted.
+// exceeds about kWaitLimitNs or another role of the CTA has already aborted.
+// The limit is counted in SM clock cycles (clock64 is cheap; %globaltimer is
+// not) and only checked every 1024 polls, so a healthy wait costs nothing
+// beyond its try_wait polls.
+constexpr long long kWaitLimitCycles = 4000000000ll;  // ~2 s at 2 GHz
 template <bool kClusterAcquire = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
                                           unsigned* status) {
   const uint32_t a = smem_u32(bar);
-  if (kClusterAcquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-  const unsigned long long t0 = globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
+  long long t0 = 0;
+  for (uint32_t it = 0;; ++it) {
     if (kClusterAcquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-    if ((it & 31u) == 0u) {
+    if ((it & 1023u) == 1023u) {
       if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > kWaitLimitNs) {
+      const long long now = clock64();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > kWaitLimitCycles) {
         *abort_flag = 1;
         atomicOr(status, ST_ETIMEOUT);
         return false;
@@ -114,6 +120,17 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* m, uin
       : "memory");
 }
 
+// 3-D tiled load.  The bf16 tensor maps used here view a row-major [rows, d]
+// array as (d % 64, row, d / 64) so that one load brings several 64-column
+// chunks, each laid out as 128-byte-swizzled rows, chunk after chunk.  x is 0.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* m, uint64_t* bar, int x, int y, int z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(m)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+
 // ---- tcgen05: tensor memory ---------------------------------------------------
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
@@ -136,8 +153,24 @@ __device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t a_desc, uint
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
-// Arrive (once) on `bar` when all previously issued tcgen05.mma of this thread
-// have completed.
+// Same with the A operand read from tensor memory: A is M x 16 (bf16) at
+// a_tmem, one row per lane, the 16 K values packed two per 32-bit column
+// (8 columns).
+__device__ __forceinline__ void umma_bf16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                             uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(
+          d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// Copy a 128-row x 256-bit block (128 x 16 bf16) described by a shared-memory
+// matrix descriptor into tensor memory: row i to lane i, 8 columns.
+__device__ __forceinline__ void tmem_cp_128x256b(uint32_t taddr, uint64_t s_desc) {
+  asm volatile("tcgen05.cp.cta_group::1.128x256b [%0], %1;" ::"r"(taddr), "l"(s_desc) : "memory");
+}
+// Arrive (once) on `bar` when all previously issued tcgen05 operations (mma,
+// cp) of this thread have completed.
 __device__ __forceinline__ void umma_commit(uint64_t* bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
                : "memory");
@@ -218,6 +251,15 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
 }
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+// Asynchronous 16-byte store into another CTA's shared memory that performs
+// complete_tx(16) on the mbarrier at shared::cluster address `mbar` (also in
+// that CTA) once the data has landed.
+__device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d,
+                                            uint32_t mbar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(addr),
+               "r"(a), "r"(b), "r"(c), "r"(d), "r"(mbar)
                : "memory");
 }
 __device__ __forceinline__ void cluster_arrive() {

@@ -1,0 +1,53 @@
+"""Host-side helpers for running the head on several GPUs, one process each.
+
+The path shards over rows (tokens are independent): rank r takes a
+contiguous slice of the rows and the whole tied table W.  nll, lse and dh
+stay local.  Only two reductions cross ranks:
+  * the bits-per-byte sums (sum nll fp64, sum bytes, row count: 24 bytes),
+    gathered and added in rank order so the result does not depend on
+    arrival order;
+  * dW (the data-parallel gradient of the tied table), a sum all-reduce.
+These run through torch.distributed (NCCL on GPUs, gloo on CPU).
+"""
+from __future__ import annotations
+
+import torch
+
+
+def row_shard(N: int, rank: int, world: int) -> tuple:
+    """[start, stop) of rank's contiguous row slice; sizes differ by <= 1."""
+    if world < 1 or not 0 <= rank < world:
+        raise ValueError("bad rank / world")
+    return (N * rank) // world, (N * (rank + 1)) // world
+
+
+def combine_bpb(parts) -> tuple:
+    """Sum per-rank (sum_nll, sum_bytes, n) triples in the given (rank) order."""
+    sn, sb, n = 0.0, 0, 0
+    for a, b, c in parts:
+        sn += float(a)
+        sb += int(b)
+        n += int(c)
+    return sn, sb, n
+
+
+def allreduce_bpb(local: tuple, group=None) -> tuple:
+    """All ranks receive the rank-ordered combination of every rank's sums."""
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    backend = dist.get_backend(group)
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(local[0]), float(local[1]), float(local[2])], dtype=torch.float64, device=dev)
+    out = [torch.empty_like(t) for _ in range(world)]
+    dist.all_gather(out, t, group=group)
+    parts = [(float(o[0]), int(round(float(o[1]))), int(round(float(o[2])))) for o in out]
+    return combine_bpb(parts)
+
+
+def allreduce_dW(dW: torch.Tensor, group=None) -> torch.Tensor:
+    """Sum the tied-table gradient over ranks in place."""
+    import torch.distributed as dist
+
+    dist.all_reduce(dW, op=dist.ReduceOp.SUM, group=group)
+    return dW

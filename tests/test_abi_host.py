@@ -1,0 +1,134 @@
+"""CPU-only checks of the C ABI: the library loads and exports every symbol
+the header declares, and every host-detectable error is returned before any
+CUDA call (these run without a GPU)."""
+import ctypes
+import math
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "lmhead_ce.h")
+
+OK, EINVAL, ENOTSUP, ECUDA, EDATA, ETIMEOUT = range(6)
+
+
+@pytest.fixture(scope="module")
+def L():
+    from lm_head_softcapped_lmhead_b300 import build
+    build.build()
+    import lm_head_softcapped_lmhead_b300 as lm
+    return lm.lib()
+
+
+def header_functions():
+    src = open(HEADER).read()
+    return re.findall(r"^LMCE_API\s+[\w\s\*]+?\b(\w+)\s*\(", src, flags=re.M)
+
+
+def test_every_declared_symbol_is_exported(L):
+    names = header_functions()
+    assert len(names) >= 14
+    for n in names:
+        assert hasattr(L, n), n
+    import lm_head_softcapped_lmhead_b300 as lm
+    assert set(lm.EXPORTS) == set(names)
+
+
+def test_no_torch_types_in_header():
+    src = open(HEADER).read()
+    assert "torch" not in src.lower().replace("pytorch", "") and "at::" not in src
+
+
+A = 0x10000  # a 16-byte aligned fake address: never dereferenced by these calls
+
+
+def fwd(L, h=A, ldh=512, W=A, N=100, V=200, d=512, tgt=A, mask=None, c=30.0, nll=A, lse=None, ws=A,
+        ws_bytes=1 << 40):
+    P = ctypes.c_void_p
+    return L.lmhead_ce_fwd(P(h), ldh, P(W), N, V, d, P(tgt), P(mask), c, P(nll), P(lse), P(ws), ws_bytes, None)
+
+
+def test_fwd_host_validation(L):
+    assert fwd(L, h=0) == EINVAL
+    assert fwd(L, W=0) == EINVAL
+    assert fwd(L, tgt=0) == EINVAL
+    assert fwd(L, nll=0) == EINVAL
+    assert fwd(L, ws=0) == EINVAL
+    assert fwd(L, N=0) == EINVAL
+    assert fwd(L, V=0) == EINVAL
+    assert fwd(L, d=100, ldh=104) == ENOTSUP
+    assert fwd(L, d=1024, ldh=1024) == ENOTSUP
+    assert fwd(L, ldh=500) == EINVAL
+    assert fwd(L, ldh=516) == EINVAL        # row pitch not a multiple of 16 bytes
+    assert fwd(L, h=A + 2) == EINVAL        # misaligned base
+    assert fwd(L, c=0.0) == ENOTSUP
+    assert fwd(L, c=-1.0) == ENOTSUP
+    assert fwd(L, c=float("nan")) == ENOTSUP
+    assert fwd(L, c=82.0) == ENOTSUP        # above lmce_softcap_max(200) = 86 - ln 200
+    assert fwd(L, ws_bytes=100) == EINVAL   # workspace too small
+
+
+def test_bwd_host_validation(L):
+    P = ctypes.c_void_p
+
+    def bwd(lse=A, w=1.0, dh=A, dW=A, d=512):
+        return L.lmhead_ce_bwd(P(A), 512, P(A), 100, 200, d, P(A), None, 30.0, P(lse), w, P(dh), P(dW), 0, P(A),
+                               1 << 40, None)
+    assert bwd(lse=0) == EINVAL
+    assert bwd(dh=0, dW=0) == EINVAL
+    assert bwd(w=float("nan")) == EINVAL
+    assert bwd(dh=A + 4) == EINVAL
+    assert bwd(d=96) == ENOTSUP
+
+
+def test_int4_host_validation(L):
+    P = ctypes.c_void_p
+    assert L.lmhead_int4_dequant(P(A), P(A), 10, 512, 10, P(A), None) == EINVAL    # group not /16
+    assert L.lmhead_int4_dequant(P(A), P(A), 10, 512, 48, P(A), None) == EINVAL    # does not divide d
+    assert L.lmhead_int4_dequant(P(0), P(A), 10, 512, 64, P(A), None) == EINVAL
+    assert L.lmhead_int4_dequant(P(A + 3), P(A), 10, 512, 64, P(A), None) == EINVAL
+
+
+def test_bpb_reduce_validation(L):
+    P = ctypes.c_void_p
+    assert L.bpb_reduce(P(0), P(A), None, 10, P(A), P(A), 1 << 20, None) == EINVAL
+    assert L.bpb_reduce(P(A), P(A), None, 0, P(A), P(A), 1 << 20, None) == EINVAL
+    assert L.bpb_reduce(P(A), P(A), None, 10, P(A), P(A), 16, None) == EINVAL
+
+
+def test_host_bpb_helper(L):
+    import lm_head_softcapped_lmhead_b300 as lm
+    acc = lm._BpbAcc(10.0 * math.log(2.0), 5, 3)
+    out = ctypes.c_double()
+    assert L.lmce_bpb(ctypes.byref(acc), ctypes.byref(out)) == OK
+    assert out.value == pytest.approx(2.0, rel=1e-15)
+    zero = lm._BpbAcc(1.0, 0, 1)
+    assert L.lmce_bpb(ctypes.byref(zero), ctypes.byref(out)) == EDATA
+
+
+def test_workspace_and_softcap_bounds(L):
+    import lm_head_softcapped_lmhead_b300 as lm
+    a = lm.lmce_workspace_bytes(65536, 8192, 512)
+    b = lm.lmce_workspace_bytes(65536, 8192, 512, lm.LMCE_WS_MASKED)
+    c = lm.lmce_workspace_bytes(65536, 8192, 512, lm.LMCE_WS_INT4)
+    assert 0 < a < b and a < c
+    assert lm.lmce_workspace_bytes(0, 10, 64) == 0
+    cm = lm.lmce_softcap_max(8192)
+    # e^{-c} normal and V e^{c} finite in fp32, with margin
+    assert 30.0 < cm < 88.7 - math.log(8192)
+    assert math.exp(-cm) > 1.18e-38
+
+
+def test_valid_call_without_gpu_fails_cleanly(L):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert fwd(L) == ECUDA
+    assert L.lmce_last_cuda_error()
+
+
+def test_strerror(L):
+    for code in range(6):
+        assert L.lmce_strerror(code)

@@ -1,0 +1,73 @@
+"""Multi-rank host logic on CPU: two gloo ranks each score a contiguous row
+shard (with the CPU oracle standing in for a GPU's forward), then combine the
+bits-per-byte sums and the dW gradient; the result equals the single-process
+answer."""
+import math
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    p = s.getsockname()[1]
+    s.close()
+    return p
+
+
+def _worker(rank, world, port, out_path):
+    import sys
+    sys.path.insert(0, ROOT)
+    import torch.distributed as dist
+
+    import oracle
+    import synth_inputs as si
+    from lm_head_softcapped_lmhead_b300 import dist as ld
+
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    inp = si.make_inputs(2, N=101, V=64, d=64, w_scale=10.0)
+    a, b = ld.row_shard(inp["N"], rank, world)
+    nll, lse = oracle.fwd(inp["h"][a:b], inp["W"], inp["tgt"][a:b], 30.0)
+    _, sn, sb, n = oracle.bpb(nll, inp["nbytes"][a:b])
+    tot = ld.allreduce_bpb((sn, sb, n))
+    _, dW = oracle.bwd(inp["h"][a:b], inp["W"], inp["tgt"][a:b], 30.0, lse, 1.0 / inp["N"], want_dh=False)
+    dWt = torch.from_numpy(dW)
+    ld.allreduce_dW(dWt)
+    if rank == 0:
+        np.savez(out_path, sn=tot[0], sb=tot[1], n=tot[2], dW=dWt.numpy())
+    dist.barrier()
+    dist.destroy_process_group()
+
+
+def test_row_shard_partition():
+    from lm_head_softcapped_lmhead_b300.dist import row_shard
+    for N in (1, 7, 100, 65536):
+        for world in (1, 2, 3, 8):
+            spans = [row_shard(N, r, world) for r in range(world)]
+            assert spans[0][0] == 0 and spans[-1][1] == N
+            assert all(spans[i][1] == spans[i + 1][0] for i in range(world - 1))
+            sizes = [b - a for a, b in spans]
+            assert max(sizes) - min(sizes) <= 1
+
+
+def test_two_gloo_ranks_match_single_process(tmp_path, oracle_mod):
+    import synth_inputs as si
+    out = str(tmp_path / "r0.npz")
+    mp.start_processes(_worker, args=(2, _free_port(), out), nprocs=2, join=True, start_method="spawn")
+    got = np.load(out)
+    inp = si.make_inputs(2, N=101, V=64, d=64, w_scale=10.0)
+    nll, lse = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], 30.0)
+    b, sn, sb, n = oracle_mod.bpb(nll, inp["nbytes"])
+    assert int(got["sb"]) == sb and int(got["n"]) == n
+    assert float(got["sn"]) == pytest.approx(sn, rel=1e-13)
+    _, dW = oracle_mod.bwd(inp["h"], inp["W"], inp["tgt"], 30.0, lse, 1.0 / inp["N"], want_dh=False)
+    assert np.allclose(got["dW"], dW, rtol=0, atol=1e-14)
