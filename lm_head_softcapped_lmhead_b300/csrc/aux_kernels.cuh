@@ -10,28 +10,29 @@
 namespace lmce {
 
 // ---- forward finalize ----------------------------------------------------------
-// The forward's G CTAs cover T = ceil(rows / 128) * VT tiles, CTA b taking
-// [b T / G, (b+1) T / G).  Row block rb (tiles g0 .. g0 + VT - 1) is covered
-// by CTAs b_first .. b_last; each non-empty one wrote, per column half, its
-// segment's sum of e^s into part[2 s + half][row], s = max(0, start(b) - g0).  lse = ln(sum of those, in CTA and half
-// order, in fp64); nll = lse - s_t.  With a compaction map, row r of the
-// compacted problem goes to row idx[r] of the outputs.  A target outside
-// [0, V) raises ST_EDATA and gives nll = NaN.
-__global__ void fwd_finalize_kernel(const float* __restrict__ part, int VT, int G, int N_pad,
+// The forward's G work groups (2-CTA clusters) cover T = ceil(rows / R) * VT
+// tiles (R rows per unit), group b taking [b T / G, (b+1) T / G).  Unit u
+// (tiles g0 = u VT .. g0 + VT - 1) is covered by groups b_first .. b_last;
+// each non-empty one wrote, per column half, its segment's sum of e^s into
+// part[2 s + half][row], s = max(0, start(b) - g0) < VT.  lse = ln(sum of
+// those, in group and half order, in fp64); nll = lse - s_t.  With a
+// compaction map, row r of the compacted problem goes to row idx[r] of the
+// outputs.  A target outside [0, V) raises ST_EDATA and gives nll = NaN.
+__global__ void fwd_finalize_kernel(const float* __restrict__ part, int VT, int G, int R, int N_pad,
                                     const float* __restrict__ st, const int64_t* __restrict__ tgt,
                                     const int* __restrict__ n_rows_dev, int N, int V, const int* __restrict__ idx,
                                     float* __restrict__ nll, float* __restrict__ lse, unsigned* status) {
   const int n = n_rows_dev ? min(*n_rows_dev, N) : N;
-  const long long T = static_cast<long long>((n + 127) / 128) * VT;
+  const long long T = static_cast<long long>((n + R - 1) / R) * VT;
   for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < n; r += gridDim.x * blockDim.x) {
-    const long long rb = r / 128;
-    const long long g0 = rb * VT, g1 = g0 + VT - 1;
+    const long long u = r / R;
+    const long long g0 = u * VT, g1 = g0 + VT - 1;
     const long long b_first = ((g0 + 1) * G - 1) / T;
     const long long b_last = ((g1 + 1) * G - 1) / T;
     double S = 0.0;
     for (long long b = b_first; b <= b_last; ++b) {
       const long long start = b * T / G;
-      if ((b + 1) * T / G == start) continue;  // a CTA without tiles wrote nothing
+      if ((b + 1) * T / G == start) continue;  // a group without tiles wrote nothing
       const size_t slot = static_cast<size_t>(start > g0 ? start - g0 : 0);
       S += static_cast<double>(part[(2 * slot) * N_pad + r]);
       S += static_cast<double>(part[(2 * slot + 1) * N_pad + r]);

@@ -44,31 +44,35 @@ constexpr int BM = 128;   // stationary block (TMEM lanes)
 constexpr int BT = 128;   // streamed tile (z columns; K of the accumulation)
 constexpr int KB = 64;    // K elements per chunk
 constexpr int MAX_KC = 8; // d <= 512
-constexpr int YSTAGES = 3;  // Z ring: stages of two 64-column chunks (32 KB, one TMA load each)
+constexpr int YSTAGES = 3;  // Z ring: stages of four 64-column chunks (64 KB, one TMA load each)
+constexpr int ZSC = 4;      // chunks per Z ring stage
 constexpr int EPI_WARPS = 8;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int THREADS = 320;
 constexpr uint32_t CHUNK = 128 * KB * 2;  // 16 KB: 128 rows x 64 bf16
-constexpr uint32_t ZSTAGE = 2 * CHUNK;     // 32 KB
+constexpr uint32_t ZSTAGE = ZSC * CHUNK;   // 64 KB
 // The A CTA loads its Y tile in 4 slabs of 32 rows x d (one TMA load per
 // slab, up to 32 KB); inside a slab the d / 64 chunks of 32 x 64 follow each
 // other (4 KB apart).
 constexpr int SLAB_ROWS = 32;
 constexpr int NSLAB = BT / SLAB_ROWS;
+constexpr int ASLOTS = 5;                  // A CTA: ring of slab slots (one tile + one slab)
 constexpr uint32_t SLAB_CHUNK = SLAB_ROWS * KB * 2;  // 4 KB
 // Z CTA layout
-constexpr uint32_t Z_X = 0;
-constexpr uint32_t Z_Y = Z_X + MAX_KC * CHUNK;          // ring of YSTAGES two-chunk stages
+// Z CTA: the stationary block X lives in TMEM (columns 256-511, copied there
+// from the ring with tcgen05.cp); shared memory is only the ring.
+constexpr uint32_t Z_Y = 0;                             // ring of YSTAGES stages
 constexpr uint32_t Z_END = Z_Y + YSTAGES * ZSTAGE;
+constexpr uint32_t Z_TMEM_X = 256;
 // A CTA layout
-constexpr uint32_t A_Y = 0;                             // one full Y tile: NSLAB slabs
-constexpr uint32_t A_P = A_Y + MAX_KC * CHUNK;          // 2 P slots of 128 x 128 bf16
+constexpr uint32_t A_Y = 0;                             // ring of ASLOTS slabs (32 x d each)
+constexpr uint32_t A_P = A_Y + ASLOTS * MAX_KC * SLAB_CHUNK;  // 2 P slots of 128 x 128 bf16
 constexpr uint32_t P_SLOT = 2 * CHUNK;                  // 32 KB
 constexpr uint32_t A_END = A_P + 2 * P_SLOT;
 constexpr uint32_t BAR_OFF = (Z_END > A_END ? Z_END : A_END);
-constexpr uint32_t SMEM_BYTES = BAR_OFF + 256 + 1024;
-constexpr uint32_t Z_TMEM_COLS = 256;
+constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;
+constexpr uint32_t Z_TMEM_COLS = 512;
 constexpr uint32_t A_TMEM_COLS = 512;
 constexpr uint32_t IDESC_Z = idesc_bf16_f32(128, BT, false, false);
 constexpr int MAX_SPLIT = 8;
@@ -177,7 +181,7 @@ __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiCon
     Chunk32 c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) c.v[j] = r[j];
-    SlowArgs none;
+    SlowArgs none = {};
     const Packed16 o = g_chunk_slow(c, k.inv_c, k.cl2e, 0, none, lse2, rel, -1, lim);
 #pragma unroll
     for (int j = 0; j < 16; ++j) out[j] = o.v[j];
@@ -236,27 +240,26 @@ template <int MODE>
 __global__ void __launch_bounds__(THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                const __grid_constant__ CUtensorMap tm_ys, const Params p) {
-  // tm_x: X blocks, box 64 x 128 x KC (the whole 128 x d block in one load);
-  // tm_y: Y tiles, box 64 x 128 x 2 (two chunks); tm_ys: Y slabs, box
-  // 64 x 32 x KC.
+  // tm_x: X blocks and tm_y: Y tiles, box 64 x 128 x 4 (four chunks, 64 KB);
+  // tm_ys: Y slabs, box 64 x 32 x KC.
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   // Z CTA barriers
   uint64_t* zy_full = bars + 0;     // [YSTAGES]
   uint64_t* zy_empty = bars + 6;    // [YSTAGES]
-  uint64_t* x_full = bars + 12;
-  uint64_t* x_empty = bars + 13;
+  uint64_t* x_free = bars + 12;     // Z: the previous unit's MMAs no longer read X in TMEM
+  uint64_t* x_ready = bars + 13;    // Z: X's tcgen05.cp have completed
   uint64_t* acc_full = bars + 14;   // [2]  Z: z tiles; A: [0] = accumulator done
   uint64_t* acc_empty = bars + 16;  // [2]  Z: z tiles; A: [0] = accumulator drained
   uint64_t* p_empty = bars + 18;    // [2]  in Z, arrived by A's MMA commit
   // A CTA barriers
   uint64_t* p_full = bars + 20;     // [2]  in A: A's expect_tx + the bytes of Z's st.async
-  uint64_t* ay_full = bars + 22;    // [NSLAB] slabs of the Y tile
-  uint64_t* ay_empty = bars + 26;   // [NSLAB]
-  uint64_t* mma_done = bars + 30;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 248);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 252);
+  uint64_t* ay_full = bars + 22;    // [ASLOTS] slab slots of the Y ring
+  uint64_t* ay_empty = bars + 28;   // [ASLOTS]
+  uint64_t* mma_done = bars + 34;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 504);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 508);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -270,15 +273,15 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(zy_full + i, 1);
       mbar_init(zy_empty + i, 1);
     }
-    mbar_init(x_full, 1);
-    mbar_init(x_empty, 1);
+    mbar_init(x_free, 1);
+    mbar_init(x_ready, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(acc_full + i, 1);
       mbar_init(acc_empty + i, EPI_WARPS);
       mbar_init(p_empty + i, 1);
       mbar_init(p_full + i, 1);
     }
-    for (int i = 0; i < NSLAB; ++i) {
+    for (int i = 0; i < ASLOTS; ++i) {
       mbar_init(ay_full + i, 1);
       mbar_init(ay_empty + i, 1);
     }
@@ -303,76 +306,99 @@ __global__ void __launch_bounds__(THREADS, 1)
     // =========================== Z CTA ===========================
     if (warp == TMA_WARP) {
       if (lane == 0) {
+        // Ring order: per unit the X block's stages, then per tile the Y
+        // tile's stages (chunks past d / 64 read zeros).
         int stage = 0;
-        uint32_t phase = 0, xph = 0;
-        bool first = true, ok = true;
+        uint32_t phase = 0;
+        bool ok = true;
         uint32_t pend = 0, pend_ph[YSTAGES] = {0, 0, 0};
-        const int npair = (p.KC + 1) / 2;
+        const int nst = (p.KC + ZSC - 1) / ZSC;
+        auto put = [&](const CUtensorMap* m, int row0, int s4) -> bool {
+          if (!mbar_wait(zy_empty + stage, phase ^ 1u, abort_flag, p.status)) return false;
+          mbar_expect_tx(zy_full + stage, ZSTAGE);
+          tma_load_3d(smem + Z_Y + stage * ZSTAGE, m, zy_full + stage, 0, row0, ZSC * s4);
+          pend |= 1u << stage;
+          pend_ph[stage] = phase;
+          if (++stage == YSTAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          return true;
+        };
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
-          if (!first) {
-            ok = mbar_wait(x_empty, xph, abort_flag, p.status);
-            xph ^= 1u;
-            if (!ok) break;
-          }
-          first = false;
-          mbar_expect_tx(x_full, p.KC * CHUNK);
-          tma_load_3d(smem + Z_X, &tm_x, x_full, 0, blk * BM, 0);
-          for (int t = t0; t < t1 && ok; ++t) {
-            for (int pr = 0; pr < npair; ++pr) {
-              ok = mbar_wait(zy_empty + stage, phase ^ 1u, abort_flag, p.status);
-              if (!ok) break;
-              // A pair past an odd KC reads zeros for its second chunk; the
-              // load still delivers the full box.
-              mbar_expect_tx(zy_full + stage, ZSTAGE);
-              tma_load_3d(smem + Z_Y + stage * ZSTAGE, &tm_y, zy_full + stage, 0, t * BT, 2 * pr);
-              pend |= 1u << stage;
-              pend_ph[stage] = phase;
-              if (++stage == YSTAGES) {
-                stage = 0;
-                phase ^= 1u;
-              }
-            }
-          }
+          for (int s4 = 0; s4 < nst && ok; ++s4) ok = put(&tm_x, blk * BM, s4);
+          for (int t = t0; t < t1 && ok; ++t)
+            for (int s4 = 0; s4 < nst && ok; ++s4) ok = put(&tm_y, t * BT, s4);
         }
         if (!ok) {
-          const unsigned long long t0 = globaltimer_ns();
+          const long long c0 = clock64();
           for (int s = 0; s < YSTAGES; ++s)
             if (pend & (1u << s))
-              while (!mbar_try_wait(smem_u32(zy_full + s), pend_ph[s]) && globaltimer_ns() - t0 < kWaitLimitNs) {
+              while (!mbar_try_wait(smem_u32(zy_full + s), pend_ph[s]) && clock64() - c0 < kWaitLimitCycles) {
               }
         }
       }
     } else if (warp == MMA_WARP) {
       if (lane == 0) {
         int stage = 0, acc = 0;
-        uint32_t phase = 0, aph = 0, xph = 0;
-        bool ok = true;
+        uint32_t phase = 0, aph = 0, fph = 0, rph = 0;
+        bool ok = true, first = true;
+        const int nst = (p.KC + ZSC - 1) / ZSC;
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
-          ok = mbar_wait(x_full, xph, abort_flag, p.status);
-          xph ^= 1u;
+          if (!first) {
+            // X in TMEM is overwritten only after the previous unit's MMAs.
+            umma_commit(x_free);
+            ok = mbar_wait(x_free, fph, abort_flag, p.status);
+            fph ^= 1u;
+            if (!ok) break;
+          }
+          first = false;
+          for (int s4 = 0; s4 < nst && ok; ++s4) {
+            ok = mbar_wait(zy_full + stage, phase, abort_flag, p.status);
+            if (!ok) break;
+            tc_fence_after();
+            for (int c = 0; c < ZSC; ++c) {
+              const int kc = ZSC * s4 + c;
+              if (kc >= p.KC) break;
+              const uint32_t xa = smem_u32(smem + Z_Y + stage * ZSTAGE + c * CHUNK);
+#pragma unroll
+              for (int k = 0; k < KB / 16; ++k)
+                tmem_cp_128x256b(tmem_base + Z_TMEM_X + static_cast<uint32_t>(kc * 32 + k * 8),
+                                 sdesc_sw128(xa + k * 32, 16, 1024));
+            }
+            umma_commit(zy_empty + stage);
+            if (++stage == YSTAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
           if (!ok) break;
+          umma_commit(x_ready);
+          ok = mbar_wait(x_ready, rph, abort_flag, p.status);
+          rph ^= 1u;
+          if (!ok) break;
+          tc_fence_after();
           for (int t = t0; t < t1 && ok; ++t) {
             ok = mbar_wait(acc_empty + acc, aph ^ 1u, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
             const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BT);
-            for (int pr = 0; pr < (p.KC + 1) / 2; ++pr) {
+            for (int s4 = 0; s4 < nst && ok; ++s4) {
               ok = mbar_wait(zy_full + stage, phase, abort_flag, p.status);
               if (!ok) break;
               tc_fence_after();
-              for (int c = 0; c < 2; ++c) {
-                const int kc = 2 * pr + c;
+              for (int c = 0; c < ZSC; ++c) {
+                const int kc = ZSC * s4 + c;
                 if (kc >= p.KC) break;
-                const uint32_t xa = smem_u32(smem + Z_X + kc * CHUNK);
                 const uint32_t ya = smem_u32(smem + Z_Y + stage * ZSTAGE + c * CHUNK);
 #pragma unroll
                 for (int k = 0; k < KB / 16; ++k)
-                  umma_bf16(d_tmem, sdesc_sw128(xa + k * 32, 16, 1024), sdesc_sw128(ya + k * 32, 16, 1024), IDESC_Z,
-                            (kc | k) != 0 ? 1u : 0u);
+                  umma_bf16_ts(d_tmem, tmem_base + Z_TMEM_X + static_cast<uint32_t>(kc * 32 + k * 8),
+                               sdesc_sw128(ya + k * 32, 16, 1024), IDESC_Z, (kc | k) != 0 ? 1u : 0u);
               }
               umma_commit(zy_empty + stage);
               if (++stage == YSTAGES) {
@@ -385,11 +411,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             acc ^= 1;
             if (acc == 0) aph ^= 1u;
           }
-          if (ok) umma_commit(x_empty);
         }
         umma_commit(mma_done);
-        const unsigned long long t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(mma_done), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        const long long c0 = clock64();
+        while (!mbar_try_wait(smem_u32(mma_done), 0) && clock64() - c0 < kWaitLimitCycles) {
         }
       }
     } else {
@@ -505,7 +530,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tmem_ld32(tb, ra);
           tmem_ld_wait();
           reg_fence32(ra);
-          tmem_ld32(tb + 32, rc);  // in flight while chunk 0 is processed
+          tmem_ld32(tb + 32, rc);
           do_chunk(ra, 0);
           tmem_ld_wait();
           reg_fence32(rc);
@@ -524,37 +549,42 @@ __global__ void __launch_bounds__(THREADS, 1)
     // =========================== A CTA ===========================
     if (warp == TMA_WARP) {
       if (lane == 0) {
-        // The Y tile arrives in NSLAB slabs of 32 rows x d, one load each.
-        uint32_t yph = 0;
+        // The Y tiles arrive in slabs of 32 rows x d (one load each) through
+        // a ring of ASLOTS slab slots.
+        int rs = 0;
+        uint32_t rph = 0;
         bool ok = true;
-        uint32_t pend = 0, pend_ph[NSLAB] = {0, 0, 0, 0};
+        uint32_t pend = 0, pend_ph[ASLOTS] = {0, 0, 0, 0, 0};
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
           for (int t = t0; t < t1 && ok; ++t) {
             for (int sl = 0; sl < NSLAB; ++sl) {
-              ok = mbar_wait(ay_empty + sl, yph ^ 1u, abort_flag, p.status);
+              ok = mbar_wait(ay_empty + rs, rph ^ 1u, abort_flag, p.status);
               if (!ok) break;
-              mbar_expect_tx(ay_full + sl, p.KC * SLAB_CHUNK);
-              tma_load_3d(smem + A_Y + sl * p.KC * SLAB_CHUNK, &tm_ys, ay_full + sl, 0, t * BT + sl * SLAB_ROWS, 0);
-              pend |= 1u << sl;
-              pend_ph[sl] = yph;
+              mbar_expect_tx(ay_full + rs, p.KC * SLAB_CHUNK);
+              tma_load_3d(smem + A_Y + rs * p.KC * SLAB_CHUNK, &tm_ys, ay_full + rs, 0, t * BT + sl * SLAB_ROWS, 0);
+              pend |= 1u << rs;
+              pend_ph[rs] = rph;
+              if (++rs == ASLOTS) {
+                rs = 0;
+                rph ^= 1u;
+              }
             }
-            yph ^= 1u;
           }
         }
         if (!ok) {
-          const unsigned long long t0 = globaltimer_ns();
-          for (int s = 0; s < NSLAB; ++s)
+          const long long c0 = clock64();
+          for (int s = 0; s < ASLOTS; ++s)
             if (pend & (1u << s))
-              while (!mbar_try_wait(smem_u32(ay_full + s), pend_ph[s]) && globaltimer_ns() - t0 < kWaitLimitNs) {
+              while (!mbar_try_wait(smem_u32(ay_full + s), pend_ph[s]) && clock64() - c0 < kWaitLimitCycles) {
               }
         }
       }
     } else if (warp == MMA_WARP) {
       if (lane == 0) {
-        uint32_t yph = 0, sph = 0, dph = 0;
-        int slot = 0;
+        uint32_t rph = 0, sph = 0, dph = 0;
+        int slot = 0, rs = 0;
         bool ok = true;
         // The accumulator's d columns in two N halves of nh0 and nh1 chunks.
         const int nh0 = (p.KC + 1) / 2;
@@ -578,9 +608,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             tc_fence_after();
             const uint32_t pa = smem_u32(smem + A_P + slot * P_SLOT);
             for (int ks = 0; ks < BT / 16 && ok; ++ks) {
-              const int sl = ks / (SLAB_ROWS / 16);
               if (ks % (SLAB_ROWS / 16) == 0) {
-                ok = mbar_wait(ay_full + sl, yph, abort_flag, p.status);
+                ok = mbar_wait(ay_full + rs, rph, abort_flag, p.status);
                 if (!ok) break;
                 tc_fence_after();
               }
@@ -590,25 +619,30 @@ __global__ void __launch_bounds__(THREADS, 1)
                 if (nh == 0) continue;
                 const uint32_t idesc = idesc_bf16_f32(128, 64 * nh, false, true);
                 // MN-major B: N = 64 nh columns of d in chunks 4 KB apart inside
-                // the slab; K-step ks covers rows 16 (ks % 2) .. +15 of slab sl.
-                const uint32_t yb = smem_u32(smem + A_Y + sl * p.KC * SLAB_CHUNK + half * nh0 * SLAB_CHUNK);
+                // the slab; K-step ks covers rows 16 (ks % 2) .. +15 of its slab.
+                const uint32_t yb = smem_u32(smem + A_Y + rs * p.KC * SLAB_CHUNK + half * nh0 * SLAB_CHUNK);
                 const uint64_t bd = sdesc_sw128(yb + (ks % (SLAB_ROWS / 16)) * 2048, SLAB_CHUNK, 1024);
                 umma_bf16(tmem_base + static_cast<uint32_t>(half * 64 * nh0), ad, bd, idesc,
                           (t != t0 || ks != 0) ? 1u : 0u);
               }
-              if (ks % (SLAB_ROWS / 16) == SLAB_ROWS / 16 - 1) umma_commit(ay_empty + sl);
+              if (ks % (SLAB_ROWS / 16) == SLAB_ROWS / 16 - 1) {
+                umma_commit(ay_empty + rs);
+                if (++rs == ASLOTS) {
+                  rs = 0;
+                  rph ^= 1u;
+                }
+              }
             }
             if (!ok) break;
             umma_commit_mc(p_empty + slot, static_cast<uint16_t>(1u << 0));  // P slot free (Z CTA)
-            yph ^= 1u;
             slot ^= 1;
             if (slot == 0) sph ^= 1u;
           }
           if (ok) umma_commit(acc_full);  // accumulator of this unit complete
         }
         umma_commit(mma_done);
-        const unsigned long long t0 = globaltimer_ns();
-        while (!mbar_try_wait(smem_u32(mma_done), 0) && globaltimer_ns() - t0 < kWaitLimitNs) {
+        const long long c0 = clock64();
+        while (!mbar_try_wait(smem_u32(mma_done), 0) && clock64() - c0 < kWaitLimitCycles) {
         }
       }
     } else {
@@ -806,10 +840,10 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
                   int accumulate, unsigned* status, void* scratch, int sms, cudaStream_t s) {
   const uint32_t kc = static_cast<uint32_t>(d / KB);
   CUtensorMap tm_hx, tm_wx, tm_hy, tm_wy, tm_hs, tm_ws;
-  if (int rc = make_map_bf16_3d(&tm_hx, h, d, N, ldh * 2, BM, kc); rc) return rc;
-  if (int rc = make_map_bf16_3d(&tm_wx, W, d, V, d * 2, BM, kc); rc) return rc;
-  if (int rc = make_map_bf16_3d(&tm_hy, h, d, N, ldh * 2, BT, 2); rc) return rc;
-  if (int rc = make_map_bf16_3d(&tm_wy, W, d, V, d * 2, BT, 2); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_hx, h, d, N, ldh * 2, BM, ZSC); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_wx, W, d, V, d * 2, BM, ZSC); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_hy, h, d, N, ldh * 2, BT, ZSC); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_wy, W, d, V, d * 2, BT, ZSC); rc) return rc;
   if (int rc = make_map_bf16_3d(&tm_hs, h, d, N, ldh * 2, SLAB_ROWS, kc); rc) return rc;
   if (int rc = make_map_bf16_3d(&tm_ws, W, d, V, d * 2, SLAB_ROWS, kc); rc) return rc;
   const int clusters_max = max_clusters(sms);

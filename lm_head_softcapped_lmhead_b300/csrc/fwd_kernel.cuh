@@ -10,56 +10,65 @@
 // TiedEmbeddings) and softcapped logits ("HYDRA Golf" stack list: "fused
 // softcapped CE kernel").
 //
-// Design (one CTA per SM, persistent):
-//  * work = tiles (row block of 128 rows) x (vocab tile of 128); CTA b takes
-//    the contiguous tile range [b T / G, (b+1) T / G) in row-block-major
-//    order ("segments" of one row block).
-//  * the h block of the current row block lives in TMEM (256 of the 512
-//    columns, bf16 packed two per column) and is the A operand of every MMA;
-//    shared memory is a 3-stage ring of 64 KB TMA loads (four 64-column
-//    chunks of 128 rows each) that carries first the h block (copied to
-//    TMEM with tcgen05.cp) and then the W tiles.  TMA sustains only a few
-//    million loads per second per SM, so the loads are as large as the ring
-//    allows; 128+ KB stay in flight to cover the L2 latency under load.
-//  * warp 8 (one lane) issues the TMA loads; warp 9 (one lane) issues
-//    tcgen05.cp and tcgen05.mma (M=128, N=128, K=16) into one of two TMEM
-//    accumulators (columns 0-127 and 128-255).
-//  * warps 0-7: epilogue.  Warp w reads TMEM lanes 32 (w % 4) .. +31 (its 32
-//    rows) and columns 64 (w / 4) .. +63 of the tile.  Per logit:
-//    e = 2^(c log2(e) tanh(z/c)) with tanh from the minimax polynomial,
-//    summed in fp32 over the segment.  No running max is needed: |s| < c,
-//    so S = sum e^s lies in (V e^-c, V e^c) and cannot overflow for the
-//    accepted c (the host rejects c > c_max(V)).
+// Design (2-CTA clusters, persistent; tcgen05 pair MMAs):
+//  * work = tiles (pair of row blocks = 256 rows) x (vocab tile of 256);
+//    cluster p takes the contiguous tile range [p T / P, (p+1) T / P) in
+//    row-pair-major order ("segments" of one row pair).
+//  * CTA r of the pair keeps its 128 rows of h (128 x d bf16, one 3-D TMA
+//    load) in shared memory and loads its half (128 vocab rows) of each W
+//    tile in 32 KB loads (two 64-column chunks) through a 3-stage ring.  The
+//    pair leader issues tcgen05.mma.cta_group::2 M=256 N=256 K=16: each CTA
+//    supplies its rows of h and its half of W, and receives its 128 rows x
+//    256 columns of z in its own TMEM (two accumulators = all 512 columns).
+//    Per SM this halves the W bytes per FLOP (L2 -> SM and shared memory)
+//    relative to a one-CTA M=128 tile, which is what bounds this head.
+//  * loads complete on the leader's barriers; the leader's commits arrive on
+//    both CTAs' barriers; both CTAs' epilogue warps release an accumulator
+//    on the leader's barrier.
+//  * warps 0-7 of each CTA: epilogue.  Warp w reads TMEM lanes 32 (w % 4) ..
+//    +31 (its 32 rows) and columns 128 (w / 4) .. +127 of the tile.  Per
+//    logit: e = 2^(c log2(e) tanh(z/c)) with tanh from the minimax
+//    polynomial (packed fp32x2), summed in fp32 over the segment.  No running
+//    max is needed: |s| < c, so S = sum e^s lies in (V e^-c, V e^c) and
+//    cannot overflow for the accepted c (the host rejects c > c_max(V)).
 //  * outputs: per (segment, column half) the partial sum into
-//    part[2 s + half][row], s = the segment's first tile inside its row block
-//    (< VT); the target logit s_t into
-//    st[row] by the one thread whose columns hold t.  A finalize kernel adds
-//    the partials in a fixed order (deterministic) and forms lse and nll.
+//    part[2 s + half][row], s = the segment's first tile inside its row pair
+//    (< VT); the target logit s_t into st[row] by the one thread whose
+//    columns hold t.  A finalize kernel adds the partials in a fixed order
+//    (deterministic) and forms lse and nll.
 #pragma once
+#include <cuda_runtime.h>
+
+#include <string>
+
 #include "ptx.cuh"
 #include "softcap_math.cuh"
 
 namespace lmce {
+void set_last_error(const std::string& s);
 namespace fwdk {
 
-constexpr int BM = 128;        // rows per block (TMEM lanes, UMMA M)
-constexpr int BN = 128;        // vocab per tile (UMMA N)
+constexpr int BM = 128;        // rows per CTA (TMEM lanes); a pair covers 256
+constexpr int PAIR_ROWS = 2 * BM;
+constexpr int BN = 256;        // vocab per tile (pair MMA N)
+constexpr int HALF_N = BN / 2; // vocab rows of a tile loaded by each CTA
 constexpr int KB = 64;         // K elements per chunk (one 128-byte swizzle row)
+constexpr int SC = 2;          // chunks per ring stage (one 32 KB TMA load)
 constexpr int STAGES = 3;      // ring depth
-constexpr int SC = 4;          // 64-column chunks per stage (one 64 KB TMA load)
 constexpr int MAX_KC = 8;      // d <= 512
 constexpr int EPI_WARPS = 8;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
 constexpr int THREADS = 320;
-constexpr uint32_t CHUNK = 128 * KB * 2;   // 16 KB: 128 rows x 64 bf16
-constexpr uint32_t STAGE = SC * CHUNK;     // 64 KB
-constexpr uint32_t SMEM_RING = 0;
+constexpr uint32_t X_CHUNK = BM * KB * 2;      // 16 KB: 128 rows x 64
+constexpr uint32_t W_CHUNK = HALF_N * KB * 2;  // 16 KB: 128 vocab rows x 64
+constexpr uint32_t STAGE = SC * W_CHUNK;       // 32 KB
+constexpr uint32_t SMEM_X = 0;
+constexpr uint32_t SMEM_RING = SMEM_X + MAX_KC * X_CHUNK;
 constexpr uint32_t SMEM_BAR = SMEM_RING + STAGES * STAGE;
 constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + barriers + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_X = 256;           // h block: columns 256-511
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, false, false);
+constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_ROWS, BN, false, false);
 
 struct Params {
   int N;                // rows addressed by the h tensor map
@@ -152,89 +161,101 @@ __global__ void __launch_bounds__(THREADS, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
-  uint64_t* full = bars;            // [STAGES]
-  uint64_t* empty = bars + 8;       // [STAGES]
-  uint64_t* acc_full = bars + 16;   // [2]
-  uint64_t* acc_empty = bars + 18;  // [2]
-  uint64_t* x_free = bars + 20;     // the previous segment's MMAs no longer read the h block
-  uint64_t* x_ready = bars + 22;    // the h block's tcgen05.cp have completed
-  uint64_t* mma_done = bars + 21;
+  uint64_t* full = bars;            // [STAGES] leader: both CTAs' W bytes
+  uint64_t* empty = bars + 4;       // [STAGES] each CTA: the pair MMAs are done with the stage
+  uint64_t* x_full = bars + 8;      // leader: both CTAs' h bytes
+  uint64_t* x_empty = bars + 9;     // each CTA: the segment's MMAs are done with h
+  uint64_t* acc_full = bars + 10;   // [2] each CTA
+  uint64_t* acc_empty = bars + 12;  // [2] leader: 8 warps of each CTA
+  uint64_t* mma_done = bars + 14;   // each CTA
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 192);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 196);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const bool leader = (rank == 0);
 
   const int n_rows = p.n_rows ? min(*p.n_rows, p.N) : p.N;
-  const int NB = (n_rows + BM - 1) / BM;
-  const long long T = static_cast<long long>(NB) * p.VT;
-  const long long G = gridDim.x;
-  const long long g_begin = static_cast<long long>(blockIdx.x) * T / G;
-  const long long g_end = static_cast<long long>(blockIdx.x + 1) * T / G;
-  const int npair = (p.KC + SC - 1) / SC;  // ring stages per h block / W tile
+  const int NBP = (n_rows + PAIR_ROWS - 1) / PAIR_ROWS;
+  const long long T = static_cast<long long>(NBP) * p.VT;
+  const long long P = gridDim.x / 2;
+  const long long pair = blockIdx.x / 2;
+  const long long g_begin = pair * T / P;
+  const long long g_end = (pair + 1) * T / P;
+  const int npair = (p.KC + SC - 1) / SC;  // ring stages per W tile
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
       mbar_init(full + i, 1);
       mbar_init(empty + i, 1);
     }
+    mbar_init(x_full, 1);
+    mbar_init(x_empty, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(acc_full + i, 1);
-      mbar_init(acc_empty + i, EPI_WARPS);
+      mbar_init(acc_empty + i, 2 * EPI_WARPS);
     }
-    mbar_init(x_free, 1);
-    mbar_init(x_ready, 1);
     mbar_init(mma_done, 1);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
   }
   if (warp == MMA_WARP) {
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc_pair(tmem_slot, TMEM_COLS);
+    tmem_relinquish_pair();
   }
   if (warp == TMA_WARP && lane == 0) {
     tma_prefetch_desc(&tm_h);
     tma_prefetch_desc(&tm_w);
   }
   tc_fence_before();
-  __syncthreads();
+  // Both CTAs' barriers exist before any load or arrive targets them.
+  cluster_arrive();
+  cluster_wait();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
   if (warp == TMA_WARP) {
     if (lane == 0 && g_begin < g_end) {
-      // Ring order per tile: (at a new row block) the h block's stages, then
-      // the W tile's stages.  Chunks past d / 64 read zeros.
+      const uint32_t lead_x_full = mapa_shared(smem_u32(x_full), 0);
       int stage = 0;
-      uint32_t phase = 0;
-      int prev_rb = -1;
+      uint32_t phase = 0, xph = 0;
+      int prev_rbp = -1;
       uint32_t pend = 0;
       uint32_t pend_ph[STAGES] = {0, 0, 0};
       bool ok = true;
-      auto put = [&](const CUtensorMap* m, int row0, int pr) -> bool {
-        if (!mbar_wait(empty + stage, phase ^ 1u, abort_flag, p.status)) return false;
-        mbar_expect_tx(full + stage, STAGE);
-        tma_load_3d(smem + SMEM_RING + stage * STAGE, m, full + stage, 0, row0, SC * pr);
-        pend |= 1u << stage;
-        pend_ph[stage] = phase;
-        if (++stage == STAGES) {
-          stage = 0;
-          phase ^= 1u;
-        }
-        return true;
-      };
       for (long long g = g_begin; g < g_end && ok; ++g) {
-        const int rb = static_cast<int>(g / p.VT);
+        const int rbp = static_cast<int>(g / p.VT);
         const int vt = static_cast<int>(g % p.VT);
-        if (rb != prev_rb) {
-          for (int pr = 0; pr < npair && ok; ++pr) ok = put(&tm_h, rb * BM, pr);
-          prev_rb = rb;
+        if (rbp != prev_rbp) {
+          if (prev_rbp >= 0) {
+            ok = mbar_wait(x_empty, xph, abort_flag, p.status);
+            xph ^= 1u;
+            if (!ok) break;
+          }
+          if (leader) mbar_expect_tx(x_full, 2u * p.KC * X_CHUNK);
+          tma_load_3d_pair(smem + SMEM_X, &tm_h, lead_x_full, 0, rbp * PAIR_ROWS + static_cast<int>(rank) * BM, 0);
+          prev_rbp = rbp;
         }
-        for (int pr = 0; pr < npair && ok; ++pr) ok = put(&tm_w, vt * BN, pr);
+        for (int pr = 0; pr < npair; ++pr) {
+          ok = mbar_wait(empty + stage, phase ^ 1u, abort_flag, p.status);
+          if (!ok) break;
+          if (leader) mbar_expect_tx(full + stage, 2u * STAGE);
+          tma_load_3d_pair(smem + SMEM_RING + stage * STAGE, &tm_w, mapa_shared(smem_u32(full + stage), 0), 0,
+                           vt * BN + static_cast<int>(rank) * HALF_N, SC * pr);
+          pend |= 1u << stage;
+          pend_ph[stage] = phase;
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
       }
-      if (!ok) {
-        // Let every issued copy land before the CTA can exit (bounded).
+      if (!ok && leader) {
+        // Bounded wait for issued copies to land (the leader's full barriers
+        // count both CTAs' bytes; the peer leaves only after the leader,
+        // through the final cluster barrier).
         const long long t0 = clock64();
         for (int s = 0; s < STAGES; ++s)
           if (pend & (1u << s))
@@ -244,21 +265,23 @@ __global__ void __launch_bounds__(THREADS, 1)
     }
   } else if (warp == MMA_WARP) {
     if (lane == 0 && g_begin < g_end) {
-      int stage = 0, acc = 0;
-      uint32_t phase = 0, aph = 0, xph = 0, rph = 0;
-      int prev_rb = -1;
-      bool ok = true;
-      for (long long g = g_begin; g < g_end && ok; ++g) {
-        const int rb = static_cast<int>(g / p.VT);
-        if (rb != prev_rb) {
-          if (prev_rb >= 0) {
-            // The h block in TMEM is overwritten only after the previous
-            // segment's MMAs are done with it.
-            umma_commit(x_free);
-            ok = mbar_wait(x_free, xph, abort_flag, p.status);
+      if (leader) {
+        int stage = 0, acc = 0;
+        uint32_t phase = 0, aph = 0, xph = 0;
+        int prev_rbp = -1;
+        bool ok = true;
+        for (long long g = g_begin; g < g_end && ok; ++g) {
+          const int rbp = static_cast<int>(g / p.VT);
+          if (rbp != prev_rbp) {
+            ok = mbar_wait(x_full, xph, abort_flag, p.status);
             xph ^= 1u;
             if (!ok) break;
+            prev_rbp = rbp;
           }
+          ok = mbar_wait<true>(acc_empty + acc, aph ^ 1u, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
           for (int pr = 0; pr < npair && ok; ++pr) {
             ok = mbar_wait(full + stage, phase, abort_flag, p.status);
             if (!ok) break;
@@ -266,57 +289,30 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int c = 0; c < SC; ++c) {
               const int kc = SC * pr + c;
               if (kc >= p.KC) break;
-              const uint32_t xa = smem_u32(smem + SMEM_RING + stage * STAGE + c * CHUNK);
+              const uint32_t xa = smem_u32(smem + SMEM_X + kc * X_CHUNK);
+              const uint32_t ya = smem_u32(smem + SMEM_RING + stage * STAGE + c * W_CHUNK);
 #pragma unroll
               for (int k = 0; k < KB / 16; ++k)
-                tmem_cp_128x256b(tmem_base + TMEM_X + static_cast<uint32_t>(kc * 32 + k * 8),
-                                 sdesc_sw128(xa + k * 32, 16, 1024));
+                umma_bf16_pair(d_tmem, sdesc_sw128(xa + k * 32, 16, 1024), sdesc_sw128(ya + k * 32, 16, 1024), IDESC,
+                               (kc | k) != 0 ? 1u : 0u);
             }
-            umma_commit(empty + stage);
+            umma_commit_pair(empty + stage, 0x3);
             if (++stage == STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
           if (!ok) break;
-          // The MMAs below read the copied block: wait for the copies.
-          umma_commit(x_ready);
-          ok = mbar_wait(x_ready, rph, abort_flag, p.status);
-          rph ^= 1u;
-          if (!ok) break;
-          tc_fence_after();
-          prev_rb = rb;
+          umma_commit_pair(acc_full + acc, 0x3);
+          const bool seg_end = (g + 1 == g_end) || ((g + 1) / p.VT != rbp);
+          if (seg_end) umma_commit_pair(x_empty, 0x3);
+          acc ^= 1;
+          if (acc == 0) aph ^= 1u;
         }
-        ok = mbar_wait(acc_empty + acc, aph ^ 1u, abort_flag, p.status);
-        if (!ok) break;
-        tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int pr = 0; pr < npair && ok; ++pr) {
-          ok = mbar_wait(full + stage, phase, abort_flag, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          for (int c = 0; c < SC; ++c) {
-            const int kc = SC * pr + c;
-            if (kc >= p.KC) break;
-            const uint32_t ya = smem_u32(smem + SMEM_RING + stage * STAGE + c * CHUNK);
-#pragma unroll
-            for (int k = 0; k < KB / 16; ++k)
-              umma_bf16_ts(d_tmem, tmem_base + TMEM_X + static_cast<uint32_t>(kc * 32 + k * 8),
-                           sdesc_sw128(ya + k * 32, 16, 1024), IDESC, (kc | k) != 0 ? 1u : 0u);
-          }
-          umma_commit(empty + stage);
-          if (++stage == STAGES) {
-            stage = 0;
-            phase ^= 1u;
-          }
-        }
-        if (!ok) break;
-        umma_commit(acc_full + acc);
-        acc ^= 1;
-        if (acc == 0) aph ^= 1u;
+        umma_commit_pair(mma_done, 0x3);
       }
-      // All issued tcgen05 work completes before TMEM is released (bounded).
-      umma_commit(mma_done);
+      // Both CTAs: every pair MMA writing this CTA's TMEM completes before
+      // TMEM is released (bounded).
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(mma_done), 0) && clock64() - t0 < kWaitLimitCycles) {
       }
@@ -324,60 +320,79 @@ __global__ void __launch_bounds__(THREADS, 1)
   } else {
     // ---------------- epilogue warps ----------------
     const int q = warp & 3;    // TMEM lane quarter -> rows 32q .. 32q+31
-    const int hc = warp >> 2;  // column half of the tile (64 columns)
+    const int hc = warp >> 2;  // column half of the tile (128 columns)
     float2 k2[kTanhTerms];
 #pragma unroll
     for (int i = 0; i < kTanhTerms; ++i) k2[i] = make_float2(p.k[i], p.k[i]);
+    const uint32_t lead_acc_empty = mapa_shared(smem_u32(acc_empty), 0);
     int acc = 0;
     uint32_t aph = 0;
-    int cur_rb = -1;
+    int cur_rbp = -1;
     int row = 0;
     long long t = -1;
     float seg_sum = 0.f;
     for (long long g = g_begin; g < g_end; ++g) {
-      const int rb = static_cast<int>(g / p.VT);
+      const int rbp = static_cast<int>(g / p.VT);
       const int vt = static_cast<int>(g % p.VT);
-      if (rb != cur_rb) {
-        row = rb * BM + q * 32 + lane;
+      if (rbp != cur_rbp) {
+        row = rbp * PAIR_ROWS + static_cast<int>(rank) * BM + q * 32 + lane;
         t = (row < n_rows) ? p.tgt[row] : -1;
-        cur_rb = rb;
+        cur_rbp = rbp;
         seg_sum = 0.f;
       }
       if (!mbar_wait(acc_full + acc, aph, abort_flag, p.status)) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + hc * 64);
-      const int col0 = vt * BN + hc * 64;
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BN + hc * 128);
+      const int col0 = vt * BN + hc * 128;
       float st_val = 0.f;
       bool st_hit = false;
-      // Two 32-column chunks; the TMEM load of the second is in flight while
-      // the first is processed.
+      // Four 32-column chunks; the TMEM load of chunk i+1 is in flight while
+      // chunk i is processed.
       uint32_t ra[32], rc[32];
       tmem_ld32(tbase, ra);
       tmem_ld_wait();
       reg_fence32(ra);
-      tmem_ld32(tbase + 32, rc);
-      {
-        const int lim = min(32, p.V - col0);
-        if (lim > 0) seg_sum += chunk_sum(ra, k2, p, lim);
-        pick_target(ra, t - col0, p, st_val, st_hit);
-      }
-      tmem_ld_wait();
-      reg_fence32(rc);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acc_empty + acc);  // TMEM buffer free: both chunks are in registers
-      {
-        const int lim = min(32, p.V - (col0 + 32));
-        if (lim > 0) seg_sum += chunk_sum(rc, k2, p, lim);
-        pick_target(rc, t - (col0 + 32), p, st_val, st_hit);
+#pragma unroll
+      for (int ch = 0; ch < 4; ch += 2) {
+        tmem_ld32(tbase + (ch + 1) * 32, rc);
+        {
+          const int cbase = col0 + ch * 32;
+          const int lim = min(32, p.V - cbase);
+          if (lim > 0) seg_sum += chunk_sum(ra, k2, p, lim);
+          pick_target(ra, t - cbase, p, st_val, st_hit);
+        }
+        tmem_ld_wait();
+        reg_fence32(rc);
+        if (ch + 2 < 4) tmem_ld32(tbase + (ch + 2) * 32, ra);
+        if (ch + 2 >= 4) {
+          // All of this warp's columns are in registers: release the buffer.
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            if (leader)
+              mbar_arrive(acc_empty + acc);
+            else
+              mbar_arrive_cluster(lead_acc_empty + static_cast<uint32_t>(acc) * 8u);
+          }
+        }
+        {
+          const int cbase = col0 + (ch + 1) * 32;
+          const int lim = min(32, p.V - cbase);
+          if (lim > 0) seg_sum += chunk_sum(rc, k2, p, lim);
+          pick_target(rc, t - cbase, p, st_val, st_hit);
+        }
+        if (ch + 2 < 4) {
+          tmem_ld_wait();
+          reg_fence32(ra);
+        }
       }
       if (row < n_rows) {
         if (st_hit) p.st[row] = st_val;
-        const bool seg_end = (g + 1 == g_end) || ((g + 1) / p.VT != rb);
+        const bool seg_end = (g + 1 == g_end) || ((g + 1) / p.VT != rbp);
         if (seg_end) {
-          // Slot: this segment's first tile inside row block rb (< VT, unique
-          // among the CTAs covering rb).
-          const long long g0 = static_cast<long long>(rb) * p.VT;
+          // Slot: this segment's first tile inside its row pair (< VT,
+          // unique among the clusters covering the pair).
+          const long long g0 = static_cast<long long>(rbp) * p.VT;
           const int slot = static_cast<int>(g_begin > g0 ? g_begin - g0 : 0);
           p.part[static_cast<size_t>(2 * slot + hc) * p.N_pad + row] = seg_sum;
         }
@@ -389,10 +404,58 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  // No CTA leaves while its peer may still signal its barriers.
+  cluster_arrive();
+  cluster_wait();
   if (warp == MMA_WARP) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc_pair(tmem_base, TMEM_COLS);
   }
+}
+
+// Co-resident 2-CTA clusters of fwd_kernel (cached per process).
+inline int max_clusters(int sms) {
+  static int cached = 0;
+  if (cached) return cached;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * (sms / 2));
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel, &cfg) != cudaSuccess || n <= 0) {
+    (void)cudaGetLastError();
+    n = sms / 2;
+  }
+  cached = n;
+  return n;
+}
+
+inline int launch(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const Params& p, int pairs, cudaStream_t s) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2 * pairs);
+  cfg.blockDim = dim3(THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&cfg, fwd_kernel, tm_h, tm_w, p);
+  if (e != cudaSuccess) {
+    set_last_error(std::string("fwd_kernel launch: ") + cudaGetErrorString(e));
+    return 3;
+  }
+  return 0;
 }
 
 }  // namespace fwdk

@@ -54,9 +54,9 @@ Layout make_layout(int64_t N, int64_t V, int64_t d, unsigned flags) {
   o = up(o + 64);
   L.bpb = o;
   o = up(o + sizeof(lmce::BpbPartial) * lmce::kBpbBlocks);
-  const int64_t N_pad = cdiv(N, lmce::fwdk::BM) * lmce::fwdk::BM;
+  const int64_t N_pad = cdiv(N, lmce::fwdk::PAIR_ROWS) * lmce::fwdk::PAIR_ROWS;
   const int64_t VT = cdiv(V, lmce::fwdk::BN);
-  L.part = o;  // at most VT CTAs cover one row block: 2 VT slots per row
+  L.part = o;  // at most VT clusters cover one row pair: 2 VT slots per row
   o = up(o + sizeof(float) * 2 * VT * N_pad);
   L.st = o;
   o = up(o + sizeof(float) * N_pad);
@@ -261,8 +261,10 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
   }
 
   CUtensorMap tm_h, tm_w;
-  if (int rc = lmce::make_map_bf16_3d(&tm_h, hx, d, N, ldx * 2, lmce::fwdk::BM, lmce::fwdk::SC); rc) return rc;
-  if (int rc = lmce::make_map_bf16_3d(&tm_w, W, d, V, d * 2, lmce::fwdk::BN, lmce::fwdk::SC); rc) return rc;
+  // h: each CTA's 128 x d rows in one load; W: 128 vocab rows x 2 chunks.
+  if (int rc = lmce::make_map_bf16_3d(&tm_h, hx, d, N, ldx * 2, lmce::fwdk::BM, static_cast<uint32_t>(d / 64)); rc)
+    return rc;
+  if (int rc = lmce::make_map_bf16_3d(&tm_w, W, d, V, d * 2, lmce::fwdk::HALF_N, lmce::fwdk::SC); rc) return rc;
 
   lmce::fwdk::Params p{};
   p.N = static_cast<int>(N);
@@ -271,7 +273,7 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
   p.d = static_cast<int>(d);
   p.KC = static_cast<int>(d / 64);
   p.VT = static_cast<int>(cdiv(V, lmce::fwdk::BN));
-  p.N_pad = static_cast<int>(cdiv(N, lmce::fwdk::BM) * lmce::fwdk::BM);
+  p.N_pad = static_cast<int>(cdiv(N, lmce::fwdk::PAIR_ROWS) * lmce::fwdk::PAIR_ROWS);
   p.tgt = tg;
   p.inv_c = 1.0f / c;
   p.c = c;
@@ -280,16 +282,16 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
   p.part = reinterpret_cast<float*>(w + L.part);
   p.st = reinterpret_cast<float*>(w + L.st);
   p.status = status;
-
-  const int64_t T_max = cdiv(N, lmce::fwdk::BM) * p.VT;
-  const int grid = static_cast<int>(std::min<int64_t>(T_max, di.sms));
   p.maxseg = p.VT;
+
+  const int64_t T_max = cdiv(N, lmce::fwdk::PAIR_ROWS) * p.VT;
+  const int pairs = static_cast<int>(std::min<int64_t>(T_max, lmce::fwdk::max_clusters(di.sms)));
   lmce::count_launches(2);
-  lmce::fwdk::fwd_kernel<<<grid, lmce::fwdk::THREADS, lmce::fwdk::SMEM_BYTES, s>>>(tm_h, tm_w, p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "fwd_kernel launch");
+  if (int rc = lmce::fwdk::launch(tm_h, tm_w, p, pairs, s); rc) return rc;
+  cudaError_t e = cudaSuccess;
   const int fblocks = static_cast<int>(std::min<int64_t>(cdiv(N, 256), int64_t(di.sms) * 4));
-  lmce::fwd_finalize_kernel<<<fblocks, 256, 0, s>>>(p.part, p.VT, grid, p.N_pad, p.st, tg, nrows_dev,
+  lmce::fwd_finalize_kernel<<<fblocks, 256, 0, s>>>(p.part, p.VT, pairs, lmce::fwdk::PAIR_ROWS, p.N_pad, p.st, tg,
+                                                    nrows_dev,
                                                     static_cast<int>(N), static_cast<int>(V), idx, nll, lse, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fwd_finalize launch");
