@@ -155,6 +155,27 @@ LMCE_API int lmce_bpb(const lmce_bpb_acc* acc, double* bpb_out);
 LMCE_API int lmhead_int4_dequant(const uint8_t* Wq, const lmce_f16* scales, int64_t V, int64_t d, int group, lmce_bf16* out,
                         void* stream);
 
+/* Forward that allocates nothing and takes no workspace.  For callers that
+ * cannot give the library device memory: code whose host process owns every
+ * byte of device memory through its own pool and forbids other allocations,
+ * or code on a path where cudaMalloc's implicit device synchronisation is not
+ * acceptable.  There is no counterpart of this call in the pages; it is the
+ * same computation as lmhead_ce_fwd without a row mask.
+ * The scratch (about 16.3 MiB) is a static device array of this library:
+ * every GPU that loads the library holds it until the process exits, and
+ * all calls on one device share it, so calls that overlap on the GPU (other
+ * streams, other threads) race and must be serialised by the caller.
+ * Limits: N <= 65536 and V <= 8192 (else LMCE_EINVAL); d and the softcap as
+ * for lmhead_ce_fwd.  The first call on a device looks up the scratch's
+ * device address (cudaGetSymbolAddress); make that first call before any
+ * stream capture.  A target outside [0, V) gives nll = NaN for that row (the
+ * status word of this scratch is not readable by the caller).
+ * Arguments: as lmhead_ce_fwd (all pointers device pointers; stream is a
+ * cudaStream_t). */
+LMCE_API int lmhead_ce_fwd_noalloc(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V,
+                                   int64_t d, const int64_t* tgt, float softcap, float* nll, float* lse,
+                                   void* stream);
+
 /* Synchronise stream, then read and clear the workspace's device status
  * word.  *code receives LMCE_OK, LMCE_EDATA or LMCE_ETIMEOUT (the most
  * severe recorded).  Returns LMCE_ECUDA if the synchronisation fails. */

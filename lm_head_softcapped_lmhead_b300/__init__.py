@@ -29,7 +29,7 @@ LMCE_WS_INT4 = 2
 EXPORTS = (
     "lmce_workspace_bytes", "lmce_workspace_init", "lmce_softcap_max", "lmhead_ce_fwd", "lmhead_ce_bwd",
     "lmhead_ce_fwd_int4", "lmhead_ce_bwd_int4", "bpb_reduce", "lmce_bpb", "lmhead_int4_dequant",
-    "lmce_status", "lmce_last_cuda_error", "lmce_strerror", "lmce_launch_count",
+    "lmce_status", "lmce_last_cuda_error", "lmce_strerror", "lmce_launch_count", "lmhead_ce_fwd_noalloc",
 )
 
 _lib = None

@@ -460,3 +460,94 @@ const char* lmce_strerror(int code) {
 }
 
 }  // extern "C"
+
+// ---- forward without a caller workspace ------------------------------------
+// For callers that cannot hand the library a device allocation: the scratch
+// of the forward (status word, partial sums of e^s, target logits) lives in a
+// file-scope device array instead.  Every GPU that loads this library holds
+// the array until the process exits; all calls on a device share it.
+namespace {
+
+constexpr int64_t kNoAllocMaxRows = 65536;   // N limit of lmhead_ce_fwd_noalloc
+constexpr int64_t kNoAllocMaxVocab = 8192;   // V limit
+constexpr size_t kNoAllocPartOff = 256;      // [0, 256): status word
+constexpr size_t kNoAllocPartBytes =
+    sizeof(float) * 2 * ((kNoAllocMaxVocab + lmce::fwdk::BN - 1) / lmce::fwdk::BN) * kNoAllocMaxRows;
+constexpr size_t kNoAllocStOff = kNoAllocPartOff + kNoAllocPartBytes;
+constexpr size_t kNoAllocBytes = kNoAllocStOff + sizeof(float) * kNoAllocMaxRows;  // about 16.3 MiB
+
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocBytes];
+
+// Device address of g_noalloc_scratch on the current device, looked up once
+// per device (the symbol's host-side name is not a device address).
+int noalloc_scratch(int dev, unsigned char** out) {
+  static std::mutex mu;
+  static unsigned char* ptr[64] = {};
+  if (dev < 0 || dev >= 64) return LMCE_ENOTSUP;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptr[dev]) {
+    void* p = nullptr;
+    cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(no-alloc scratch)");
+    ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = ptr[dev];
+  return LMCE_OK;
+}
+
+}  // namespace
+
+extern "C" int lmhead_ce_fwd_noalloc(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V,
+                                     int64_t d, const int64_t* tgt, float softcap, float* nll, float* lse,
+                                     void* stream) {
+  if (!h || !W || !tgt || !nll) return LMCE_EINVAL;
+  if (N < 1 || V < 1 || d < 1) return LMCE_EINVAL;
+  if (N > kNoAllocMaxRows || V > kNoAllocMaxVocab) {
+    g_last_err = "lmhead_ce_fwd_noalloc: N <= 65536 and V <= 8192 (size of its static scratch)";
+    return LMCE_EINVAL;
+  }
+  if (d % 64 != 0 || d > 512) return LMCE_ENOTSUP;
+  if (ldh < d || ldh % 8 != 0) return LMCE_EINVAL;
+  if (!aligned16(h) || !aligned16(W)) return LMCE_EINVAL;
+  if (!(softcap > 0.0f) || !(softcap <= softcap_max(V))) return LMCE_ENOTSUP;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  unsigned char* scratch = nullptr;
+  if (int rc = noalloc_scratch(di.dev, &scratch); rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* status = reinterpret_cast<unsigned*>(scratch);
+
+  CUtensorMap tm_h, tm_w;
+  if (int rc = lmce::make_map_bf16_3d(&tm_h, h, d, N, ldh * 2, lmce::fwdk::BM, static_cast<uint32_t>(d / 64)); rc)
+    return rc;
+  if (int rc = lmce::make_map_bf16_3d(&tm_w, W, d, V, d * 2, lmce::fwdk::HALF_N, lmce::fwdk::SC); rc) return rc;
+  lmce::fwdk::Params p{};
+  p.N = static_cast<int>(N);
+  p.n_rows = nullptr;
+  p.V = static_cast<int>(V);
+  p.d = static_cast<int>(d);
+  p.KC = static_cast<int>(d / 64);
+  p.VT = static_cast<int>(cdiv(V, lmce::fwdk::BN));
+  p.N_pad = static_cast<int>(cdiv(N, lmce::fwdk::PAIR_ROWS) * lmce::fwdk::PAIR_ROWS);
+  p.tgt = tgt;
+  p.inv_c = 1.0f / softcap;
+  p.c = softcap;
+  p.zlim2 = (lmce::kTanhXmax * softcap) * (lmce::kTanhXmax * softcap);
+  lmce::scaled_tanh_coeffs(static_cast<double>(softcap) * 1.4426950408889634, 1.0 / static_cast<double>(softcap),
+                           p.k);
+  p.part = reinterpret_cast<float*>(scratch + kNoAllocPartOff);
+  p.st = reinterpret_cast<float*>(scratch + kNoAllocStOff);
+  p.status = status;
+  p.maxseg = p.VT;
+  const int64_t T_max = cdiv(N, lmce::fwdk::PAIR_ROWS) * p.VT;
+  const int pairs = static_cast<int>(std::min<int64_t>(T_max, lmce::fwdk::max_clusters(di.sms)));
+  lmce::count_launches(2);
+  if (int rc = lmce::fwdk::launch(tm_h, tm_w, p, pairs, s); rc) return rc;
+  const int fblocks = static_cast<int>(std::min<int64_t>(cdiv(N, 256), int64_t(di.sms) * 4));
+  lmce::fwd_finalize_kernel<<<fblocks, 256, 0, s>>>(p.part, p.VT, pairs, lmce::fwdk::PAIR_ROWS, p.N_pad, p.st, tgt,
+                                                    nullptr, static_cast<int>(N), static_cast<int>(V), nullptr, nll,
+                                                    lse, status);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "lmhead_ce_fwd_noalloc launch");
+  return LMCE_OK;
+}
