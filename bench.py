@@ -279,7 +279,8 @@ def run_ours(args, rank, world, local_rank):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_burst,
                      "unit": "TFLOP/s", "frac": achieved / peak_burst, "peak_source": f"{peak_src} bf16 burst",
-                     "frac_of_sustained": achieved / peak_sust, "traffic": None,
+                     "frac_of_sustained": achieved / peak_sust, "traffic": ncu_traffic(dom),
+                     "traffic_unit": "bytes/launch (ncu dram read + write)",
                      "flops_per_launch": fpt[dom] * N},
         "kernels_ms": avg,
         "mfu_6NVd": model_flops / (ms_step / 1e3) / 1e12 / peak_burst,
@@ -291,6 +292,37 @@ def run_ours(args, rank, world, local_rank):
         "wall_s_timed": t_wall,
     }
     return line
+
+
+KERNEL_SOURCES = {"fwd": "fwd_kernel.cuh", "bwd_dh": "bwd_kernel.cuh", "bwd_dW": "bwd_kernel.cuh"}
+
+
+def kernel_sources_sha(kernel: str) -> str:
+    """sha256 (first 16 hex digits) of the sources that define a kernel."""
+    import hashlib
+    csrc = os.path.join(ROOT, "lm_head_softcapped_lmhead_b300", "csrc")
+    h = hashlib.sha256()
+    for f in (KERNEL_SOURCES[kernel], "ptx.cuh", "softcap_math.cuh"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel: str):
+    """DRAM bytes (read + write) per launch of a kernel, from the ncu summaries
+    under profiles/ (lines 'traffic <kernel> <bytes> bytes/launch sources <sha>').
+    None when no summary was taken on the kernel's current sources."""
+    import glob
+    import re
+    sha = kernel_sources_sha(kernel)
+    pat = re.compile(r"^traffic (\S+) (\d+) bytes/launch sources ([0-9a-f]+)\s*$")
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        with open(path) as fh:
+            for line in fh:
+                m = pat.match(line.strip())
+                if m and m.group(1) == kernel and m.group(3) == sha:
+                    return int(m.group(2))
+    return None
 
 
 # ---------------------------------------------------------------- oracle arm
