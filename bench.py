@@ -3,10 +3,11 @@
 
 One step = the whole hot path over one batch of the training-micro-batch
 workload (N = 65536 tokens = 32 x 2048, d = 512, V = 8192, softcap 30, Zipf
-targets, mean loss): forward (nll, lse) -> bits-per-byte reduction ->
-backward dh -> backward dW (fp32, accumulated).  Inputs are synthetic
-(seeded numpy PCG64, shaped like the pages' models) and resident in HBM when
-the timed region starts; L2 is flushed (a 256 MB write) between steps.
+targets, mean loss): forward (nll, lse) and dh in one pass ->
+bits-per-byte reduction -> backward dW (fp32, accumulated).  Inputs are
+synthetic (seeded numpy PCG64, shaped like the pages' models) and resident
+in HBM when the timed region starts; L2 is flushed (a 256 MB write) between
+steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
 
@@ -35,7 +36,7 @@ import numpy as np  # noqa: E402
 CFG = 3
 SOFTCAP = 30.0
 WORKLOAD = "training micro-batch: N=65536 (32x2048) d=512 V=8192 softcap=30 Zipf(1.1) targets, mean loss, " \
-           "fwd + bpb_reduce + bwd dh + bwd dW (fp32 +=)"
+           "fwd + dh (one pass) + bpb_reduce + bwd dW (fp32 +=)"
 
 
 def parse():
@@ -116,8 +117,7 @@ def measured_peaks():
 
 def flops_per_token(V, d):
     """Algorithmic tensor FLOPs per token of each launch (2 per MAC)."""
-    return {"fwd": 2 * V * d,          # z = h W^T
-            "bwd_dh": 4 * V * d,       # z recomputed + dh = G W
+    return {"fwd_dh": 4 * V * d,       # z = h W^T + dh = G W, one pass
             "bwd_dW": 4 * V * d}       # z recomputed + dW = G^T h
 
 
@@ -149,22 +149,22 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    # One step: forward + dh in one pass, the bits-per-byte sums, then the dW
+    # pass (which needs the forward's lse), each call bracketed by events.
     def step(events=None):
-        ev = events or [None] * 5
+        ev = events or [None] * 4
         if ev[0] is not None:
             ev[0].record(stream)
-        lm.lmhead_ce_fwd(h, W, tgt, SOFTCAP, nll, lse, ws=ws, stream=stream)
+        lm.lmhead_ce_fwd_bwd(h, W, tgt, SOFTCAP, grad_scale, nll, lse, dh=dh, ws=ws, stream=stream)
         if ev[1] is not None:
             ev[1].record(stream)
         lm.bpb_reduce(nll, nbytes, acc, ws=ws, stream=stream)
         if ev[2] is not None:
             ev[2].record(stream)
-        lm.lmhead_ce_bwd(h, W, tgt, SOFTCAP, lse, grad_scale, dh=dh, ws=ws, stream=stream)
+        lm.lmhead_ce_bwd(h, W, tgt, SOFTCAP, lse, grad_scale, dW=dW, accumulate_dW=True, ws=ws, stream=stream,
+                         nll=nll)
         if ev[3] is not None:
             ev[3].record(stream)
-        lm.lmhead_ce_bwd(h, W, tgt, SOFTCAP, lse, grad_scale, dW=dW, accumulate_dW=True, ws=ws, stream=stream)
-        if ev[4] is not None:
-            ev[4].record(stream)
 
     def barrier():
         if world > 1:
@@ -190,7 +190,7 @@ def run_ours(args, rank, world, local_rank):
     if lm.lmce_status(ws, stream) != lm.LMCE_OK:
         raise RuntimeError("device status after warm-up is not OK")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     launches0 = lm.lmce_launch_count()
@@ -206,11 +206,10 @@ def run_ours(args, rank, world, local_rank):
     if lm.lmce_status(ws, stream) != lm.LMCE_OK:
         raise RuntimeError("device status after the timed steps is not OK")
 
-    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
-    part_ms = {"fwd": [e[0].elapsed_time(e[1]) for e in evs],
+    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    part_ms = {"fwd_dh": [e[0].elapsed_time(e[1]) for e in evs],
                "bpb_reduce": [e[1].elapsed_time(e[2]) for e in evs],
-               "bwd_dh": [e[2].elapsed_time(e[3]) for e in evs],
-               "bwd_dW": [e[3].elapsed_time(e[4]) for e in evs]}
+               "bwd_dW": [e[2].elapsed_time(e[3]) for e in evs]}
     total_ms = sum(step_ms)
 
     if args.profile:
@@ -227,10 +226,9 @@ def run_ours(args, rank, world, local_rank):
         h_in.copy_(h_host, non_blocking=True)
         t_in.copy_(t_host, non_blocking=True)
         b_in.copy_(b_host, non_blocking=True)
-        lm.lmhead_ce_fwd(h_in, W, t_in, SOFTCAP, nll, lse, ws=ws, stream=stream)
+        lm.lmhead_ce_fwd_bwd(h_in, W, t_in, SOFTCAP, grad_scale, nll, lse, dh=dh, dW=dW, accumulate_dW=True,
+                             ws=ws, stream=stream)
         lm.bpb_reduce(nll, b_in, acc, ws=ws, stream=stream)
-        lm.lmhead_ce_bwd(h_in, W, t_in, SOFTCAP, lse, grad_scale, dh=dh, dW=dW, accumulate_dW=True, ws=ws,
-                         stream=stream)
         acc_host.copy_(acc, non_blocking=True)
 
     for _ in range(2):
@@ -263,7 +261,7 @@ def run_ours(args, rank, world, local_rank):
     peak_burst, peak_sust, hbm, peak_src = measured_peaks()
     fpt = flops_per_token(V, d)
     avg = {k: statistics.mean(v) for k, v in part_ms.items()}
-    dom = max(("fwd", "bwd_dh", "bwd_dW"), key=lambda k: avg[k])
+    dom = max(("fwd_dh", "bwd_dW"), key=lambda k: avg[k])
     achieved = fpt[dom] * N / (avg[dom] / 1e3) / 1e12
     ms_step = total_ms / args.steps
     model_flops = 6 * V * d * N
@@ -294,7 +292,8 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-KERNEL_SOURCES = {"fwd": "fwd_kernel.cuh", "bwd_dh": "bwd_kernel.cuh", "bwd_dW": "bwd_kernel.cuh"}
+KERNEL_SOURCES = {"fwd": "fwd_kernel.cuh", "fwd_dh": "bwd_kernel.cuh", "bwd_dh": "bwd_kernel.cuh",
+                  "bwd_dW": "bwd_kernel.cuh"}
 
 
 def kernel_sources_sha(kernel: str) -> str:

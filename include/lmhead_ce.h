@@ -113,14 +113,39 @@ LMCE_API int lmhead_ce_fwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, 
                   size_t ws_bytes, void* stream);
 
 /* Backward of L = grad_scale * sum over scored rows of nll_i.
- * Inputs as lmhead_ce_fwd plus lse [N] fp32 from the forward.
+ * Inputs as lmhead_ce_fwd plus lse [N] fp32 from the forward, and
+ * optionally (nullable) nll [N] fp32 from the same forward call.  With nll
+ * the target's p - 1 is taken as expm1(-nll) instead of e^{s_t - lse} - 1;
+ * the latter loses its relative precision in fp32 as p_t -> 1 (s_t and lse
+ * cancel), which matters for confident predictions.
  * Outputs (each nullable, at least one non-NULL):
  *   dh [N, d] bf16 (row stride ldh), overwritten; masked rows get 0.
  *   dW [V, d] fp32: accumulate_dW != 0 adds into it, else overwrites.
  * grad_scale: dL/dnll of each scored row (1/M for a mean over M rows). */
 LMCE_API int lmhead_ce_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
-                  const int64_t* tgt, const uint8_t* row_mask, float softcap, const float* lse, float grad_scale,
-                  lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes, void* stream);
+                  const int64_t* tgt, const uint8_t* row_mask, float softcap, const float* lse, const float* nll,
+                  float grad_scale, lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes,
+                  void* stream);
+
+/* Forward and backward of one training step, for L = grad_scale * sum over
+ * scored rows of nll_i (defining passages as lmhead_ce_fwd and
+ * lmhead_ce_bwd).  Outputs: nll and lse [N] fp32 (both required); dh [N, d]
+ * bf16 (row stride ldh, nullable); dW [V, d] fp32 (nullable;
+ * accumulate_dW != 0 adds into it).
+ * With dh requested and softcap <= 60 the forward and dh come from ONE pass
+ * over the vocabulary: the row's normaliser is applied after the
+ * accumulation (dh_i = -w/S_i sum_{j != t_i} e^{s_ij}(1 - tanh^2) W_j
+ * + w (p_{i,t_i} - 1)(1 - tanh_{i,t_i}^2) W_{t_i}, S_i = sum_j e^{s_ij}),
+ * which saves the separate forward's logit GEMM.  dW then takes a second
+ * pass that reads lse and nll.  Masked rows are computed and zeroed in that pass
+ * (no compaction), so a heavily masked batch is better served by
+ * lmhead_ce_fwd + lmhead_ce_bwd.  Larger softcaps, or dh == NULL, run the
+ * forward and the backward passes separately.  Same workspace and layout
+ * rules as lmhead_ce_bwd. */
+LMCE_API int lmhead_ce_fwd_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+                      const int64_t* tgt, const uint8_t* row_mask, float softcap, float grad_scale, float* nll,
+                      float* lse, lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes,
+                      void* stream);
 
 /* Forward with the head stored as per-group int4 (symmetric, two's-complement
  * nibbles; element 2m of a row in the low nibble of byte m) with one fp16
@@ -137,7 +162,8 @@ LMCE_API int lmhead_ce_fwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* 
  * Same layout rules as lmhead_ce_fwd_int4 and lmhead_ce_bwd. */
 LMCE_API int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
                        int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
-                       const float* lse, float grad_scale, lmce_bf16* dh, void* ws, size_t ws_bytes, void* stream);
+                       const float* lse, const float* nll, float grad_scale, lmce_bf16* dh, void* ws,
+                       size_t ws_bytes, void* stream);
 
 /* Bits-per-byte sums (tproger news, "Rules and metric").  Adds, over rows with
  * row_mask != 0 (all rows if NULL), sum nll (fp64), sum bytes and the row

@@ -13,9 +13,11 @@ namespace lmce {
 // The forward's G work groups (2-CTA clusters) cover T = ceil(rows / R) * VT
 // tiles (R rows per unit), group b taking [b T / G, (b+1) T / G).  Unit u
 // (tiles g0 = u VT .. g0 + VT - 1) is covered by groups b_first .. b_last;
-// each non-empty one wrote, per column half, its segment's sum of e^s into
-// part[2 s + half][row], s = max(0, start(b) - g0) < VT.  lse = ln(sum of
-// those, in group and half order, in fp64); nll = lse - s_t.  With a
+// each non-empty one wrote, per column half, its segment's sum of e^s over
+// the non-target columns into part[2 s + half][row], s = max(0, start(b) -
+// g0) < VT.  S_other = the sum of those, in group and half order, in fp64;
+// with e^{s_t} from st[row]: lse = ln(S_other + e^{s_t}) and
+// nll = log1p(S_other / e^{s_t}).  With a
 // compaction map, row r of the compacted problem goes to row idx[r] of the
 // outputs.  A target outside [0, V) raises ST_EDATA and gives nll = NaN.
 __global__ void fwd_finalize_kernel(const float* __restrict__ part, int VT, int G, int R, int N_pad,
@@ -37,14 +39,19 @@ __global__ void fwd_finalize_kernel(const float* __restrict__ part, int VT, int 
       S += static_cast<double>(part[(2 * slot) * N_pad + r]);
       S += static_cast<double>(part[(2 * slot + 1) * N_pad + r]);
     }
-    const float l = static_cast<float>(log(S));
+    // S holds the non-target terms and st[r] the target's e^{s_t}:
+    // nll = -ln p_t = log1p(S / e^{s_t}) keeps its relative precision as
+    // p_t -> 1.
     const int64_t t = tgt[r];
-    float v;
+    float v, l;
     if (t < 0 || t >= V) {
       atomicOr(status, ST_EDATA);
       v = __int_as_float(0x7fc00000);
+      l = static_cast<float>(log(S));
     } else {
-      v = l - st[r];
+      const double et = static_cast<double>(st[r]);
+      v = static_cast<float>(log1p(S / et));
+      l = static_cast<float>(log(S + et));
     }
     const int o = idx ? idx[r] : r;
     nll[o] = v;

@@ -2,6 +2,7 @@
 //   G_ij = (p_ij - [j == t_i]) (1 - tanh^2(z_ij / c)),  p_ij = e^{s_ij - lse_i}
 //   dh = w G W            (rows stationary, "DH" mode)
 //   dW (+)= w G^T h       (vocab stationary, "DW" mode)
+//   forward + dh in one pass ("FD" mode, below)
 // Chain rule of nll_i = lse_i - s_{i,t_i} through s = c tanh(z/c), for the
 // training step of "parameter-golf: ... Where Model Size Becomes the Game",
 // section "The Baseline Is a Map, Not the Destination" (loss.backward()).
@@ -21,6 +22,20 @@
 //    (bf16) or dW (fp32, added or stored; or a partial for a later ordered
 //    reduction when the rows are split across several clusters).
 // The logits and G never leave the two SMs.  Every wait is bounded.
+//
+// FD mode computes the forward (nll, lse) and dh in the same pass over the
+// vocabulary, without the forward's lse.  dh_i = w sum_j G_ij W_j splits as
+//   dh_i = w [ sum_{j != t_i} p_ij (1 - tanh_ij^2) W_j
+//              + (p_{i,t_i} - 1)(1 - tanh_{i,t_i}^2) W_{t_i} ],
+// and p_ij = e^{s_ij} / S_i with S_i = sum_j e^{s_ij} constant along the row.
+// So the Z CTA streams the unnormalised tile P = e^{s} (tanh^2 - 1) with the
+// target column left out (so no large p_t - 1 cancellation happens in bf16),
+// and keeps per row S_other = the sum of e^{s} over the non-target columns,
+// and the target's e^{s_t} and 1 - tanh^2.  At the end of the row block the
+// A CTA's drain forms S = S_other + e^{s_t}, lse = ln S,
+// nll = log1p(S_other / e^{s_t}) and dh_i = alpha_i acc_i + beta_i W_{t_i}
+// with alpha_i = -w / S and beta_i = -w (S_other / S)(1 - tanh_t^2): no
+// quantity there cancels as p_t -> 1.
 #pragma once
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -38,7 +53,7 @@ void count_launches(unsigned n);
 
 namespace bwdk {
 
-enum Mode : int { DH = 0, DW = 1 };
+enum Mode : int { DH = 0, DW = 1, FD = 2 };
 
 constexpr int BM = 128;   // stationary block (TMEM lanes)
 constexpr int BT = 128;   // streamed tile (z columns; K of the accumulation)
@@ -65,6 +80,12 @@ constexpr uint32_t SLAB_CHUNK = SLAB_ROWS * KB * 2;  // 4 KB
 constexpr uint32_t Z_Y = 0;                             // ring of YSTAGES stages
 constexpr uint32_t Z_END = Z_Y + YSTAGES * ZSTAGE;
 constexpr uint32_t Z_TMEM_X = 256;
+// FD: per-row records of the Z epilogue, [column half][row] x 32 bytes:
+// {double sum of e^s over the non-target columns, float e^{s_t},
+//  1 - tanh_t^2, int target, int flags}.
+constexpr uint32_t Z_REC = Z_END;
+constexpr uint32_t REC_BYTES = 32;
+constexpr int FL_LIVE = 1, FL_TVALID = 2, FL_HIT = 4;
 // A CTA layout
 constexpr uint32_t A_Y = 0;                             // ring of ASLOTS slabs (32 x d each)
 constexpr uint32_t A_P = A_Y + ASLOTS * MAX_KC * SLAB_CHUNK;  // 2 P slots of 128 x 128 bf16
@@ -72,6 +93,7 @@ constexpr uint32_t P_SLOT = 2 * CHUNK;                  // 32 KB
 constexpr uint32_t A_END = A_P + 2 * P_SLOT;
 constexpr uint32_t BAR_OFF = (Z_END > A_END ? Z_END : A_END);
 constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;
+static_assert(Z_REC + 2 * BM * REC_BYTES <= BAR_OFF, "FD row records overlap the barriers");
 constexpr uint32_t Z_TMEM_COLS = 512;
 constexpr uint32_t A_TMEM_COLS = 512;
 constexpr uint32_t IDESC_Z = idesc_bf16_f32(128, BT, false, false);
@@ -86,7 +108,12 @@ struct Params {
   const int64_t* tgt;   // [N]
   const uint8_t* mask;  // [N] or null
   const float* lse;     // [N]
-  float inv_c, cl2e, w;  // w: the drain's scale (-grad_scale: the tiles hold -G)
+  const float* nll_in;  // [N] from the same forward, or null: the target's p - 1 = expm1(-nll)
+  float inv_c, cl2e, w;  // w: the drain's scale (-grad_scale: the tiles hold -G; FD: +grad_scale)
+  float c;
+  const __nv_bfloat16* W;  // FD: the head, for the target-row term of dh
+  float* nll;              // FD outputs [N]
+  float* lse_out;
   float zlim2;
   float q[kTanhTerms];  // -C_i / c^(2i+1)
   __nv_bfloat16* dh;    // DH output [N, ldh]
@@ -127,12 +154,12 @@ struct Chunk32 {
 struct Packed16 {
   uint32_t v[16];
 };
-struct SlowArgs {
-  float lse2_col[32];  // per-column lse2 (DW) -- unused when per_col == 0
-  int hit_col[32];     // per-column target lane (DW)
-};
-__device__ __noinline__ Packed16 g_chunk_slow(Chunk32 r, float inv_c, float cl2e, int per_col, SlowArgs cols,
-                                              float lse2_row, int rel, int my_lane, int lim) {
+// At the target column p - 1 is either formed here (pp - 1) or, when the
+// forward's nll is known (use_pm1), taken as expm1(-nll): that keeps its
+// relative precision when p_t -> 1, where s_t - lse cancels in fp32.
+// DH: one row per thread (lse2_row, target column rel, valid columns lim).
+__device__ __noinline__ Packed16 g_chunk_slow_dh(Chunk32 r, float inv_c, float cl2e, float lse2_row, int rel, int lim,
+                                                 int use_pm1, float pm1_row) {
   Packed16 out;
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
@@ -140,11 +167,32 @@ __device__ __noinline__ Packed16 g_chunk_slow(Chunk32 r, float inv_c, float cl2e
 #pragma unroll
     for (int e = 0; e < 2; ++e) {
       const float th = tanh_any(__uint_as_float(r.v[j + e]) * inv_c);
-      const float l2 = per_col ? cols.lse2_col[j + e] : lse2_row;
-      float pp = ex2_approx(fmaf(th, cl2e, -l2));
-      const bool hit = per_col ? (cols.hit_col[j + e] == my_lane) : (j + e == rel);
-      if (hit) pp -= 1.0f;
+      float pp = ex2_approx(fmaf(th, cl2e, -lse2_row));
+      if (j + e == rel) pp = use_pm1 ? pm1_row : pp - 1.0f;
       g[e] = (j + e < lim) ? pp * fmaf(th, th, -1.0f) : 0.f;
+    }
+    out.v[j / 2] = pack_bf16x2(g[0], g[1]);
+  }
+  return out;
+}
+// DW: lane = vocab row, column j = tile row j; lane j holds column j's
+// -lse log2(e) (nl_col), target lane (hit_col) and p_t - 1 (pm1_col), read
+// by every lane with shuffles (the whole warp calls this).
+__device__ __noinline__ Packed16 g_chunk_slow_dw(Chunk32 r, float inv_c, float cl2e, float nl_col, int hit_col,
+                                                 float pm1_col, int my_lane, int use_pm1) {
+  Packed16 out;
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    float g[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float th = tanh_any(__uint_as_float(r.v[j + e]) * inv_c);
+      const float nl = __shfl_sync(0xffffffffu, nl_col, j + e);
+      const int hit = __shfl_sync(0xffffffffu, hit_col, j + e);
+      const float q1 = __shfl_sync(0xffffffffu, pm1_col, j + e);
+      float pp = ex2_approx(fmaf(th, cl2e, nl));
+      if (hit == my_lane) pp = use_pm1 ? q1 : pp - 1.0f;
+      g[e] = pp * fmaf(th, th, -1.0f);
     }
     out.v[j / 2] = pack_bf16x2(g[0], g[1]);
   }
@@ -155,7 +203,7 @@ __device__ __noinline__ Packed16 g_chunk_slow(Chunk32 r, float inv_c, float cl2e
 // row, rel = target column inside the chunk or -1, lim = valid columns).
 template <bool kHit>
 __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiConst& k, float lse2, int rel, int lim,
-                                           uint32_t (&out)[16]) {
+                                           int use_pm1, float pm1, uint32_t (&out)[16]) {
   const float2 nl = make_float2(-lse2, -lse2);
   float2 su = make_float2(0.f, 0.f);
 #pragma unroll
@@ -167,8 +215,8 @@ __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiCon
     const float2 a = __ffma2_rn(nth, k.ncl2e, nl);
     float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
     if (kHit) {
-      pp.x -= (2 * j == rel) ? 1.0f : 0.0f;
-      pp.y -= (2 * j + 1 == rel) ? 1.0f : 0.0f;
+      if (2 * j == rel) pp.x = use_pm1 ? pm1 : pp.x - 1.0f;
+      if (2 * j + 1 == rel) pp.y = use_pm1 ? pm1 : pp.y - 1.0f;
     }
     float2 g = __fmul2_rn(pp, __ffma2_rn(nth, nth, k.m1));
     if (lim < 32) {
@@ -181,8 +229,7 @@ __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiCon
     Chunk32 c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) c.v[j] = r[j];
-    SlowArgs none = {};
-    const Packed16 o = g_chunk_slow(c, k.inv_c, k.cl2e, 0, none, lse2, rel, -1, lim);
+    const Packed16 o = g_chunk_slow_dh(c, k.inv_c, k.cl2e, lse2, rel, lim, use_pm1, pm1);
 #pragma unroll
     for (int j = 0; j < 16; ++j) out[j] = o.v[j];
   }
@@ -194,7 +241,7 @@ __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiCon
 // outside the block); every lane reads them with shuffles.
 template <bool kHit>
 __device__ __forceinline__ void g_chunk_dw(const uint32_t (&r)[32], const EpiConst& k, float nl_col, int hit_col,
-                                           int my_lane, uint32_t (&out)[16]) {
+                                           int my_lane, int use_pm1, float pm1_col, uint32_t (&out)[16]) {
   float2 su = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -206,25 +253,108 @@ __device__ __forceinline__ void g_chunk_dw(const uint32_t (&r)[32], const EpiCon
     const float2 a = __ffma2_rn(nth, k.ncl2e, nl);
     float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
     if (kHit) {
-      pp.x -= (__shfl_sync(0xffffffffu, hit_col, 2 * j) == my_lane) ? 1.0f : 0.0f;
-      pp.y -= (__shfl_sync(0xffffffffu, hit_col, 2 * j + 1) == my_lane) ? 1.0f : 0.0f;
+      const float qx = __shfl_sync(0xffffffffu, pm1_col, 2 * j);
+      const float qy = __shfl_sync(0xffffffffu, pm1_col, 2 * j + 1);
+      if (__shfl_sync(0xffffffffu, hit_col, 2 * j) == my_lane) pp.x = use_pm1 ? qx : pp.x - 1.0f;
+      if (__shfl_sync(0xffffffffu, hit_col, 2 * j + 1) == my_lane) pp.y = use_pm1 ? qy : pp.y - 1.0f;
     }
     const float2 g = __fmul2_rn(pp, __ffma2_rn(nth, nth, k.m1));
     out[j] = pack_bf16x2(g.x, g.y);
   }
   if (__any_sync(0xffffffffu, !(su.x + su.y <= k.zlim2))) {
     Chunk32 c;
-    SlowArgs cols;
 #pragma unroll
-    for (int j = 0; j < 32; ++j) {
-      c.v[j] = r[j];
-      cols.lse2_col[j] = -__shfl_sync(0xffffffffu, nl_col, j);
-      cols.hit_col[j] = __shfl_sync(0xffffffffu, hit_col, j);
-    }
-    const Packed16 o = g_chunk_slow(c, k.inv_c, k.cl2e, 1, cols, 0.f, -1, my_lane, 32);
+    for (int j = 0; j < 32; ++j) c.v[j] = r[j];
+    const Packed16 o = g_chunk_slow_dw(c, k.inv_c, k.cl2e, nl_col, hit_col, pm1_col, my_lane, use_pm1);
 #pragma unroll
     for (int j = 0; j < 16; ++j) out[j] = o.v[j];
   }
+}
+
+// FD mode: 32 vocab columns of this thread's row.  e = e^{s} =
+// 2^(c log2(e) tanh + nl) (nl = 0, or -inf for a row that does not count;
+// 0 past column lim), P = e (tanh^2 - 1) except at the target column (rel),
+// where P = 0 and e, 1 - tanh^2 go to tg.  Returns the chunk's sum of e over
+// its non-target columns.
+struct FdTarget {
+  float e, om;
+};
+struct FdSlowOut {
+  uint32_t v[16];
+  float sum;
+  FdTarget tg;
+};
+__device__ __noinline__ FdSlowOut fd_chunk_slow(Chunk32 r, float inv_c, float cl2e, float nl, int rel, int lim) {
+  FdSlowOut o;
+  o.sum = 0.f;
+  o.tg = FdTarget{0.f, 0.f};
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) {
+    float g[2];
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const float z = __uint_as_float(r.v[j + e]);
+      const float th = tanh_any(z * inv_c);
+      const float ee = (j + e < lim) ? ex2_approx(fmaf(th, cl2e, nl)) : 0.f;
+      const float om = fmaf(-th, th, 1.0f);
+      float gg = -ee * om;
+      if (j + e == rel) {
+        o.tg = FdTarget{ee, om};
+        gg = 0.f;
+      } else {
+        o.sum += ee;
+      }
+      g[e] = gg;
+    }
+    o.v[j / 2] = pack_bf16x2(g[0], g[1]);
+  }
+  return o;
+}
+template <bool kHit>
+__device__ __forceinline__ float g_chunk_fd(const uint32_t (&r)[32], const EpiConst& k, float nl, int rel, int lim,
+                                            uint32_t (&out)[16], FdTarget& tg) {
+  const float2 nl2 = make_float2(nl, nl);
+  float2 su = make_float2(0.f, 0.f);
+  float2 se = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    const float2 u = __fmul2_rn(z, z);
+    su = __fadd2_rn(su, u);
+    const float2 nth = poly_z2(z, u, k.q);
+    const float2 a = __ffma2_rn(nth, k.ncl2e, nl2);
+    float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
+    if (lim < 32) {
+      e.x = (2 * j < lim) ? e.x : 0.f;
+      e.y = (2 * j + 1 < lim) ? e.y : 0.f;
+    }
+    const float2 w = __ffma2_rn(nth, nth, k.m1);
+    if (kHit) {
+      if (2 * j == rel) {
+        tg = FdTarget{e.x, -w.x};
+        e.x = 0.f;
+      }
+      if (2 * j + 1 == rel) {
+        tg = FdTarget{e.y, -w.y};
+        e.y = 0.f;
+      }
+    }
+    se = __fadd2_rn(se, e);
+    const float2 g = __fmul2_rn(e, w);
+    out[j] = pack_bf16x2(g.x, g.y);
+  }
+  float sum = se.x + se.y;
+  if (__any_sync(0xffffffffu, !(su.x + su.y <= k.zlim2))) {
+    Chunk32 c;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c.v[j] = r[j];
+    const FdSlowOut o = fd_chunk_slow(c, k.inv_c, k.cl2e, nl, rel, lim);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) out[j] = o.v[j];
+    sum = o.sum;
+    if (kHit) tg = o.tg;
+  }
+  return sum;
 }
 
 // Split-major order: clusters running at the same time share a row range
@@ -258,6 +388,8 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* ay_full = bars + 22;    // [ASLOTS] slab slots of the Y ring
   uint64_t* ay_empty = bars + 28;   // [ASLOTS]
   uint64_t* mma_done = bars + 34;
+  uint64_t* rd_full = bars + 35;    // FD, in A: the Z epilogue's row records are written
+  uint64_t* rd_empty = bars + 36;   // FD, in Z: the A drain has read them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 504);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 508);
 
@@ -286,6 +418,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(ay_empty + i, 1);
     }
     mbar_init(mma_done, 1);
+    mbar_init(rd_full, 2 * BM);
+    mbar_init(rd_empty, 2 * BM);
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -436,26 +570,51 @@ __global__ void __launch_bounds__(THREADS, 1)
       // lane of the row's target.  pf_* is the next tile's, fetched early.
       float cur_nl[2] = {kNegInf, kNegInf};
       int cur_hit[2] = {-1, -1};
+      float cur_pm1[2] = {0.f, 0.f};
       float pf_nl[2] = {kNegInf, kNegInf};
       int pf_hit[2] = {-1, -1};
+      float pf_pm1[2] = {0.f, 0.f};
+      const int use_pm1 = p.nll_in != nullptr;
       const uint32_t peer_p = mapa_shared(smem_u32(smem + A_P), 1);
       const uint32_t peer_pfull = mapa_shared(smem_u32(p_full), 1);
+      const uint32_t peer_rd_full = mapa_shared(smem_u32(rd_full), 1);
       int acc = 0, slot = 0;
       uint32_t aph = 0, sph = 0;
       bool ok = true;
+      int fd_units = 0;
       for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
         int blk, t0, t1;
         unit_range(p, u, blk, t0, t1);
         // DH: this thread's row data.
         float nl_row = kNegInf;
         long long trow = -1;
+        float pm1_row = 0.f;
         if (MODE == DH) {
           const int row = blk * BM + m;
           if (row < p.N && (!p.mask || p.mask[row])) {
             const long long tt = p.tgt[row];
             nl_row = -p.lse[row] * kLog2e;
+            if (use_pm1) pm1_row = expm1f(-p.nll_in[row]);
             if (tt >= 0 && tt < p.V) trow = tt;
             else atomicOr(p.status, ST_EDATA);
+          }
+        }
+        // FD: this thread's row data and its running sums over the unit.
+        int fd_flags = 0;
+        double s_acc = 0.0;
+        FdTarget rec_tg{0.f, 0.f};
+        if (MODE == FD) {
+          const int row = blk * BM + m;
+          if (row < p.N && (!p.mask || p.mask[row])) {
+            const long long tt = p.tgt[row];
+            nl_row = 0.f;
+            fd_flags = FL_LIVE;
+            if (tt >= 0 && tt < p.V) {
+              trow = tt;
+              fd_flags |= FL_TVALID;
+            } else if (hc == 0) {
+              atomicOr(p.status, ST_EDATA);
+            }
           }
         }
         const long long vbase = static_cast<long long>(blk) * BM;
@@ -466,6 +625,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             const int row = t * BT + hc * 64 + k * 32 + lane;
             float nl = kNegInf;
             int hl = -1;
+            float q1 = 0.f;
             if (row < p.N) {
               const uint8_t mk = p.mask ? p.mask[row] : uint8_t(1);
               const long long tt = p.tgt[row];
@@ -474,10 +634,12 @@ __global__ void __launch_bounds__(THREADS, 1)
                 nl = -l * kLog2e;
                 if (tt < 0 || tt >= p.V) atomicOr(p.status, ST_EDATA);
                 else if (tt >= vbase && tt < vbase + BM) hl = static_cast<int>(tt - vbase);
+                if (hl >= 0 && use_pm1) q1 = expm1f(-p.nll_in[row]);
               }
             }
             pf_nl[k] = nl;
             pf_hit[k] = hl;
+            pf_pm1[k] = q1;
           }
         };
         if (MODE == DW && t0 < t1) fetch_dw(t0);
@@ -488,6 +650,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int k = 0; k < 2; ++k) {
               cur_nl[k] = pf_nl[k];
               cur_hit[k] = pf_hit[k];
+              cur_pm1[k] = pf_pm1[k];
               hit_any[k] = __any_sync(0xffffffffu, pf_hit[k] >= 0);
             }
             if (t + 1 < t1) fetch_dw(t + 1);
@@ -510,14 +673,30 @@ __global__ void __launch_bounds__(THREADS, 1)
               const long long relw = trow - cbase;
               const int rel = (relw >= 0 && relw < 32) ? static_cast<int>(relw) : -1;
               if (__any_sync(0xffffffffu, rel >= 0))
-                g_chunk_dh<true>(r, kc, -nl_row, rel, lim, packed);
+                g_chunk_dh<true>(r, kc, -nl_row, rel, lim, use_pm1, pm1_row, packed);
               else
-                g_chunk_dh<false>(r, kc, -nl_row, -1, lim, packed);
+                g_chunk_dh<false>(r, kc, -nl_row, -1, lim, use_pm1, pm1_row, packed);
+            } else if (MODE == FD) {
+              const int cbase = t * BT + hc * 64 + ch * 32;
+              const int lim = min(32, p.V - cbase);
+              const long long relw = trow - cbase;
+              const int rel = (relw >= 0 && relw < 32) ? static_cast<int>(relw) : -1;
+              FdTarget tg{0.f, 0.f};
+              float cs;
+              if (__any_sync(0xffffffffu, rel >= 0))
+                cs = g_chunk_fd<true>(r, kc, nl_row, rel, lim, packed, tg);
+              else
+                cs = g_chunk_fd<false>(r, kc, nl_row, -1, lim, packed, tg);
+              s_acc += static_cast<double>(cs);
+              if (rel >= 0) {
+                rec_tg = tg;
+                fd_flags |= FL_HIT;
+              }
             } else {
               if (hit_any[ch])
-                g_chunk_dw<true>(r, kc, cur_nl[ch], cur_hit[ch], m, packed);
+                g_chunk_dw<true>(r, kc, cur_nl[ch], cur_hit[ch], m, use_pm1, cur_pm1[ch], packed);
               else
-                g_chunk_dw<false>(r, kc, cur_nl[ch], cur_hit[ch], m, packed);
+                g_chunk_dw<false>(r, kc, cur_nl[ch], cur_hit[ch], m, use_pm1, cur_pm1[ch], packed);
             }
 #pragma unroll
             for (int v = 0; v < 4; ++v) {
@@ -542,6 +721,21 @@ __global__ void __launch_bounds__(THREADS, 1)
           if (acc == 0) aph ^= 1u;
           slot ^= 1;
           if (slot == 0) sph ^= 1u;
+        }
+        if (MODE == FD) {
+          // Row record for the A drain, once it has read the previous one.
+          if (!ok) break;
+          if (fd_units > 0) {
+            ok = mbar_wait<true>(rd_empty, static_cast<uint32_t>(fd_units - 1) & 1u, abort_flag, p.status);
+            if (!ok) break;
+          }
+          uint4* rec = reinterpret_cast<uint4*>(smem + Z_REC + (static_cast<uint32_t>(hc) * BM + m) * REC_BYTES);
+          const unsigned long long sb = static_cast<unsigned long long>(__double_as_longlong(s_acc));
+          rec[0] = make_uint4(static_cast<uint32_t>(sb), static_cast<uint32_t>(sb >> 32), __float_as_uint(rec_tg.e),
+                              __float_as_uint(rec_tg.om));
+          rec[1] = make_uint4(static_cast<uint32_t>(trow), static_cast<uint32_t>(fd_flags), 0u, 0u);
+          mbar_arrive_cluster(peer_rd_full);
+          ++fd_units;
         }
       }
     }
@@ -650,24 +844,95 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int q = warp & 3;
       const int hc = warp >> 2;       // column half of the accumulator
       const int m = q * 32 + lane;
-      uint32_t fph = 0;
+      uint32_t fph = 0, rph = 0;
+      const uint32_t z_rec = mapa_shared(smem_u32(smem + Z_REC), 0);
+      const uint32_t z_rd_empty = mapa_shared(smem_u32(rd_empty), 0);
       for (int u = cluster; u < p.n_units; u += n_clusters) {
         int blk, t0, t1;
         unit_range(p, u, blk, t0, t1);
+        const int row = blk * BM + m;  // DH, FD: token row; DW: vocab row
+        const int ncols_half = p.d / 2;
+        // FD: the row's scale alpha, target term beta W_t, and the forward's
+        // outputs, from the two Z epilogue records of the row.
+        float alpha = 0.f, beta = 0.f;
+        long long trow = -1;
+        if (MODE == FD) {
+          if (!mbar_wait<true>(rd_full, rph, abort_flag, p.status)) break;
+          rph ^= 1u;
+          const uint32_t ra = z_rec + static_cast<uint32_t>(m) * REC_BYTES;
+          const uint32_t rb = z_rec + static_cast<uint32_t>(BM + m) * REC_BYTES;
+          const uint4 a0 = ld_cluster_v4(ra), a1 = ld_cluster_v4(ra + 16);
+          const uint4 b0 = ld_cluster_v4(rb), b1 = ld_cluster_v4(rb + 16);
+          mbar_arrive_cluster(z_rd_empty);
+          // S_other: the row's sum of e^s over its non-target columns.
+          const double S_other = __hiloint2double(static_cast<int>(a0.y), static_cast<int>(a0.x)) +
+                                 __hiloint2double(static_cast<int>(b0.y), static_cast<int>(b0.x));
+          const int flags = static_cast<int>(a1.y | b1.y);
+          const bool in_b = (b1.y & FL_HIT) != 0;
+          const double et = static_cast<double>(__uint_as_float(in_b ? b0.z : a0.z));
+          const double om = static_cast<double>(__uint_as_float(in_b ? b0.w : a0.w));
+          const bool tv = (flags & FL_TVALID) != 0;
+          const double S = tv ? S_other + et : S_other;
+          if (flags & FL_LIVE) {
+            alpha = static_cast<float>(-static_cast<double>(p.w) / S);
+            if (tv) {
+              // w (p_t - 1)(1 - tanh_t^2), p_t - 1 = -S_other / S (no cancellation).
+              beta = static_cast<float>(-static_cast<double>(p.w) * (S_other / S) * om);
+              trow = static_cast<long long>(static_cast<int>(a1.x));
+            }
+          }
+          if (hc == 0 && row < p.N) {
+            float nll = 0.f, lse = 0.f;
+            if (flags & FL_LIVE) {
+              lse = static_cast<float>(log(S));
+              nll = tv ? static_cast<float>(log1p(S_other / et)) : __int_as_float(0x7fc00000);
+            }
+            p.nll[row] = nll;
+            if (p.lse_out) p.lse_out[row] = lse;
+          }
+        }
+        // FD: W_t's columns of chunk ch (bf16), fetched one chunk ahead.
+        uint4 wcur[4], wnxt[4];
+        auto load_w = [&](int ch, uint4(&dst)[4]) {
+#pragma unroll
+          for (int v = 0; v < 4; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
+          if (trow >= 0) {
+            const uint4* src = reinterpret_cast<const uint4*>(p.W + trow * p.d + hc * ncols_half + ch * 32);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) dst[v] = __ldg(src + v);
+          }
+        };
+        if (MODE == FD) load_w(0, wcur);
         if (!mbar_wait(acc_full, fph, abort_flag, p.status)) break;
         fph ^= 1u;
         tc_fence_after();
-        const int row = blk * BM + m;  // DH: token row; DW: vocab row
-        const int ncols_half = p.d / 2;
         const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(hc * ncols_half);
 #pragma unroll 1
         for (int ch = 0; ch < ncols_half / 32; ++ch) {
+          if (MODE == FD && ch + 1 < ncols_half / 32) load_w(ch + 1, wnxt);
           uint32_t r[32];
           tmem_ld32(tb + ch * 32, r);
           tmem_ld_wait();
           reg_fence32(r);
           const int col = hc * ncols_half + ch * 32;
-          if (MODE == DH) {
+          if (MODE == FD) {
+            if (row < p.N) {
+              const uint32_t* wb = reinterpret_cast<const uint32_t*>(wcur);
+              __align__(16) __nv_bfloat16 o[32];
+#pragma unroll
+              for (int j = 0; j < 16; ++j) {
+                const float wl = __uint_as_float(wb[j] << 16);
+                const float wh = __uint_as_float(wb[j] & 0xffff0000u);
+                o[2 * j] = __float2bfloat16_rn(fmaf(alpha, __uint_as_float(r[2 * j]), beta * wl));
+                o[2 * j + 1] = __float2bfloat16_rn(fmaf(alpha, __uint_as_float(r[2 * j + 1]), beta * wh));
+              }
+              uint4* dst = reinterpret_cast<uint4*>(p.dh + static_cast<long long>(row) * p.ldh + col);
+#pragma unroll
+              for (int v = 0; v < 4; ++v) dst[v] = reinterpret_cast<const uint4*>(o)[v];
+            }
+#pragma unroll
+            for (int v = 0; v < 4; ++v) wcur[v] = wnxt[v];
+          } else if (MODE == DH) {
             if (row < p.N) {
               __align__(16) __nv_bfloat16 o[32];
 #pragma unroll
@@ -780,6 +1045,8 @@ inline int setup_attributes() {
   cudaError_t e = cudaFuncSetAttribute(bwd_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e == cudaSuccess)
     e = cudaFuncSetAttribute(bwd_kernel<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(bwd_kernel<FD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
   if (e != cudaSuccess) {
     set_last_error(std::string("cudaFuncSetAttribute(bwd): ") + cudaGetErrorString(e));
     return 3;
@@ -836,8 +1103,8 @@ inline int launch_mode(const CUtensorMap& tx, const CUtensorMap& ty, const CUten
 }
 
 inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long N, long long V, long long d,
-                  const int64_t* tgt, const uint8_t* mask, float c, const float* lse, float w, uint16_t* dh, float* dW,
-                  int accumulate, unsigned* status, void* scratch, int sms, cudaStream_t s) {
+                  const int64_t* tgt, const uint8_t* mask, float c, const float* lse, const float* nll, float w,
+                  uint16_t* dh, float* dW, int accumulate, unsigned* status, void* scratch, int sms, cudaStream_t s) {
   const uint32_t kc = static_cast<uint32_t>(d / KB);
   CUtensorMap tm_hx, tm_wx, tm_hy, tm_wy, tm_hs, tm_ws;
   if (int rc = make_map_bf16_3d(&tm_hx, h, d, N, ldh * 2, BM, ZSC); rc) return rc;
@@ -855,6 +1122,7 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
   p.tgt = tgt;
   p.mask = mask;
   p.lse = lse;
+  p.nll_in = nll;
   p.inv_c = 1.0f / c;
   p.cl2e = c * kLog2e;
   p.w = -w;  // the P tiles hold -G
@@ -899,6 +1167,43 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
     }
   }
   return 0;
+}
+
+// Forward + dh in one pass (FD mode): nll and lse (nullable) [N] fp32, dh
+// [N, ldh] bf16, for L = grad_scale * sum of nll over the scored rows.
+inline int launch_fd(const uint16_t* h, long long ldh, const uint16_t* W, long long N, long long V, long long d,
+                     const int64_t* tgt, const uint8_t* mask, float c, float grad_scale, float* nll, float* lse,
+                     uint16_t* dh, unsigned* status, int sms, cudaStream_t s) {
+  CUtensorMap tm_hx, tm_wy, tm_ws;
+  if (int rc = make_map_bf16_3d(&tm_hx, h, d, N, ldh * 2, BM, ZSC); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_wy, W, d, V, d * 2, BT, ZSC); rc) return rc;
+  if (int rc = make_map_bf16_3d(&tm_ws, W, d, V, d * 2, SLAB_ROWS, static_cast<uint32_t>(d / KB)); rc) return rc;
+  const int clusters_max = max_clusters(sms);
+  Params p{};
+  p.N = static_cast<int>(N);
+  p.V = static_cast<int>(V);
+  p.d = static_cast<int>(d);
+  p.KC = static_cast<int>(d / KB);
+  p.tgt = tgt;
+  p.mask = mask;
+  p.inv_c = 1.0f / c;
+  p.c = c;
+  p.cl2e = c * kLog2e;
+  p.w = grad_scale;
+  p.zlim2 = (kTanhXmax * c) * (kTanhXmax * c);
+  scaled_tanh_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
+  p.status = status;
+  p.W = reinterpret_cast<const __nv_bfloat16*>(W);
+  p.nll = nll;
+  p.lse_out = lse;
+  p.dh = reinterpret_cast<__nv_bfloat16*>(dh);
+  p.ldh = ldh;
+  p.n_blocks = static_cast<int>(cdivll(N, BM));
+  p.n_tiles = static_cast<int>(cdivll(V, BT));
+  p.split = 1;
+  p.n_units = p.n_blocks;
+  const int cl = static_cast<int>(p.n_units < clusters_max ? p.n_units : clusters_max);
+  return launch_mode<FD>(tm_hx, tm_wy, tm_ws, p, cl, s);
 }
 
 }  // namespace bwdk

@@ -31,11 +31,12 @@
 //    polynomial (packed fp32x2), summed in fp32 over the segment.  No running
 //    max is needed: |s| < c, so S = sum e^s lies in (V e^-c, V e^c) and
 //    cannot overflow for the accepted c (the host rejects c > c_max(V)).
-//  * outputs: per (segment, column half) the partial sum into
-//    part[2 s + half][row], s = the segment's first tile inside its row pair
-//    (< VT); the target logit s_t into st[row] by the one thread whose
-//    columns hold t.  A finalize kernel adds the partials in a fixed order
-//    (deterministic) and forms lse and nll.
+//  * outputs: per (segment, column half) the partial sum over the non-target
+//    columns into part[2 s + half][row], s = the segment's first tile inside
+//    its row pair (< VT); the target's term e^{s_t} into st[row] by the one
+//    thread whose columns hold t.  A finalize kernel adds the partials in a
+//    fixed order (deterministic) and forms lse = ln(S_other + e^{s_t}) and
+//    nll = log1p(S_other / e^{s_t}).
 #pragma once
 #include <cuda_runtime.h>
 
@@ -80,8 +81,8 @@ struct Params {
   float inv_c, c;
   float zlim2;          // (kTanhXmax * c)^2: range of the polynomial in z^2
   float k[kTanhTerms];  // c log2(e) C_i / c^(2i+1): 2^(z P(z^2)) = e^(c tanh(z/c))
-  float* part;          // [2 maxseg][N_pad] partial sums of e^s
-  float* st;            // [N] softcapped target logit
+  float* part;          // [2 maxseg][N_pad] partial sums of e^s over the non-target columns
+  float* st;            // [N] e^{s_t}, the target column's term
   unsigned* status;
 };
 
@@ -91,17 +92,26 @@ struct Params {
 struct ChunkF32 {
   uint32_t v[32];
 };
-__device__ __noinline__ float chunk_sum_slow(ChunkF32 r, float c, float inv_c, int lim) {
-  float a0 = 0.f, a1 = 0.f;
+// Returns (sum over the non-target columns, the target column's term).
+__device__ __noinline__ float2 chunk_sum_slow(ChunkF32 r, float c, float inv_c, int lim, int rel) {
+  float a0 = 0.f, a1 = 0.f, et = 0.f;
   const float cl2e = c * kLog2e;
 #pragma unroll
   for (int j = 0; j < 32; j += 2) {
-    const float e0 = ex2_approx(cl2e * tanh_any(__uint_as_float(r.v[j]) * inv_c));
-    const float e1 = ex2_approx(cl2e * tanh_any(__uint_as_float(r.v[j + 1]) * inv_c));
+    float e0 = ex2_approx(cl2e * tanh_any(__uint_as_float(r.v[j]) * inv_c));
+    float e1 = ex2_approx(cl2e * tanh_any(__uint_as_float(r.v[j + 1]) * inv_c));
+    if (j == rel) {
+      et = e0;
+      e0 = 0.f;
+    }
+    if (j + 1 == rel) {
+      et = e1;
+      e1 = 0.f;
+    }
     a0 += (j < lim) ? e0 : 0.f;
     a1 += (j + 1 < lim) ? e1 : 0.f;
   }
-  return a0 + a1;
+  return make_float2(a0 + a1, et);
 }
 
 // Sum over 32 columns of 2^(c log2e tanh(z/c)), packed fp32x2: per column
@@ -110,8 +120,13 @@ __device__ __noinline__ float chunk_sum_slow(ChunkF32 r, float c, float inv_c, i
 // except in the last vocab tile).  If some |z| may exceed the polynomial's
 // range (sum of z^2 over the chunk > (kTanhXmax c)^2, a conservative test),
 // the warp recomputes the chunk with the exact-form tanh.
+// kHit: the column `rel` (the thread's target, if in this chunk) is left out
+// of the sum and its term returned in et.  Keeping e^{s_t} apart lets the
+// finalize form nll = log1p(S_other / e^{s_t}), which keeps its relative
+// precision when p_t -> 1 (lse - s_t would cancel in fp32).
+template <bool kHit>
 __device__ __forceinline__ float chunk_sum(const uint32_t (&r)[32], const float2 (&k)[kTanhTerms], const Params& p,
-                                           int lim) {
+                                           int lim, int rel, float& et) {
   float2 s0 = make_float2(0.f, 0.f), s1 = s0, su = s0;
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
@@ -124,6 +139,16 @@ __device__ __forceinline__ float chunk_sum(const uint32_t (&r)[32], const float2
       e.x = (2 * j < lim) ? e.x : 0.f;
       e.y = (2 * j + 1 < lim) ? e.y : 0.f;
     }
+    if (kHit) {
+      if (2 * j == rel) {
+        et = e.x;
+        e.x = 0.f;
+      }
+      if (2 * j + 1 == rel) {
+        et = e.y;
+        e.y = 0.f;
+      }
+    }
     if (j & 1)
       s1 = __fadd2_rn(s1, e);
     else
@@ -134,24 +159,28 @@ __device__ __forceinline__ float chunk_sum(const uint32_t (&r)[32], const float2
     ChunkF32 c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) c.v[j] = r[j];
-    s = chunk_sum_slow(c, p.c, p.inv_c, lim);
+    const float2 o = chunk_sum_slow(c, p.c, p.inv_c, lim, kHit ? rel : -1);
+    s = o.x;
+    if (kHit && rel >= 0 && rel < 32) et = o.y;
   }
   return s;
 }
 
-// Target logit: the thread whose target column falls in this chunk takes
-// z from its registers (predicated selects, only when some lane hits).
-__device__ __forceinline__ void pick_target(const uint32_t (&r)[32], long long rel, const Params& p, float& st_val,
-                                            bool& st_hit) {
-  const bool hit = (rel >= 0 && rel < 32);
-  if (__any_sync(0xffffffffu, hit)) {
-    float zt = 0.f;
-#pragma unroll
-    for (int j = 0; j < 32; ++j) zt = (rel == j) ? __uint_as_float(r[j]) : zt;
-    if (hit) {
-      st_val = p.c * tanh_any(zt * p.inv_c);
+// One chunk of the epilogue: the sum over its non-target columns (added to
+// seg_sum) and, for the thread whose target column is in it, e^{s_t}.
+__device__ __forceinline__ void chunk_terms(const uint32_t (&r)[32], const float2 (&k)[kTanhTerms], const Params& p,
+                                            int lim, long long relw, float& seg_sum, float& st_val, bool& st_hit) {
+  const int rel = (relw >= 0 && relw < 32) ? static_cast<int>(relw) : -1;
+  if (__any_sync(0xffffffffu, rel >= 0)) {
+    float et = 0.f;
+    if (lim > 0) seg_sum += chunk_sum<true>(r, k, p, lim, rel, et);
+    if (rel >= 0) {
+      st_val = et;
       st_hit = true;
     }
+  } else {
+    float et = 0.f;
+    if (lim > 0) seg_sum += chunk_sum<false>(r, k, p, lim, -1, et);
   }
 }
 
@@ -357,9 +386,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(tbase + (ch + 1) * 32, rc);
         {
           const int cbase = col0 + ch * 32;
-          const int lim = min(32, p.V - cbase);
-          if (lim > 0) seg_sum += chunk_sum(ra, k2, p, lim);
-          pick_target(ra, t - cbase, p, st_val, st_hit);
+          chunk_terms(ra, k2, p, min(32, p.V - cbase), t - cbase, seg_sum, st_val, st_hit);
         }
         tmem_ld_wait();
         reg_fence32(rc);
@@ -377,9 +404,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         {
           const int cbase = col0 + (ch + 1) * 32;
-          const int lim = min(32, p.V - cbase);
-          if (lim > 0) seg_sum += chunk_sum(rc, k2, p, lim);
-          pick_target(rc, t - cbase, p, st_val, st_hit);
+          chunk_terms(rc, k2, p, min(32, p.V - cbase), t - cbase, seg_sum, st_val, st_hit);
         }
         if (ch + 2 < 4) {
           tmem_ld_wait();

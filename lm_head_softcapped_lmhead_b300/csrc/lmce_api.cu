@@ -198,6 +198,12 @@ namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The one-pass forward + dh accumulates sum_j e^{s_ij} (1 - tanh^2) W_j in
+// fp32 before normalising, which stays finite while V e^c max|W| < 3.4e38:
+// up to c = 60 that allows |W| up to about 3e8.  Larger softcaps take the
+// forward and the dh pass as two launches.
+constexpr float kFusedSoftcapMax = 60.0f;
+
 float softcap_max(int64_t V) {
   // e^{-c} must stay a normal float (c < 87.3) and V e^{c} finite (c + ln V < 88.7);
   // keep a margin of 2 on both.
@@ -345,8 +351,9 @@ int lmhead_ce_fwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N
 }
 
 int lmhead_ce_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
-                  const int64_t* tgt, const uint8_t* row_mask, float softcap, const float* lse, float grad_scale,
-                  lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes, void* stream) {
+                  const int64_t* tgt, const uint8_t* row_mask, float softcap, const float* lse, const float* nll,
+                  float grad_scale, lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes,
+                  void* stream) {
   if (int rc = check_common(h, ldh, W, N, V, d, tgt, softcap, ws); rc) return rc;
   if (!lse || (!dh && !dW)) return LMCE_EINVAL;
   if (dh && !aligned16(dh)) return LMCE_EINVAL;
@@ -357,9 +364,50 @@ int lmhead_ce_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N
   DevInfo di;
   if (int rc = dev_info(&di); rc) return rc;
   char* w = static_cast<char*>(ws);
-  return lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, grad_scale, dh, dW, accumulate_dW,
-                            reinterpret_cast<unsigned*>(w + L.status), w + L.bwd, di.sms,
+  return lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, dW,
+                            accumulate_dW, reinterpret_cast<unsigned*>(w + L.status), w + L.bwd, di.sms,
                             static_cast<cudaStream_t>(stream));
+}
+
+int lmhead_ce_fwd_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+                      const int64_t* tgt, const uint8_t* row_mask, float softcap, float grad_scale, float* nll,
+                      float* lse, lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes,
+                      void* stream) {
+  if (int rc = check_common(h, ldh, W, N, V, d, tgt, softcap, ws); rc) return rc;
+  if (!nll || !lse) return LMCE_EINVAL;
+  if (dh && !aligned16(dh)) return LMCE_EINVAL;
+  if (dW && !aligned16(dW)) return LMCE_EINVAL;
+  if (!std::isfinite(grad_scale)) return LMCE_EINVAL;
+  const Layout L = make_layout(N, V, d, row_mask ? LMCE_WS_MASKED : 0u);
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  char* w = static_cast<char*>(ws);
+  unsigned* status = reinterpret_cast<unsigned*>(w + L.status);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dh && softcap <= kFusedSoftcapMax) {
+    // Forward and dh in one pass over the vocabulary.
+    if (int rc = lmce::bwdk::launch_fd(h, ldh, W, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, status,
+                                       di.sms, s);
+        rc)
+      return rc;
+  } else {
+    if (int rc = fwd_impl(h, ldh, W, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, 0u); rc)
+      return rc;
+    if (dh) {
+      if (int rc = lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh,
+                                      nullptr, 0, status, w + L.bwd, di.sms, s);
+          rc)
+        return rc;
+    }
+  }
+  if (dW) {
+    if (int rc = lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, nullptr, dW,
+                                    accumulate_dW, status, w + L.bwd, di.sms, s);
+        rc)
+      return rc;
+  }
+  return LMCE_OK;
 }
 
 int lmhead_ce_fwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
@@ -381,7 +429,8 @@ int lmhead_ce_fwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const
 
 int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
                        int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
-                       const float* lse, float grad_scale, lmce_bf16* dh, void* ws, size_t ws_bytes, void* stream) {
+                       const float* lse, const float* nll, float grad_scale, lmce_bf16* dh, void* ws,
+                       size_t ws_bytes, void* stream) {
   if (int rc = check_int4(Wq, scales, group, V, d); rc) return rc;
   if (!ws || !aligned16(ws) || !dh) return LMCE_EINVAL;
   const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_INT4 | (row_mask ? LMCE_WS_MASKED : 0u));
@@ -392,7 +441,7 @@ int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const
   if (int rc = dev_info(&di); rc) return rc;
   if (int rc = dequant_impl(Wq, scales, V, d, group, wdeq, static_cast<cudaStream_t>(stream), di.sms); rc)
     return rc;
-  return lmhead_ce_bwd(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, lse, grad_scale, dh, nullptr, 0, ws,
+  return lmhead_ce_bwd(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, nullptr, 0, ws,
                        ws_bytes, stream);
 }
 

@@ -74,13 +74,29 @@ def test_bwd_host_validation(L):
     P = ctypes.c_void_p
 
     def bwd(lse=A, w=1.0, dh=A, dW=A, d=512):
-        return L.lmhead_ce_bwd(P(A), 512, P(A), 100, 200, d, P(A), None, 30.0, P(lse), w, P(dh), P(dW), 0, P(A),
-                               1 << 40, None)
+        return L.lmhead_ce_bwd(P(A), 512, P(A), 100, 200, d, P(A), None, 30.0, P(lse), None, w, P(dh), P(dW), 0,
+                               P(A), 1 << 40, None)
     assert bwd(lse=0) == EINVAL
     assert bwd(dh=0, dW=0) == EINVAL
     assert bwd(w=float("nan")) == EINVAL
     assert bwd(dh=A + 4) == EINVAL
     assert bwd(d=96) == ENOTSUP
+
+
+def test_fwd_bwd_host_validation(L):
+    P = ctypes.c_void_p
+
+    def fb(nll=A, lse=A, w=1.0, dh=A, dW=A, d=512, c=30.0, ws_bytes=1 << 40):
+        return L.lmhead_ce_fwd_bwd(P(A), 512, P(A), 100, 200, d, P(A), None, c, w, P(nll), P(lse), P(dh), P(dW), 0,
+                                   P(A), ws_bytes, None)
+    assert fb(nll=0) == EINVAL
+    assert fb(lse=0) == EINVAL               # the dW pass and the caller's backward need lse
+    assert fb(w=float("inf")) == EINVAL
+    assert fb(dh=A + 4) == EINVAL
+    assert fb(dW=A + 8) == EINVAL
+    assert fb(d=96) == ENOTSUP
+    assert fb(c=82.0) == ENOTSUP
+    assert fb(ws_bytes=100) == EINVAL
 
 
 def test_int4_host_validation(L):

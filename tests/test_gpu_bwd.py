@@ -17,7 +17,7 @@ def lm():
     return lm
 
 
-def run_fwd_bwd(lm, d_inp, c, grad_scale, mask=None, want_dh=True, want_dW=True, dW_init=None):
+def run_fwd_bwd(lm, d_inp, c, grad_scale, mask=None, want_dh=True, want_dW=True, dW_init=None, pass_nll=False):
     N, d = d_inp["h"].shape
     V = d_inp["W"].shape[0]
     ws = lm.workspace(N, V, d, lm.LMCE_WS_MASKED if mask is not None else 0)
@@ -29,7 +29,7 @@ def run_fwd_bwd(lm, d_inp, c, grad_scale, mask=None, want_dh=True, want_dW=True,
     if want_dW:
         dW = torch.full((V, d), float("nan"), device="cuda") if dW_init is None else dW_init.clone()
     lm.lmhead_ce_bwd(d_inp["h"], d_inp["W"], d_inp["tgt"], c, lse, grad_scale, dh=dh, dW=dW,
-                     accumulate_dW=dW_init is not None, row_mask=mask, ws=ws)
+                     accumulate_dW=dW_init is not None, row_mask=mask, ws=ws, nll=nll if pass_nll else None)
     assert lm.lmce_status(ws) == lm.LMCE_OK
     return nll, lse, dh, dW
 
@@ -88,7 +88,7 @@ def test_bwd_config2_full(lm, oracle_mod):
     N = inp["N"]
     d_inp = dev_inputs(inp)
     w = 1.0 / N
-    _, lse, dh, dW = run_fwd_bwd(lm, d_inp, 30.0, w)
+    _, lse, dh, dW = run_fwd_bwd(lm, d_inp, 30.0, w, pass_nll=True)
     rows = np.random.default_rng(1).choice(N, 24, replace=False)
     _, ref_lse = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], 30.0, rows=rows)
     ref = oracle_mod.dh_rows(inp["h"], inp["W"], inp["tgt"], 30.0, rows, ref_lse, w)
@@ -106,3 +106,21 @@ def test_bwd_deterministic(lm):
     r1 = run_fwd_bwd(lm, d_inp, 30.0, 1 / 2048)
     r2 = run_fwd_bwd(lm, d_inp, 30.0, 1 / 2048)
     assert torch.equal(r1[2], r2[2]) and torch.equal(r1[3], r2[3])
+
+
+def test_bwd_confident_rows_with_nll(lm, oracle_mod):
+    """Rows with p_t within about 1e-4 of 1: given the forward's nll, the
+    target's p - 1 is expm1(-nll) and dh, dW stay within tolerance (from
+    lse alone, s_t - lse cancels in fp32 there)."""
+    from test_gpu_fwd_bwd import confident_inputs
+    inp = confident_inputs()
+    N = inp["N"]
+    d_inp = dev_inputs(inp)
+    for mask in (None, (np.arange(N) % 3 != 1).astype(np.uint8)):
+        M = N if mask is None else int(mask.sum())
+        mk = None if mask is None else torch.from_numpy(mask).cuda()
+        _, _, dh, dW = run_fwd_bwd(lm, d_inp, 30.0, 1.0 / M, mask=mk, pass_nll=True)
+        _, ref_lse = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], 30.0, mask=mask)
+        ref_dh, ref_dW = oracle_mod.bwd(inp["h"], inp["W"], inp["tgt"], 30.0, ref_lse, 1.0 / M, mask=mask)
+        assert rel_fro(bf16_to_f64(dh), ref_dh) <= GRAD_RTOL
+        assert rel_fro(dW.cpu().numpy(), ref_dW) <= GRAD_RTOL

@@ -1,0 +1,163 @@
+"""Training-step entry point lmhead_ce_fwd_bwd (through the C ABI) against the
+fp64 oracle on the same bf16 inputs: nll and lse of the forward, dh and dW of
+the backward.  With dh requested and softcap <= 60 the forward and dh come
+from one pass that normalises after the accumulation; these tests cover that
+pass's ragged tiles, the exact-tanh path, masks, confident rows (p_t near 1),
+bad targets and the full training micro-batch size."""
+import numpy as np
+import pytest
+import torch
+
+import synth_inputs as si
+from gpu_util import GRAD_RTOL, NLL_ATOL, bf16_to_f64, dev_inputs, rel_fro
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def lm():
+    import lm_head_softcapped_lmhead_b300 as lm
+    lm.lib()
+    return lm
+
+
+def run_train(lm, d_inp, c, w, mask=None, want_dh=True, want_dW=True, dW_init=None):
+    N, d = d_inp["h"].shape
+    V = d_inp["W"].shape[0]
+    ws = lm.workspace(N, V, d, lm.LMCE_WS_MASKED if mask is not None else 0)
+    nll = torch.full((N,), float("nan"), device="cuda")
+    lse = torch.full((N,), float("nan"), device="cuda")
+    dh = torch.full_like(d_inp["h"], float("nan")) if want_dh else None
+    dW = None
+    if want_dW:
+        dW = torch.full((V, d), float("nan"), device="cuda") if dW_init is None else dW_init.clone()
+    lm.lmhead_ce_fwd_bwd(d_inp["h"], d_inp["W"], d_inp["tgt"], c, w, nll, lse, dh=dh, dW=dW,
+                         accumulate_dW=dW_init is not None, row_mask=mask, ws=ws)
+    return lm.lmce_status(ws), nll, lse, dh, dW
+
+
+def check_against_oracle(oracle_mod, inp, c, w, nll, lse, dh, dW, mask=None):
+    ref_nll, ref_lse = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], c, mask=mask)
+    assert np.abs(nll.cpu().numpy() - ref_nll).max() <= NLL_ATOL
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= NLL_ATOL
+    ref_dh, ref_dW = oracle_mod.bwd(inp["h"], inp["W"], inp["tgt"], c, ref_lse, w, mask=mask,
+                                    want_dh=dh is not None, want_dW=dW is not None)
+    if dh is not None:
+        assert rel_fro(bf16_to_f64(dh), ref_dh) <= GRAD_RTOL
+    if dW is not None:
+        assert rel_fro(dW.cpu().numpy(), ref_dW) <= GRAD_RTOL
+
+
+@pytest.mark.parametrize("cfg,N,V,d,w_scale,c", [
+    (2, 300, 700, 256, 1.0, 30.0),     # ragged N and V
+    (2, 512, 1024, 512, 1.0, 30.0),    # d = 512, whole tiles
+    (2, 257, 1000, 512, 50.0, 30.0),   # W x 50: the cap is active, exact-tanh chunks
+    (2, 200, 300, 64, 20.0, 2.0),      # c = 2, d = 64 (one K chunk)
+    (2, 150, 260, 192, 1.0, 30.0),     # odd number of 64-chunks
+    (2, 130, 100, 128, 1.0, 30.0),     # V below one 128-column tile
+    (1, 4096, 1024, 512, 1.0, 30.0),   # tiny-forward config shape
+    (2, 300, 700, 256, 1.0, 70.0),     # softcap above 60: forward and dh as two passes
+])
+def test_fwd_bwd_matches_oracle(lm, oracle_mod, cfg, N, V, d, w_scale, c):
+    inp = si.make_inputs(cfg, N=N, V=V, d=d, w_scale=w_scale)
+    w = 1.0 / N
+    st, nll, lse, dh, dW = run_train(lm, dev_inputs(inp), c, w)
+    assert st == lm.LMCE_OK
+    check_against_oracle(oracle_mod, inp, c, w, nll, lse, dh, dW)
+
+
+def test_fwd_bwd_without_dh(lm, oracle_mod):
+    inp = si.make_inputs(2, N=260, V=390, d=256)
+    st, nll, lse, dh, dW = run_train(lm, dev_inputs(inp), 30.0, 0.5, want_dh=False)
+    assert st == lm.LMCE_OK
+    check_against_oracle(oracle_mod, inp, 30.0, 0.5, nll, lse, None, dW)
+
+
+def test_fwd_bwd_mask_and_accumulate(lm, oracle_mod):
+    N, V, d = 400, 600, 128
+    inp = si.make_inputs(2, N=N, V=V, d=d, w_scale=10.0)
+    mask = (np.arange(N) % 5 != 2).astype(np.uint8)
+    M = int(mask.sum())
+    d_inp = dev_inputs(inp)
+    init = torch.randn(V, d, device="cuda") * 1e-3
+    st, nll, lse, dh, dW = run_train(lm, d_inp, 30.0, 1.0 / M, mask=torch.from_numpy(mask).cuda(), dW_init=init)
+    assert st == lm.LMCE_OK
+    dh_np = bf16_to_f64(dh)
+    assert np.all(dh_np[mask == 0] == 0)
+    assert np.all(nll.cpu().numpy()[mask == 0] == 0) and np.all(lse.cpu().numpy()[mask == 0] == 0)
+    check_against_oracle(oracle_mod, inp, 30.0, 1.0 / M, nll, lse, dh, dW - init, mask=mask)
+
+
+def confident_inputs(N=256, V=2048, d=512, zt=20.0, seed=7):
+    """Rows whose target logit is about zt (the others stay near 0), so that
+    p_t is within about 1e-3 of 1 and the target's gradient term nearly
+    cancels: a bf16 rounding of the target column before that cancellation
+    would show up here as a large relative error in dh."""
+    rng = np.random.default_rng(seed)
+    W = si.f32_to_bf16_bits(rng.normal(0.0, 0.02, (V, d)).astype(np.float32))
+    W64 = si.bf16_bits_to_f32(W).astype(np.float64)
+    tgt = rng.integers(0, V, N).astype(np.int64)
+    h = zt * W64[tgt] / (W64[tgt] ** 2).sum(axis=1, keepdims=True)
+    return dict(h=si.f32_to_bf16_bits(h.astype(np.float32)), W=W, tgt=tgt,
+                nbytes=np.ones(N, dtype=np.int32), mask=None, N=N)
+
+
+def test_fwd_bwd_confident_rows(lm, oracle_mod):
+    inp = confident_inputs()
+    N = inp["N"]
+    st, nll, lse, dh, dW = run_train(lm, dev_inputs(inp), 30.0, 1.0 / N)
+    assert st == lm.LMCE_OK
+    ref_nll, _ = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], 30.0)
+    assert ref_nll.max() < 1e-2  # the construction gives p_t near 1
+    check_against_oracle(oracle_mod, inp, 30.0, 1.0 / N, nll, lse, dh, dW)
+
+
+def test_fwd_bwd_bad_target(lm, oracle_mod):
+    N, V, d = 300, 500, 128
+    inp = si.make_inputs(2, N=N, V=V, d=d)
+    bad = 123
+    tgt_bad = inp["tgt"].copy()
+    tgt_bad[bad] = V
+    d_inp = dev_inputs(inp)
+    d_inp["tgt"] = torch.from_numpy(tgt_bad).cuda()
+    st, nll, lse, dh, _ = run_train(lm, d_inp, 30.0, 1.0 / N, want_dW=False)
+    assert st == lm.LMCE_EDATA
+    n = nll.cpu().numpy()
+    assert np.isnan(n[bad])
+    ok = np.arange(N) != bad
+    ref_nll, ref_lse = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], 30.0)
+    assert np.abs(n[ok] - ref_nll[ok]).max() <= NLL_ATOL
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= NLL_ATOL
+    assert np.all(np.isfinite(bf16_to_f64(dh)))
+
+
+def test_fwd_bwd_training_batch_full(lm, oracle_mod):
+    """The training micro-batch (N=65536, V=8192, d=512) at full size, in the
+    launch configuration bench.py times: nll and dh on 32 sampled rows
+    against the oracle, every nll finite, and dW through <dh, h> = <dW, W>
+    (which holds at any size)."""
+    inp = si.make_inputs(3)
+    N = inp["N"]
+    w = 1.0 / N
+    d_inp = dev_inputs(inp)
+    st, nll, lse, dh, dW = run_train(lm, d_inp, 30.0, w)
+    assert st == lm.LMCE_OK
+    n = nll.cpu().numpy()
+    assert np.all(np.isfinite(n))
+    rows = np.random.default_rng(3).choice(N, 32, replace=False)
+    ref_nll, ref_lse = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], 30.0, rows=rows)
+    assert np.abs(n[rows] - ref_nll).max() <= NLL_ATOL
+    ref = oracle_mod.dh_rows(inp["h"], inp["W"], inp["tgt"], 30.0, rows, ref_lse, w)
+    assert rel_fro(bf16_to_f64(dh)[rows], ref) <= GRAD_RTOL
+    a = float((bf16_to_f64(dh) * bf16_to_f64(d_inp["h"])).sum())
+    b = float((dW.double().cpu().numpy() * bf16_to_f64(d_inp["W"])).sum())
+    assert abs(a - b) <= 2e-2 * max(abs(a), abs(b))
+
+
+def test_fwd_bwd_deterministic(lm):
+    inp = si.make_inputs(2, N=2048, V=2048, d=512)
+    d_inp = dev_inputs(inp)
+    r1 = run_train(lm, d_inp, 30.0, 1 / 2048)
+    r2 = run_train(lm, d_inp, 30.0, 1 / 2048)
+    for a, b in zip(r1[1:], r2[1:]):
+        assert torch.equal(a, b)

@@ -57,7 +57,8 @@ def test_int4_fwd_bwd_match_oracle(lm, oracle_mod, N, V):
     lse = torch.zeros(N, device="cuda")
     lm.lmhead_ce_fwd_int4(d_inp["h"], d_inp["Wq"], d_inp["scales"], 64, 30.0, d_inp["tgt"], nll, lse, ws=ws)
     dh = torch.zeros_like(d_inp["h"])
-    lm.lmhead_ce_bwd_int4(d_inp["h"], d_inp["Wq"], d_inp["scales"], 64, 30.0, d_inp["tgt"], lse, 1.0 / N, dh, ws=ws)
+    lm.lmhead_ce_bwd_int4(d_inp["h"], d_inp["Wq"], d_inp["scales"], 64, 30.0, d_inp["tgt"], lse, 1.0 / N, dh, ws=ws,
+                          nll=nll)
     assert lm.lmce_status(ws) == lm.LMCE_OK
     ref_nll, ref_lse = oracle_mod.fwd(inp["h"], Wdeq, inp["tgt"], 30.0)
     assert np.abs(nll.cpu().numpy() - ref_nll).max() <= NLL_ATOL
