@@ -61,10 +61,10 @@ constexpr int KB = 64;    // K elements per chunk
 constexpr int MAX_KC = 8; // d <= 512
 constexpr int YSTAGES = 3;  // Z ring: stages of four 64-column chunks (64 KB, one TMA load each)
 constexpr int ZSC = 4;      // chunks per Z ring stage
-constexpr int EPI_WARPS = 8;
-constexpr int TMA_WARP = 8;
-constexpr int MMA_WARP = 9;
-constexpr int THREADS = 320;
+constexpr int EPI_WARPS = 16;  // Z: epilogue warps; A: drain warps
+constexpr int TMA_WARP = 16;
+constexpr int MMA_WARP = 17;
+constexpr int THREADS = 576;
 constexpr uint32_t CHUNK = 128 * KB * 2;  // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t ZSTAGE = ZSC * CHUNK;   // 64 KB
 // The A CTA loads its Y tile in 4 slabs of 32 rows x d (one TMA load per
@@ -80,7 +80,7 @@ constexpr uint32_t SLAB_CHUNK = SLAB_ROWS * KB * 2;  // 4 KB
 constexpr uint32_t Z_Y = 0;                             // ring of YSTAGES stages
 constexpr uint32_t Z_END = Z_Y + YSTAGES * ZSTAGE;
 constexpr uint32_t Z_TMEM_X = 256;
-// FD: per-row records of the Z epilogue, [column half][row] x 32 bytes:
+// FD: per-row records of the Z epilogue, [column group][row] x 32 bytes:
 // {double sum of e^s over the non-target columns, float e^{s_t},
 //  1 - tanh_t^2, int target, int flags}.
 constexpr uint32_t Z_REC = Z_END;
@@ -93,7 +93,7 @@ constexpr uint32_t P_SLOT = 2 * CHUNK;                  // 32 KB
 constexpr uint32_t A_END = A_P + 2 * P_SLOT;
 constexpr uint32_t BAR_OFF = (Z_END > A_END ? Z_END : A_END);
 constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;
-static_assert(Z_REC + 2 * BM * REC_BYTES <= BAR_OFF, "FD row records overlap the barriers");
+static_assert(Z_REC + (EPI_WARPS / 4) * BM * REC_BYTES <= BAR_OFF, "FD row records overlap the barriers");
 constexpr uint32_t Z_TMEM_COLS = 512;
 constexpr uint32_t A_TMEM_COLS = 512;
 constexpr uint32_t IDESC_Z = idesc_bf16_f32(128, BT, false, false);
@@ -357,6 +357,18 @@ __device__ __forceinline__ float g_chunk_fd(const uint32_t (&r)[32], const EpiCo
   return sum;
 }
 
+// A unit's tiles are visited from an offset that depends on its cluster
+// slot: clusters that swept the streamed operand in the same order would all
+// request the same tile from L2 at once.
+__device__ __forceinline__ int unit_rot(int u, int n, int n_clusters) {
+  return n > 0 ? static_cast<int>((static_cast<long long>(u % n_clusters) * n) / n_clusters) : 0;
+}
+__device__ __forceinline__ int rot_tile(int t0, int n, int i, int rot) {
+  int j = i + rot;
+  if (j >= n) j -= n;
+  return t0 + j;
+}
+
 // Split-major order: clusters running at the same time share a row range
 // of the streamed operand, which then stays in L2.
 __device__ __forceinline__ void unit_range(const Params& p, int u, int& blk, int& t0, int& t1) {
@@ -418,8 +430,8 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(ay_empty + i, 1);
     }
     mbar_init(mma_done, 1);
-    mbar_init(rd_full, 2 * BM);
-    mbar_init(rd_empty, 2 * BM);
+    mbar_init(rd_full, EPI_WARPS * 32);   // every Z epilogue thread
+    mbar_init(rd_empty, EPI_WARPS * 32);  // every A drain thread
     *abort_flag = 0;
     fence_mbar_init();
     fence_proxy_async_smem();
@@ -462,9 +474,12 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
+          const int nt_u = t1 - t0, rot = bwdk::unit_rot(u, nt_u, n_clusters);
           for (int s4 = 0; s4 < nst && ok; ++s4) ok = put(&tm_x, blk * BM, s4);
-          for (int t = t0; t < t1 && ok; ++t)
+          for (int i = 0; i < nt_u && ok; ++i) {
+            const int t = bwdk::rot_tile(t0, nt_u, i, rot);
             for (int s4 = 0; s4 < nst && ok; ++s4) ok = put(&tm_y, t * BT, s4);
+          }
         }
         if (!ok) {
           const long long c0 = clock64();
@@ -483,6 +498,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
+          const int nt_u = t1 - t0, rot = bwdk::unit_rot(u, nt_u, n_clusters);
           if (!first) {
             // X in TMEM is overwritten only after the previous unit's MMAs.
             umma_commit(x_free);
@@ -516,7 +532,8 @@ __global__ void __launch_bounds__(THREADS, 1)
           rph ^= 1u;
           if (!ok) break;
           tc_fence_after();
-          for (int t = t0; t < t1 && ok; ++t) {
+          for (int i = 0; i < nt_u && ok; ++i) {
+            const int t = bwdk::rot_tile(t0, nt_u, i, rot);
             ok = mbar_wait(acc_empty + acc, aph ^ 1u, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
@@ -525,14 +542,25 @@ __global__ void __launch_bounds__(THREADS, 1)
               ok = mbar_wait(zy_full + stage, phase, abort_flag, p.status);
               if (!ok) break;
               tc_fence_after();
-              for (int c = 0; c < ZSC; ++c) {
-                const int kc = ZSC * s4 + c;
-                if (kc >= p.KC) break;
-                const uint32_t ya = smem_u32(smem + Z_Y + stage * ZSTAGE + c * CHUNK);
+              // The issue loop stays short (descriptors advanced by constant
+              // offsets, unrolled): one M=128 N=128 MMA is 64 tensor cycles.
+              const uint64_t b0 = sdesc_sw128(smem_u32(smem + Z_Y + stage * ZSTAGE), 16, 1024);
+              const uint32_t a0 = tmem_base + Z_TMEM_X + static_cast<uint32_t>(s4 * ZSC * 32);
+              if (ZSC * (s4 + 1) <= p.KC) {
 #pragma unroll
-                for (int k = 0; k < KB / 16; ++k)
-                  umma_bf16_ts(d_tmem, tmem_base + Z_TMEM_X + static_cast<uint32_t>(kc * 32 + k * 8),
-                               sdesc_sw128(ya + k * 32, 16, 1024), IDESC_Z, (kc | k) != 0 ? 1u : 0u);
+                for (int c = 0; c < ZSC; ++c)
+#pragma unroll
+                  for (int k = 0; k < KB / 16; ++k)
+                    umma_bf16_ts(d_tmem, a0 + static_cast<uint32_t>(c * 32 + k * 8),
+                                 b0 + static_cast<uint64_t>((c * CHUNK + k * 32) >> 4), IDESC_Z,
+                                 (s4 | c | k) != 0 ? 1u : 0u);
+              } else {
+                for (int c = 0; c < p.KC - ZSC * s4; ++c)
+#pragma unroll
+                  for (int k = 0; k < KB / 16; ++k)
+                    umma_bf16_ts(d_tmem, a0 + static_cast<uint32_t>(c * 32 + k * 8),
+                                 b0 + static_cast<uint64_t>((c * CHUNK + k * 32) >> 4), IDESC_Z,
+                                 (s4 | c | k) != 0 ? 1u : 0u);
               }
               umma_commit(zy_empty + stage);
               if (++stage == YSTAGES) {
@@ -553,8 +581,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     } else {
       // ---- Z epilogue: z tile -> P tile in the peer's shared memory ----
-      const int q = warp & 3;    // lanes 32q .. 32q+31
-      const int hc = warp >> 2;  // columns 64hc .. 64hc+63 (one K chunk of P)
+      // Warp w reads TMEM lanes 32 (w % 4) .. +31 (its 32 rows) and columns
+      // 32 (w / 4) .. +31 of each tile: one 32-column chunk per warp and tile,
+      // four warps per scheduler so that TMEM loads, math and the DSMEM stores
+      // of different warps overlap.
+      const int q = warp & 3;
+      const int cq = warp >> 2;     // 32-column group of the tile
       const int m = q * 32 + lane;  // row of the P tile (= TMEM lane)
       EpiConst kc;
 #pragma unroll
@@ -565,15 +597,12 @@ __global__ void __launch_bounds__(THREADS, 1)
       kc.inv_c = p.inv_c;
       kc.cl2e = p.cl2e;
       const float kNegInf = __int_as_float(0xff800000);
-      // DW: row data of the warp's 64 columns (lane j holds columns j and
-      // 32 + j): -lse log2(e) (-inf for rows that do not count) and the block
-      // lane of the row's target.  pf_* is the next tile's, fetched early.
-      float cur_nl[2] = {kNegInf, kNegInf};
-      int cur_hit[2] = {-1, -1};
-      float cur_pm1[2] = {0.f, 0.f};
-      float pf_nl[2] = {kNegInf, kNegInf};
-      int pf_hit[2] = {-1, -1};
-      float pf_pm1[2] = {0.f, 0.f};
+      // DW: row data of the warp's 32 columns (lane j holds column j):
+      // -lse log2(e) (-inf for rows that do not count), the block lane of the
+      // row's target, and its p_t - 1.  pf_* is the next tile's, fetched early.
+      float cur_nl = kNegInf, pf_nl = kNegInf;
+      int cur_hit = -1, pf_hit = -1;
+      float cur_pm1 = 0.f, pf_pm1 = 0.f;
       const int use_pm1 = p.nll_in != nullptr;
       const uint32_t peer_p = mapa_shared(smem_u32(smem + A_P), 1);
       const uint32_t peer_pfull = mapa_shared(smem_u32(p_full), 1);
@@ -585,6 +614,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
         int blk, t0, t1;
         unit_range(p, u, blk, t0, t1);
+          const int nt_u = t1 - t0, rot = bwdk::unit_rot(u, nt_u, n_clusters);
         // DH: this thread's row data.
         float nl_row = kNegInf;
         long long trow = -1;
@@ -596,7 +626,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             nl_row = -p.lse[row] * kLog2e;
             if (use_pm1) pm1_row = expm1f(-p.nll_in[row]);
             if (tt >= 0 && tt < p.V) trow = tt;
-            else atomicOr(p.status, ST_EDATA);
+            else if (cq == 0) atomicOr(p.status, ST_EDATA);
           }
         }
         // FD: this thread's row data and its running sums over the unit.
@@ -612,7 +642,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (tt >= 0 && tt < p.V) {
               trow = tt;
               fd_flags |= FL_TVALID;
-            } else if (hc == 0) {
+            } else if (cq == 0) {
               atomicOr(p.status, ST_EDATA);
             }
           }
@@ -620,105 +650,94 @@ __global__ void __launch_bounds__(THREADS, 1)
         const long long vbase = static_cast<long long>(blk) * BM;
         // DW: row data of tile t is fetched into registers one tile ahead.
         auto fetch_dw = [&](int t) {
-#pragma unroll
-          for (int k = 0; k < 2; ++k) {
-            const int row = t * BT + hc * 64 + k * 32 + lane;
-            float nl = kNegInf;
-            int hl = -1;
-            float q1 = 0.f;
-            if (row < p.N) {
-              const uint8_t mk = p.mask ? p.mask[row] : uint8_t(1);
-              const long long tt = p.tgt[row];
-              const float l = p.lse[row];
-              if (mk) {
-                nl = -l * kLog2e;
-                if (tt < 0 || tt >= p.V) atomicOr(p.status, ST_EDATA);
-                else if (tt >= vbase && tt < vbase + BM) hl = static_cast<int>(tt - vbase);
-                if (hl >= 0 && use_pm1) q1 = expm1f(-p.nll_in[row]);
-              }
+          const int row = t * BT + cq * 32 + lane;
+          float nl = kNegInf;
+          int hl = -1;
+          float q1 = 0.f;
+          if (row < p.N) {
+            const uint8_t mk = p.mask ? p.mask[row] : uint8_t(1);
+            const long long tt = p.tgt[row];
+            const float l = p.lse[row];
+            if (mk) {
+              nl = -l * kLog2e;
+              if (tt < 0 || tt >= p.V) atomicOr(p.status, ST_EDATA);
+              else if (tt >= vbase && tt < vbase + BM) hl = static_cast<int>(tt - vbase);
+              if (hl >= 0 && use_pm1) q1 = expm1f(-p.nll_in[row]);
             }
-            pf_nl[k] = nl;
-            pf_hit[k] = hl;
-            pf_pm1[k] = q1;
           }
+          pf_nl = nl;
+          pf_hit = hl;
+          pf_pm1 = q1;
         };
-        if (MODE == DW && t0 < t1) fetch_dw(t0);
-        for (int t = t0; t < t1; ++t) {
-          bool hit_any[2] = {false, false};
+        if (MODE == DW && nt_u > 0) fetch_dw(bwdk::rot_tile(t0, nt_u, 0, rot));
+        for (int i = 0; i < nt_u; ++i) {
+            const int t = bwdk::rot_tile(t0, nt_u, i, rot);
+          bool hit_any = false;
           if (MODE == DW) {
-#pragma unroll
-            for (int k = 0; k < 2; ++k) {
-              cur_nl[k] = pf_nl[k];
-              cur_hit[k] = pf_hit[k];
-              cur_pm1[k] = pf_pm1[k];
-              hit_any[k] = __any_sync(0xffffffffu, pf_hit[k] >= 0);
-            }
-            if (t + 1 < t1) fetch_dw(t + 1);
+            cur_nl = pf_nl;
+            cur_hit = pf_hit;
+            cur_pm1 = pf_pm1;
+            hit_any = __any_sync(0xffffffffu, pf_hit >= 0);
+            if (i + 1 < nt_u) fetch_dw(bwdk::rot_tile(t0, nt_u, i + 1, rot));
           }
           ok = mbar_wait(acc_full + acc, aph, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
-          ok = mbar_wait<true>(p_empty + slot, sph ^ 1u, abort_flag, p.status);
-          if (!ok) break;
-          const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BT + hc * 64);
-          const uint32_t dst_row = peer_p + static_cast<uint32_t>(slot) * P_SLOT + static_cast<uint32_t>(hc) * CHUNK +
-                                   static_cast<uint32_t>(m) * 128u;
-          const uint32_t pfull_slot = peer_pfull + static_cast<uint32_t>(slot) * 8u;
-          // One 32-column chunk: gradient, pack, four swizzled 16-byte DSMEM stores.
-          auto do_chunk = [&](const uint32_t (&r)[32], int ch) {
-            uint32_t packed[16];
-            if (MODE == DH) {
-              const int cbase = t * BT + hc * 64 + ch * 32;  // vocab index
-              const int lim = min(32, p.V - cbase);
-              const long long relw = trow - cbase;
-              const int rel = (relw >= 0 && relw < 32) ? static_cast<int>(relw) : -1;
-              if (__any_sync(0xffffffffu, rel >= 0))
-                g_chunk_dh<true>(r, kc, -nl_row, rel, lim, use_pm1, pm1_row, packed);
-              else
-                g_chunk_dh<false>(r, kc, -nl_row, -1, lim, use_pm1, pm1_row, packed);
-            } else if (MODE == FD) {
-              const int cbase = t * BT + hc * 64 + ch * 32;
-              const int lim = min(32, p.V - cbase);
-              const long long relw = trow - cbase;
-              const int rel = (relw >= 0 && relw < 32) ? static_cast<int>(relw) : -1;
-              FdTarget tg{0.f, 0.f};
-              float cs;
-              if (__any_sync(0xffffffffu, rel >= 0))
-                cs = g_chunk_fd<true>(r, kc, nl_row, rel, lim, packed, tg);
-              else
-                cs = g_chunk_fd<false>(r, kc, nl_row, -1, lim, packed, tg);
-              s_acc += static_cast<double>(cs);
-              if (rel >= 0) {
-                rec_tg = tg;
-                fd_flags |= FL_HIT;
-              }
-            } else {
-              if (hit_any[ch])
-                g_chunk_dw<true>(r, kc, cur_nl[ch], cur_hit[ch], m, use_pm1, cur_pm1[ch], packed);
-              else
-                g_chunk_dw<false>(r, kc, cur_nl[ch], cur_hit[ch], m, use_pm1, cur_pm1[ch], packed);
-            }
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint32_t unit = static_cast<uint32_t>(ch * 4 + v);
-              const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
-              st_async_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3], pfull_slot);
-            }
-          };
-          uint32_t ra[32], rc[32];
-          tmem_ld32(tb, ra);
+          uint32_t r[32];
+          tmem_ld32(tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(acc * BT + cq * 32), r);
           tmem_ld_wait();
-          reg_fence32(ra);
-          tmem_ld32(tb + 32, rc);
-          do_chunk(ra, 0);
-          tmem_ld_wait();
-          reg_fence32(rc);
-          do_chunk(rc, 1);
+          reg_fence32(r);
+          // The chunk is in registers: release the accumulator buffer.
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(acc_empty + acc);
           acc ^= 1;
           if (acc == 0) aph ^= 1u;
+          // Gradient (or FD tile) of the chunk, packed to bf16.
+          uint32_t packed[16];
+          const int cbase = t * BT + cq * 32;  // first column of the chunk (vocab index in DH, FD)
+          if (MODE == DH) {
+            const int lim = min(32, p.V - cbase);
+            const long long relw = trow - cbase;
+            const int rel = (relw >= 0 && relw < 32) ? static_cast<int>(relw) : -1;
+            if (__any_sync(0xffffffffu, rel >= 0))
+              g_chunk_dh<true>(r, kc, -nl_row, rel, lim, use_pm1, pm1_row, packed);
+            else
+              g_chunk_dh<false>(r, kc, -nl_row, -1, lim, use_pm1, pm1_row, packed);
+          } else if (MODE == FD) {
+            const int lim = min(32, p.V - cbase);
+            const long long relw = trow - cbase;
+            const int rel = (relw >= 0 && relw < 32) ? static_cast<int>(relw) : -1;
+            FdTarget tg{0.f, 0.f};
+            float cs;
+            if (__any_sync(0xffffffffu, rel >= 0))
+              cs = g_chunk_fd<true>(r, kc, nl_row, rel, lim, packed, tg);
+            else
+              cs = g_chunk_fd<false>(r, kc, nl_row, -1, lim, packed, tg);
+            s_acc += static_cast<double>(cs);
+            if (rel >= 0) {
+              rec_tg = tg;
+              fd_flags |= FL_HIT;
+            }
+          } else {
+            if (hit_any)
+              g_chunk_dw<true>(r, kc, cur_nl, cur_hit, m, use_pm1, cur_pm1, packed);
+            else
+              g_chunk_dw<false>(r, kc, cur_nl, cur_hit, m, use_pm1, cur_pm1, packed);
+          }
+          // Four swizzled 16-byte DSMEM stores into the P slot, once the A
+          // CTA's MMA no longer reads it.
+          ok = mbar_wait<true>(p_empty + slot, sph ^ 1u, abort_flag, p.status);
+          if (!ok) break;
+          const uint32_t dst_row = peer_p + static_cast<uint32_t>(slot) * P_SLOT +
+                                   static_cast<uint32_t>(cq >> 1) * CHUNK + static_cast<uint32_t>(m) * 128u;
+          const uint32_t pfull_slot = peer_pfull + static_cast<uint32_t>(slot) * 8u;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t unit = static_cast<uint32_t>((cq & 1) * 4 + v);
+            const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
+            st_async_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3], pfull_slot);
+          }
           slot ^= 1;
           if (slot == 0) sph ^= 1u;
         }
@@ -729,7 +748,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = mbar_wait<true>(rd_empty, static_cast<uint32_t>(fd_units - 1) & 1u, abort_flag, p.status);
             if (!ok) break;
           }
-          uint4* rec = reinterpret_cast<uint4*>(smem + Z_REC + (static_cast<uint32_t>(hc) * BM + m) * REC_BYTES);
+          uint4* rec = reinterpret_cast<uint4*>(smem + Z_REC + (static_cast<uint32_t>(cq) * BM + m) * REC_BYTES);
           const unsigned long long sb = static_cast<unsigned long long>(__double_as_longlong(s_acc));
           rec[0] = make_uint4(static_cast<uint32_t>(sb), static_cast<uint32_t>(sb >> 32), __float_as_uint(rec_tg.e),
                               __float_as_uint(rec_tg.om));
@@ -752,7 +771,9 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
-          for (int t = t0; t < t1 && ok; ++t) {
+          const int nt_u = t1 - t0, rot = bwdk::unit_rot(u, nt_u, n_clusters);
+          for (int i = 0; i < nt_u && ok; ++i) {
+            const int t = bwdk::rot_tile(t0, nt_u, i, rot);
             for (int sl = 0; sl < NSLAB; ++sl) {
               ok = mbar_wait(ay_empty + rs, rph ^ 1u, abort_flag, p.status);
               if (!ok) break;
@@ -783,6 +804,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         // The accumulator's d columns in two N halves of nh0 and nh1 chunks.
         const int nh0 = (p.KC + 1) / 2;
         const int nh1 = p.KC - nh0;
+        const uint32_t idesc_h0 = idesc_bf16_f32(128, 64 * nh0, false, true);
+        const uint32_t idesc_h1 = idesc_bf16_f32(128, 64 * (nh1 > 0 ? nh1 : 1), false, true);
         // Each P slot completes when all its bytes (st.async from the Z CTA)
         // have landed: arm both slots for their first use.
         mbar_expect_tx(p_full + 0, P_SLOT);
@@ -790,41 +813,42 @@ __global__ void __launch_bounds__(THREADS, 1)
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
+          const int nt_u = t1 - t0, rot = bwdk::unit_rot(u, nt_u, n_clusters);
           ok = mbar_wait(acc_empty, dph ^ 1u, abort_flag, p.status);  // accumulator drained
           dph ^= 1u;
           if (!ok) break;
           tc_fence_after();
-          for (int t = t0; t < t1 && ok; ++t) {
+          for (int i = 0; i < nt_u && ok; ++i) {
+            const int t = bwdk::rot_tile(t0, nt_u, i, rot);
             ok = mbar_wait<true>(p_full + slot, sph, abort_flag, p.status);
             if (!ok) break;
             mbar_expect_tx(p_full + slot, P_SLOT);  // arm the slot's next use
             fence_proxy_async_smem();
             tc_fence_after();
-            const uint32_t pa = smem_u32(smem + A_P + slot * P_SLOT);
-            for (int ks = 0; ks < BT / 16 && ok; ++ks) {
-              if (ks % (SLAB_ROWS / 16) == 0) {
-                ok = mbar_wait(ay_full + rs, rph, abort_flag, p.status);
-                if (!ok) break;
-                tc_fence_after();
+            const uint64_t pdesc = sdesc_sw128(smem_u32(smem + A_P + slot * P_SLOT), 16, 1024);
+            for (int sl = 0; sl < NSLAB && ok; ++sl) {
+              ok = mbar_wait(ay_full + rs, rph, abort_flag, p.status);
+              if (!ok) break;
+              tc_fence_after();
+              // The slab's two K steps of 16 rows (2 KB apart); P: chunk sl / 2,
+              // K columns 32 (sl % 2) + 16 kk (32 bytes per step).  MN-major B:
+              // N = 64 nh columns of d in chunks 4 KB apart inside the slab.
+              const uint64_t bd0 = sdesc_sw128(smem_u32(smem + A_Y + rs * p.KC * SLAB_CHUNK), SLAB_CHUNK, 1024);
+              const uint64_t ad0 = pdesc + static_cast<uint64_t>(((sl >> 1) * CHUNK + (sl & 1) * 64) >> 4);
+#pragma unroll
+              for (int kk = 0; kk < SLAB_ROWS / 16; ++kk) {
+                const uint32_t accf = (i != 0 || sl != 0 || kk != 0) ? 1u : 0u;
+                const uint64_t ad = ad0 + static_cast<uint64_t>((kk * 32) >> 4);
+                const uint64_t bd = bd0 + static_cast<uint64_t>((kk * 2048) >> 4);
+                umma_bf16(tmem_base, ad, bd, idesc_h0, accf);
+                if (nh1 > 0)
+                  umma_bf16(tmem_base + static_cast<uint32_t>(64 * nh0), ad,
+                            bd + static_cast<uint64_t>((nh0 * SLAB_CHUNK) >> 4), idesc_h1, accf);
               }
-              const uint64_t ad = sdesc_sw128(pa + (ks >> 2) * CHUNK + (ks & 3) * 32, 16, 1024);
-              for (int half = 0; half < 2; ++half) {
-                const int nh = half == 0 ? nh0 : nh1;
-                if (nh == 0) continue;
-                const uint32_t idesc = idesc_bf16_f32(128, 64 * nh, false, true);
-                // MN-major B: N = 64 nh columns of d in chunks 4 KB apart inside
-                // the slab; K-step ks covers rows 16 (ks % 2) .. +15 of its slab.
-                const uint32_t yb = smem_u32(smem + A_Y + rs * p.KC * SLAB_CHUNK + half * nh0 * SLAB_CHUNK);
-                const uint64_t bd = sdesc_sw128(yb + (ks % (SLAB_ROWS / 16)) * 2048, SLAB_CHUNK, 1024);
-                umma_bf16(tmem_base + static_cast<uint32_t>(half * 64 * nh0), ad, bd, idesc,
-                          (t != t0 || ks != 0) ? 1u : 0u);
-              }
-              if (ks % (SLAB_ROWS / 16) == SLAB_ROWS / 16 - 1) {
-                umma_commit(ay_empty + rs);
-                if (++rs == ASLOTS) {
-                  rs = 0;
-                  rph ^= 1u;
-                }
+              umma_commit(ay_empty + rs);
+              if (++rs == ASLOTS) {
+                rs = 0;
+                rph ^= 1u;
               }
             }
             if (!ok) break;
@@ -841,36 +865,46 @@ __global__ void __launch_bounds__(THREADS, 1)
       }
     } else {
       // ---- A drain: accumulator -> dh / dW ----
+      // Warp w drains TMEM lanes 32 (w % 4) .. +31 and the 32-column chunks
+      // w / 4, w / 4 + 4, ... of the d columns.
       const int q = warp & 3;
-      const int hc = warp >> 2;       // column half of the accumulator
+      const int part = warp >> 2;
       const int m = q * 32 + lane;
+      constexpr int NPART = EPI_WARPS / 4;
       uint32_t fph = 0, rph = 0;
       const uint32_t z_rec = mapa_shared(smem_u32(smem + Z_REC), 0);
       const uint32_t z_rd_empty = mapa_shared(smem_u32(rd_empty), 0);
       for (int u = cluster; u < p.n_units; u += n_clusters) {
         int blk, t0, t1;
         unit_range(p, u, blk, t0, t1);
+          const int nt_u = t1 - t0, rot = bwdk::unit_rot(u, nt_u, n_clusters);
         const int row = blk * BM + m;  // DH, FD: token row; DW: vocab row
-        const int ncols_half = p.d / 2;
+        const int nch = p.d / 32;      // 32-column chunks of the accumulator
         // FD: the row's scale alpha, target term beta W_t, and the forward's
-        // outputs, from the two Z epilogue records of the row.
+        // outputs, from the Z epilogue's records of the row (one per column
+        // group, in group order).
         float alpha = 0.f, beta = 0.f;
         long long trow = -1;
         if (MODE == FD) {
           if (!mbar_wait<true>(rd_full, rph, abort_flag, p.status)) break;
           rph ^= 1u;
-          const uint32_t ra = z_rec + static_cast<uint32_t>(m) * REC_BYTES;
-          const uint32_t rb = z_rec + static_cast<uint32_t>(BM + m) * REC_BYTES;
-          const uint4 a0 = ld_cluster_v4(ra), a1 = ld_cluster_v4(ra + 16);
-          const uint4 b0 = ld_cluster_v4(rb), b1 = ld_cluster_v4(rb + 16);
+          double S_other = 0.0;  // the row's sum of e^s over its non-target columns
+          int flags = 0;
+          uint32_t tsel = 0;
+          double et = 0.0, om = 0.0;
+#pragma unroll
+          for (int g = 0; g < NPART; ++g) {
+            const uint32_t ra = z_rec + static_cast<uint32_t>(g * BM + m) * REC_BYTES;
+            const uint4 a0 = ld_cluster_v4(ra), a1 = ld_cluster_v4(ra + 16);
+            S_other += __hiloint2double(static_cast<int>(a0.y), static_cast<int>(a0.x));
+            flags |= static_cast<int>(a1.y);
+            tsel = a1.x;
+            if (a1.y & FL_HIT) {
+              et = static_cast<double>(__uint_as_float(a0.z));
+              om = static_cast<double>(__uint_as_float(a0.w));
+            }
+          }
           mbar_arrive_cluster(z_rd_empty);
-          // S_other: the row's sum of e^s over its non-target columns.
-          const double S_other = __hiloint2double(static_cast<int>(a0.y), static_cast<int>(a0.x)) +
-                                 __hiloint2double(static_cast<int>(b0.y), static_cast<int>(b0.x));
-          const int flags = static_cast<int>(a1.y | b1.y);
-          const bool in_b = (b1.y & FL_HIT) != 0;
-          const double et = static_cast<double>(__uint_as_float(in_b ? b0.z : a0.z));
-          const double om = static_cast<double>(__uint_as_float(in_b ? b0.w : a0.w));
           const bool tv = (flags & FL_TVALID) != 0;
           const double S = tv ? S_other + et : S_other;
           if (flags & FL_LIVE) {
@@ -878,10 +912,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             if (tv) {
               // w (p_t - 1)(1 - tanh_t^2), p_t - 1 = -S_other / S (no cancellation).
               beta = static_cast<float>(-static_cast<double>(p.w) * (S_other / S) * om);
-              trow = static_cast<long long>(static_cast<int>(a1.x));
+              trow = static_cast<long long>(static_cast<int>(tsel));
             }
           }
-          if (hc == 0 && row < p.N) {
+          if (part == 0 && row < p.N) {
             float nll = 0.f, lse = 0.f;
             if (flags & FL_LIVE) {
               lse = static_cast<float>(log(S));
@@ -897,24 +931,24 @@ __global__ void __launch_bounds__(THREADS, 1)
 #pragma unroll
           for (int v = 0; v < 4; ++v) dst[v] = make_uint4(0u, 0u, 0u, 0u);
           if (trow >= 0) {
-            const uint4* src = reinterpret_cast<const uint4*>(p.W + trow * p.d + hc * ncols_half + ch * 32);
+            const uint4* src = reinterpret_cast<const uint4*>(p.W + trow * p.d + ch * 32);
 #pragma unroll
             for (int v = 0; v < 4; ++v) dst[v] = __ldg(src + v);
           }
         };
-        if (MODE == FD) load_w(0, wcur);
+        if (MODE == FD && part < nch) load_w(part, wcur);
         if (!mbar_wait(acc_full, fph, abort_flag, p.status)) break;
         fph ^= 1u;
         tc_fence_after();
-        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(hc * ncols_half);
+        const uint32_t tb = tmem_base + (static_cast<uint32_t>(q * 32) << 16);
 #pragma unroll 1
-        for (int ch = 0; ch < ncols_half / 32; ++ch) {
-          if (MODE == FD && ch + 1 < ncols_half / 32) load_w(ch + 1, wnxt);
+        for (int ch = part; ch < nch; ch += NPART) {
+          if (MODE == FD && ch + NPART < nch) load_w(ch + NPART, wnxt);
           uint32_t r[32];
           tmem_ld32(tb + ch * 32, r);
           tmem_ld_wait();
           reg_fence32(r);
-          const int col = hc * ncols_half + ch * 32;
+          const int col = ch * 32;
           if (MODE == FD) {
             if (row < p.N) {
               const uint32_t* wb = reinterpret_cast<const uint32_t*>(wcur);

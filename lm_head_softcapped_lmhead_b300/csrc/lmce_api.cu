@@ -8,6 +8,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <algorithm>
 #include <atomic>
 #include <mutex>
 #include <string>
@@ -225,6 +226,18 @@ int check_common(const void* h, int64_t ldh, const void* W, int64_t N, int64_t V
   return LMCE_OK;
 }
 
+int bwd_launch(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+               const int64_t* tgt, const uint8_t* mask, float c, const float* lse, const float* nll, float w,
+               lmce_bf16* dh, float* dW, int accumulate, unsigned* status, void* scratch, int sms, cudaStream_t s) {
+  return lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, mask, c, lse, nll, w, dh, dW, accumulate, status, scratch, sms,
+                            s);
+}
+int fd_launch(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+              const int64_t* tgt, const uint8_t* mask, float c, float grad_scale, float* nll, float* lse,
+              lmce_bf16* dh, unsigned* status, int sms, cudaStream_t s) {
+  return lmce::bwdk::launch_fd(h, ldh, W, N, V, d, tgt, mask, c, grad_scale, nll, lse, dh, status, sms, s);
+}
+
 int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
              const int64_t* tgt, const uint8_t* mask, float c, float* nll, float* lse, void* ws, size_t ws_bytes,
              void* stream, unsigned extra_flags) {
@@ -364,9 +377,8 @@ int lmhead_ce_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N
   DevInfo di;
   if (int rc = dev_info(&di); rc) return rc;
   char* w = static_cast<char*>(ws);
-  return lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, dW,
-                            accumulate_dW, reinterpret_cast<unsigned*>(w + L.status), w + L.bwd, di.sms,
-                            static_cast<cudaStream_t>(stream));
+  return bwd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, dW, accumulate_dW,
+                    reinterpret_cast<unsigned*>(w + L.status), w + L.bwd, di.sms, static_cast<cudaStream_t>(stream));
 }
 
 int lmhead_ce_fwd_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
@@ -387,23 +399,22 @@ int lmhead_ce_fwd_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dh && softcap <= kFusedSoftcapMax) {
     // Forward and dh in one pass over the vocabulary.
-    if (int rc = lmce::bwdk::launch_fd(h, ldh, W, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, status,
-                                       di.sms, s);
+    if (int rc = fd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, status, di.sms, s);
         rc)
       return rc;
   } else {
     if (int rc = fwd_impl(h, ldh, W, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, 0u); rc)
       return rc;
     if (dh) {
-      if (int rc = lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh,
-                                      nullptr, 0, status, w + L.bwd, di.sms, s);
+      if (int rc = bwd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, nullptr, 0,
+                              status, w + L.bwd, di.sms, s);
           rc)
         return rc;
     }
   }
   if (dW) {
-    if (int rc = lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, nullptr, dW,
-                                    accumulate_dW, status, w + L.bwd, di.sms, s);
+    if (int rc = bwd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, nullptr, dW,
+                            accumulate_dW, status, w + L.bwd, di.sms, s);
         rc)
       return rc;
   }
