@@ -115,7 +115,7 @@ struct Params {
   float* nll;              // FD outputs [N]
   float* lse_out;
   float zlim2;
-  float q[kTanhTerms];  // -C_i / c^(2i+1)
+  float q[kTanhTerms2];  // -C_i / c^(2i+1), degree-2 fit
   __nv_bfloat16* dh;    // DH output [N, ldh]
   long long ldh;
   float* dW;            // DW output [V, d]
@@ -132,7 +132,7 @@ struct Params {
 //   -G = (p - [j == t]) * w.
 // The drain multiplies the accumulator by -grad_scale.
 struct EpiConst {
-  float2 q[kTanhTerms];  // -C_i / c^(2i+1): z * Q(z^2) = -tanh(z/c)
+  float2 q[kTanhTerms2];  // -C_i / c^(2i+1): z * Q(z^2) = -tanh(z/c) (degree-2 fit)
   float2 ncl2e;   // -c log2(e)
   float2 m1;      // -1
   float zlim2;    // (kTanhXmax c)^2
@@ -205,13 +205,13 @@ template <bool kHit>
 __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiConst& k, float lse2, int rel, int lim,
                                            int use_pm1, float pm1, uint32_t (&out)[16]) {
   const float2 nl = make_float2(-lse2, -lse2);
-  float2 su = make_float2(0.f, 0.f);
+  float mu = 0.f;  // max z^2 of the chunk (range check of the polynomial)
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
     const float2 u = __fmul2_rn(z, z);
-    su = __fadd2_rn(su, u);
-    const float2 nth = poly_z2(z, u, k.q);
+    mu = fmax3(mu, u.x, u.y);
+    const float2 nth = poly2_z2(z, u, k.q);
     const float2 a = __ffma2_rn(nth, k.ncl2e, nl);
     float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
     if (kHit) {
@@ -225,7 +225,7 @@ __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiCon
     }
     out[j] = pack_bf16x2(g.x, g.y);
   }
-  if (__any_sync(0xffffffffu, !(su.x + su.y <= k.zlim2))) {
+  if (__any_sync(0xffffffffu, !(mu <= k.zlim2))) {
     Chunk32 c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) c.v[j] = r[j];
@@ -242,13 +242,13 @@ __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiCon
 template <bool kHit>
 __device__ __forceinline__ void g_chunk_dw(const uint32_t (&r)[32], const EpiConst& k, float nl_col, int hit_col,
                                            int my_lane, int use_pm1, float pm1_col, uint32_t (&out)[16]) {
-  float2 su = make_float2(0.f, 0.f);
+  float mu = 0.f;  // max z^2 of the chunk (range check of the polynomial)
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
     const float2 u = __fmul2_rn(z, z);
-    su = __fadd2_rn(su, u);
-    const float2 nth = poly_z2(z, u, k.q);
+    mu = fmax3(mu, u.x, u.y);
+    const float2 nth = poly2_z2(z, u, k.q);
     const float2 nl = make_float2(__shfl_sync(0xffffffffu, nl_col, 2 * j), __shfl_sync(0xffffffffu, nl_col, 2 * j + 1));
     const float2 a = __ffma2_rn(nth, k.ncl2e, nl);
     float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
@@ -261,7 +261,7 @@ __device__ __forceinline__ void g_chunk_dw(const uint32_t (&r)[32], const EpiCon
     const float2 g = __fmul2_rn(pp, __ffma2_rn(nth, nth, k.m1));
     out[j] = pack_bf16x2(g.x, g.y);
   }
-  if (__any_sync(0xffffffffu, !(su.x + su.y <= k.zlim2))) {
+  if (__any_sync(0xffffffffu, !(mu <= k.zlim2))) {
     Chunk32 c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) c.v[j] = r[j];
@@ -314,14 +314,14 @@ template <bool kHit>
 __device__ __forceinline__ float g_chunk_fd(const uint32_t (&r)[32], const EpiConst& k, float nl, int rel, int lim,
                                             uint32_t (&out)[16], FdTarget& tg) {
   const float2 nl2 = make_float2(nl, nl);
-  float2 su = make_float2(0.f, 0.f);
+  float mu = 0.f;  // max z^2 of the chunk (range check of the polynomial)
   float2 se = make_float2(0.f, 0.f);
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
     const float2 u = __fmul2_rn(z, z);
-    su = __fadd2_rn(su, u);
-    const float2 nth = poly_z2(z, u, k.q);
+    mu = fmax3(mu, u.x, u.y);
+    const float2 nth = poly2_z2(z, u, k.q);
     const float2 a = __ffma2_rn(nth, k.ncl2e, nl2);
     float2 e = make_float2(ex2_approx(a.x), ex2_approx(a.y));
     if (lim < 32) {
@@ -344,7 +344,7 @@ __device__ __forceinline__ float g_chunk_fd(const uint32_t (&r)[32], const EpiCo
     out[j] = pack_bf16x2(g.x, g.y);
   }
   float sum = se.x + se.y;
-  if (__any_sync(0xffffffffu, !(su.x + su.y <= k.zlim2))) {
+  if (__any_sync(0xffffffffu, !(mu <= k.zlim2))) {
     Chunk32 c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) c.v[j] = r[j];
@@ -457,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        uint32_t pend = 0, pend_ph[YSTAGES] = {0, 0, 0};
+        uint32_t pend = 0, pend_ph[YSTAGES] = {};
         const int nst = (p.KC + ZSC - 1) / ZSC;
         auto put = [&](const CUtensorMap* m, int row0, int s4) -> bool {
           if (!mbar_wait(zy_empty + stage, phase ^ 1u, abort_flag, p.status)) return false;
@@ -590,7 +590,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int m = q * 32 + lane;  // row of the P tile (= TMEM lane)
       EpiConst kc;
 #pragma unroll
-      for (int i = 0; i < kTanhTerms; ++i) kc.q[i] = make_float2(p.q[i], p.q[i]);
+      for (int i = 0; i < kTanhTerms2; ++i) kc.q[i] = make_float2(p.q[i], p.q[i]);
       kc.ncl2e = make_float2(-p.cl2e, -p.cl2e);
       kc.m1 = make_float2(-1.0f, -1.0f);
       kc.zlim2 = p.zlim2;
@@ -1161,7 +1161,7 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
   p.cl2e = c * kLog2e;
   p.w = -w;  // the P tiles hold -G
   p.zlim2 = (kTanhXmax * c) * (kTanhXmax * c);
-  scaled_tanh_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
+  scaled_tanh2_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
   p.status = status;
   if (dh) {
     Params q = p;
@@ -1225,7 +1225,7 @@ inline int launch_fd(const uint16_t* h, long long ldh, const uint16_t* W, long l
   p.cl2e = c * kLog2e;
   p.w = grad_scale;
   p.zlim2 = (kTanhXmax * c) * (kTanhXmax * c);
-  scaled_tanh_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
+  scaled_tanh2_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
   p.status = status;
   p.W = reinterpret_cast<const __nv_bfloat16*>(W);
   p.nll = nll;
