@@ -215,36 +215,48 @@ def run_ours(args, rank, world, local_rank):
     if args.profile:
         return None
     # ---- end to end through the public API with host buffers ----
-    h_in = torch.empty_like(h)
-    t_in = torch.empty_like(tgt)
-    b_in = torch.empty_like(nbytes)
+    # Every step copies its inputs (h, targets, bytes) from pinned host memory
+    # and reads the bpb accumulator back.  As a training loop that prefetches
+    # its next batch would, the copy of step k+1 runs on a copy stream while
+    # step k computes (two device input buffers); the timed region spans the
+    # first copy to the last read-back.
+    copy_stream = torch.cuda.Stream(dev)
+    bufs = [(torch.empty_like(h), torch.empty_like(tgt), torch.empty_like(nbytes)) for _ in range(2)]
     acc_host = torch.empty(3, dtype=torch.float64).pin_memory()
     h2d = h_host.numel() * 2 + t_host.numel() * 8 + b_host.numel() * 4
     d2h = acc_host.numel() * 8
 
-    def e2e_step():
-        h_in.copy_(h_host, non_blocking=True)
-        t_in.copy_(t_host, non_blocking=True)
-        b_in.copy_(b_host, non_blocking=True)
-        lm.lmhead_ce_fwd_bwd(h_in, W, t_in, SOFTCAP, grad_scale, nll, lse, dh=dh, dW=dW, accumulate_dW=True,
-                             ws=ws, stream=stream)
-        lm.bpb_reduce(nll, b_in, acc, ws=ws, stream=stream)
-        acc_host.copy_(acc, non_blocking=True)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize()
-    e_ms = []
-    for _ in range(max(3, args.steps // 2)):
-        flush.zero_()
+    def run_e2e(n):
+        copied = [torch.cuda.Event() for _ in range(n)]
+        done = [torch.cuda.Event() for _ in range(n)]
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        e2e_step()
+        torch.cuda.synchronize()
+        e0.record(copy_stream)
+        for k in range(n):
+            hb, tb, bb = bufs[k % 2]
+            if k >= 2:
+                copy_stream.wait_event(done[k - 2])
+            with torch.cuda.stream(copy_stream):
+                hb.copy_(h_host, non_blocking=True)
+                tb.copy_(t_host, non_blocking=True)
+                bb.copy_(b_host, non_blocking=True)
+            copied[k].record(copy_stream)
+            stream.wait_event(copied[k])
+            lm.lmhead_ce_fwd_bwd(hb, W, tb, SOFTCAP, grad_scale, nll, lse, dh=dh, dW=dW, accumulate_dW=True,
+                                 ws=ws, stream=stream)
+            lm.bpb_reduce(nll, bb, acc, ws=ws, stream=stream)
+            with torch.cuda.stream(stream):
+                acc_host.copy_(acc, non_blocking=True)
+            done[k].record(stream)
         e1.record(stream)
         e1.synchronize()
-        e_ms.append(e0.elapsed_time(e1))
-    e2e_total_ms = sum(e_ms)
+        return e0.elapsed_time(e1)
+
+    run_e2e(2)
+    n_e2e = max(3, args.steps)
+    e2e_total_ms = run_e2e(n_e2e)
+    e_ms = [e2e_total_ms / n_e2e] * n_e2e
 
     # ---- max over ranks ----
     if world > 1:
@@ -284,7 +296,9 @@ def run_ours(args, rank, world, local_rank):
         "mfu_6NVd": model_flops / (ms_step / 1e3) / 1e12 / peak_burst,
         "tensor_frac_exec_8NVd": exec_flops / (ms_step / 1e3) / 1e12 / peak_burst,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                "ms_per_step": e2e_total_ms / len(e_ms)},
+                "ms_per_step": e2e_total_ms / len(e_ms),
+                "pipelining": "step k+1's H2D copy overlaps step k's compute (copy stream, 2 input buffers); "
+                              "no L2 flush: the per-step working set (h, dh, W, dW: 152 MB) exceeds L2"},
         "gpu_launches": launches,
         "clocks": dict(clocks, window="sampled every 100 ms over the warm-up (>= 1 s) and the timed steps"),
         "wall_s_timed": t_wall,
