@@ -11,16 +11,19 @@
 // tile and the accumulator cannot share one SM.  Each stationary block is
 // therefore handled by a cluster of two CTAs:
 //  * rank 0, the Z CTA: keeps the stationary operand X (128 x d bf16) in
-//    shared memory, streams the other operand Y in 128-row tiles, computes
-//    z = X Y^T (tcgen05, M=128 N=128, double-buffered in TMEM), and turns each
-//    z tile into the bf16 tile P = G (DH) or G^T (DW) in the epilogue; P is
-//    stored straight into the peer CTA's shared memory (DSMEM), in the
+//    TMEM (copied there from the ring with tcgen05.cp), streams the other
+//    operand Y in 128-row tiles through a ring of 64 KB TMA loads, computes
+//    z = X Y^T (tcgen05, A from TMEM, M=128 N=128, double-buffered in TMEM),
+//    and its 16 epilogue warps (one 32-column chunk each per tile) turn each
+//    z tile into the bf16 tile P = -G (DH) or -G^T (DW); P is stored
+//    straight into the peer CTA's shared memory (DSMEM, st.async), in the
 //    128B-swizzled K-major layout the MMA reads.
-//  * rank 1, the A CTA: loads the same Y tile (as the MN-major B operand) and
-//    accumulates acc (128 x d fp32, all 512 TMEM columns) += P Y with
-//    tcgen05 M=128 N=256; after the last tile it scales by w and writes dh
-//    (bf16) or dW (fp32, added or stored; or a partial for a later ordered
-//    reduction when the rows are split across several clusters).
+//  * rank 1, the A CTA: loads the same Y tile in 32-row slabs (as the
+//    MN-major B operand) and accumulates acc (128 x d fp32, all 512 TMEM
+//    columns) += P Y with tcgen05 M=128 N=d/2; after the last tile its 16
+//    drain warps scale by w and write dh (bf16) or dW (fp32, added or
+//    stored; or a partial for a later ordered reduction when the rows are
+//    split across several clusters).
 // The logits and G never leave the two SMs.  Every wait is bounded.
 //
 // FD mode computes the forward (nll, lse) and dh in the same pass over the
