@@ -10,6 +10,7 @@ in HBM when the timed region starts; L2 is flushed (a 256 MB write) between
 steps.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py --table     # every workload's call throughput, markdown (one GPU)
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
 on its own GPU (weak scaling, no data-path collective); the time is the max
@@ -49,7 +50,16 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--profile", action="store_true",
                     help="for profiler captures: exactly W warm-up steps, no clock sampling, no e2e leg")
-    return ap.parse_args()
+    ap.add_argument("--profile-step", choices=["train", "fwd"], default="train",
+                    help="with --profile: the step to run; fwd = the evaluation forward (lmhead_ce_fwd + "
+                         "bpb_reduce) on the same batch")
+    ap.add_argument("--table", action="store_true",
+                    help="instead of the JSON line: a markdown table of every workload's call throughput "
+                         "(one GPU) beside the oracle's on a sample (host cores)")
+    args = ap.parse_args()
+    if args.profile_step != "train" and not args.profile:
+        ap.error("--profile-step needs --profile")
+    return args
 
 
 # ---------------------------------------------------------------- helpers
@@ -155,6 +165,13 @@ def run_ours(args, rank, world, local_rank):
         ev = events or [None] * 4
         if ev[0] is not None:
             ev[0].record(stream)
+        if args.profile_step == "fwd":
+            lm.lmhead_ce_fwd(h, W, tgt, SOFTCAP, nll, lse, ws=ws, stream=stream)
+            lm.bpb_reduce(nll, nbytes, acc, ws=ws, stream=stream)
+            for e in ev[1:]:
+                if e is not None:
+                    e.record(stream)
+            return
         lm.lmhead_ce_fwd_bwd(h, W, tgt, SOFTCAP, grad_scale, nll, lse, dh=dh, ws=ws, stream=stream)
         if ev[1] is not None:
             ev[1].record(stream)
@@ -310,14 +327,27 @@ KERNEL_SOURCES = {"fwd": "fwd_kernel.cuh", "fwd_dh": "bwd_kernel.cuh", "bwd_dh":
                   "bwd_dW": "bwd_kernel.cuh"}
 
 
-def kernel_sources_sha(kernel: str) -> str:
-    """sha256 (first 16 hex digits) of the sources that define a kernel."""
+def code_only(src: str) -> str:
+    """C++ source without its comments and blank-line or trailing-space
+    differences, so that an edit of the comments keeps the hash."""
+    import re
+    src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(ln.rstrip() for ln in src.splitlines() if ln.strip())
+
+
+def kernel_sources_sha(kernel: str, read=None) -> str:
+    """sha256 (first 16 hex digits) of the code (comments dropped) of the
+    sources that define a kernel."""
     import hashlib
     csrc = os.path.join(ROOT, "lm_head_softcapped_lmhead_b300", "csrc")
+    if read is None:
+        def read(name):
+            with open(os.path.join(csrc, name)) as fh:
+                return fh.read()
     h = hashlib.sha256()
     for f in (KERNEL_SOURCES[kernel], "ptx.cuh", "softcap_math.cuh"):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            h.update(fh.read())
+        h.update(code_only(read(f)).encode())
     return h.hexdigest()[:16]
 
 
@@ -393,8 +423,118 @@ def run_reference(args, rank, world):
     }
 
 
+# ---------------------------------------------------------------- per-workload table
+def run_table(args):
+    """Every workload once through the public API on one GPU (inputs resident,
+    L2 flushed between calls, CUDA events), and the oracle on a sample of the
+    same inputs on the host cores.  Prints a markdown table."""
+    import torch
+    import lm_head_softcapped_lmhead_b300 as lm
+    import oracle
+    import synth_inputs as si
+
+    oracle.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    peak = measured_peaks()[0]
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    reps = max(args.steps, 3)
+
+    def bf(bits):
+        return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
+
+    def gpu_ms(fn):
+        for _ in range(max(args.warmup, 3)):
+            fn()
+        torch.cuda.synchronize()
+        total = 0.0
+        for _ in range(reps):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            total += e0.elapsed_time(e1)
+        return total / reps
+
+    def oracle_rate(h_bits, W_bits, tgt, nbytes, kind, target_s=4.0):
+        W = oracle.widen_bf16(W_bits)
+
+        def run(S):
+            h = oracle.widen_bf16(h_bits[:S])
+            t0 = time.perf_counter()
+            nll, lse = oracle.fwd(h, W, tgt[:S], SOFTCAP)
+            oracle.bpb(nll, nbytes[:S])
+            if kind != "fwd":
+                oracle.bwd(h, W, tgt[:S], SOFTCAP, lse, 1.0 / S, want_dW=(kind == "fwd_bwd"))
+            return time.perf_counter() - t0
+
+        tp = run(8)
+        S = int(max(8, min(4096, 8 * target_s / max(tp, 1e-3))))
+        return S / run(S), S
+
+    rows = []
+    acc = lm.bpb_acc(dev)
+    for cfg in (1, 2, 3, 4, 5):
+        # The sliding-window stream is scored in calls of 512 windows (1,048,576 rows, 32,768 scored).
+        inp = si.make_inputs(cfg, N=512 * si.WINDOW if cfg == 4 else None)
+        N, V, d = inp["N"], inp["V"], inp["d"]
+        h, tgt = bf(inp["h"]), torch.from_numpy(inp["tgt"]).to(dev)
+        nbytes = torch.from_numpy(inp["nbytes"]).to(dev)
+        mask = None if inp["mask"] is None else torch.from_numpy(inp["mask"]).to(dev)
+        M = N if inp["mask"] is None else int(inp["mask"].sum())
+        flags = (lm.LMCE_WS_MASKED if mask is not None else 0) | (lm.LMCE_WS_INT4 if cfg == 5 else 0)
+        ws = lm.workspace(N, V, d, flags, device=dev)
+        nll, lse = torch.empty(N, device=dev), torch.empty(N, device=dev)
+        if cfg in (1, 4):
+            W = bf(inp["W"])
+            ms = gpu_ms(lambda: (lm.lmhead_ce_fwd(h, W, tgt, SOFTCAP, nll, lse, row_mask=mask, ws=ws, stream=stream),
+                                 lm.bpb_reduce(nll, nbytes, acc, row_mask=mask, ws=ws, stream=stream)))
+            kind, exec_f, model_f = "fwd", 2, 2
+            what = "fwd + bpb" if cfg == 1 else f"fwd + bpb, calls of {M} scored rows in {N} (row mask)"
+        elif cfg in (2, 3):
+            W = bf(inp["W"])
+            dh, dW = torch.empty_like(h), torch.zeros((V, d), device=dev)
+            ms = gpu_ms(lambda: (lm.lmhead_ce_fwd_bwd(h, W, tgt, SOFTCAP, 1.0 / N, nll, lse, dh=dh, dW=dW,
+                                                      accumulate_dW=True, ws=ws, stream=stream),
+                                 lm.bpb_reduce(nll, nbytes, acc, ws=ws, stream=stream)))
+            kind, exec_f, model_f, what = "fwd_bwd", 8, 6, "fwd+dh pass, bpb, dW pass"
+        else:
+            Wq = torch.from_numpy(inp["Wq"]).to(dev)
+            sc = torch.from_numpy(inp["scales"].view(np.int16)).to(dev)
+            dh = torch.empty_like(h)
+            ms = gpu_ms(lambda: (lm.lmhead_ce_fwd_bwd_int4(h, Wq, sc, si.INT4_GROUP, SOFTCAP, tgt, 1.0 / N, nll, lse,
+                                                           dh, ws=ws, stream=stream),
+                                 lm.bpb_reduce(nll, nbytes, acc, ws=ws, stream=stream)))
+            kind, exec_f, model_f, what = "fwd_dh", 4, 4, "int4 dequant + fwd+dh pass, bpb"
+        if lm.lmce_status(ws) != lm.LMCE_OK:
+            raise RuntimeError(f"workload {cfg}: device status {lm.lmce_status(ws)}")
+        if mask is not None:
+            sel = np.nonzero(inp["mask"])[0]
+            o_h, o_t, o_b = inp["h"][sel], inp["tgt"][sel], inp["nbytes"][sel]
+        else:
+            o_h, o_t, o_b = inp["h"], inp["tgt"], inp["nbytes"]
+        o_W = inp["W"] if cfg != 5 else oracle.dequant_int4(inp["Wq"], inp["scales"], d, si.INT4_GROUP)
+        o_rate, S = oracle_rate(o_h, o_W, o_t, o_b, kind)
+        tf = lambda k: k * M * V * d / (ms * 1e-3) / 1e12 / peak  # noqa: E731
+        rows.append((cfg, what, N, V, M / ms * 1e3, ms, tf(exec_f), tf(model_f), o_rate, S))
+        del inp
+    print(f"bf16 peak {peak} TFLOP/s ({measured_peaks()[3]}); oracle threads {oracle.num_threads()}")
+    print("| Workload | Call | GPU tokens/s | GPU ms per call | executed FLOPs / peak | model FLOPs / peak "
+          "| Oracle tokens/s (sample rows) |")
+    print("|---|---|---|---|---|---|---|")
+    for cfg, what, N, V, tps, ms, fe, fm, o, S in rows:
+        print(f"| {cfg}: N={N}, V={V} | {what} | {tps / 1e6:.2f} M | {ms:.3f} | {100 * fe:.1f} % | {100 * fm:.1f} % "
+              f"| {o:.0f} ({S}) |")
+
+
 def main():
     args = parse()
+    if args.table:
+        run_table(args)
+        return
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))

@@ -165,6 +165,20 @@ LMCE_API int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* 
                        const float* lse, const float* nll, float grad_scale, lmce_bf16* dh, void* ws,
                        size_t ws_bytes, void* stream);
 
+/* Forward and dh for the int4 head in one call: the head is dequantised once
+ * (as in lmhead_ce_fwd_int4) and, for softcap <= 60, nll, lse and dh come
+ * from the single fused pass of lmhead_ce_fwd_bwd; above that the forward
+ * and the dh backward run as two passes.  Equal, up to rounding order, to
+ * lmhead_ce_fwd_int4 followed by lmhead_ce_bwd_int4.  nll, lse [N] fp32 and
+ * dh (row stride ldh, 16-byte aligned) are required.  Needs a workspace
+ * sized with LMCE_WS_INT4 (| LMCE_WS_MASKED with a row mask).  A target
+ * outside [0, V) sets LMCE_EDATA in the status word and nll = NaN for that
+ * row; its dh row stays finite but carries no meaning. */
+LMCE_API int lmhead_ce_fwd_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales,
+                           int group, int64_t N, int64_t V, int64_t d, const int64_t* tgt,
+                           const uint8_t* row_mask, float softcap, float grad_scale, float* nll, float* lse,
+                           lmce_bf16* dh, void* ws, size_t ws_bytes, void* stream);
+
 /* Bits-per-byte sums (tproger news, "Rules and metric").  Adds, over rows with
  * row_mask != 0 (all rows if NULL), sum nll (fp64), sum bytes and the row
  * count into *acc (device memory).  Deterministic: fixed grid, fixed

@@ -30,7 +30,7 @@ EXPORTS = (
     "lmce_workspace_bytes", "lmce_workspace_init", "lmce_softcap_max", "lmhead_ce_fwd", "lmhead_ce_bwd",
     "lmhead_ce_fwd_int4", "lmhead_ce_bwd_int4", "bpb_reduce", "lmce_bpb", "lmhead_int4_dequant",
     "lmce_status", "lmce_last_cuda_error", "lmce_strerror", "lmce_launch_count", "lmhead_ce_fwd_noalloc",
-    "lmhead_ce_fwd_bwd",
+    "lmhead_ce_fwd_bwd", "lmhead_ce_fwd_bwd_int4",
 )
 
 _lib = None
@@ -68,6 +68,7 @@ def lib():
             "lmhead_ce_fwd_bwd": ([P, I64, P, I64, I64, I64, P, P, F, F, P, P, P, P, I, P, SZ, P], I),
             "lmhead_ce_fwd_int4": ([P, I64, P, P, I, I64, I64, I64, P, P, F, P, P, P, SZ, P], I),
             "lmhead_ce_bwd_int4": ([P, I64, P, P, I, I64, I64, I64, P, P, F, P, P, F, P, P, SZ, P], I),
+            "lmhead_ce_fwd_bwd_int4": ([P, I64, P, P, I, I64, I64, I64, P, P, F, F, P, P, P, P, SZ, P], I),
             "bpb_reduce": ([P, P, P, I64, P, P, SZ, P], I),
             "lmce_bpb": ([ctypes.POINTER(_BpbAcc), ctypes.POINTER(ctypes.c_double)], I),
             "lmhead_int4_dequant": ([P, P, I64, I64, I, P, P], I),
@@ -195,6 +196,19 @@ def lmhead_ce_bwd_int4(h, Wq, scales, group, softcap, tgt, lse, grad_scale, dh, 
                                   _p(row_mask), float(softcap), _p(lse), _p(nll), float(grad_scale), _p(dh),
                                   _p(ws), ws.numel(), _stream(stream))
     _check(rc, "lmhead_ce_bwd_int4")
+
+
+def lmhead_ce_fwd_bwd_int4(h, Wq, scales, group, softcap, tgt, grad_scale, nll, lse, dh, row_mask=None, ws=None,
+                           stream=None):
+    _bf16_bits(h, "h")
+    N, d = h.shape
+    V = Wq.shape[0]
+    if dh.stride(0) != h.stride(0):
+        raise ValueError("dh must have the same row stride as h")
+    rc = lib().lmhead_ce_fwd_bwd_int4(_p(h), h.stride(0), _p(Wq), _p(scales), int(group), N, V, d, _p(tgt),
+                                      _p(row_mask), float(softcap), float(grad_scale), _p(nll), _p(lse), _p(dh),
+                                      _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "lmhead_ce_fwd_bwd_int4")
 
 
 def bpb_acc(device="cuda") -> torch.Tensor:

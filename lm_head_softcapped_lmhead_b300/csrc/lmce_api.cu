@@ -456,6 +456,34 @@ int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const
                        ws_bytes, stream);
 }
 
+int lmhead_ce_fwd_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
+                           int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask,
+                           float softcap, float grad_scale, float* nll, float* lse, lmce_bf16* dh, void* ws,
+                           size_t ws_bytes, void* stream) {
+  if (int rc = check_int4(Wq, scales, group, V, d); rc) return rc;
+  if (!ws || !aligned16(ws)) return LMCE_EINVAL;
+  const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_INT4 | (row_mask ? LMCE_WS_MASKED : 0u));
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  char* w = static_cast<char*>(ws);
+  lmce_bf16* wdeq = reinterpret_cast<lmce_bf16*>(w + L.wdeq);
+  if (int rc = check_common(h, ldh, wdeq, N, V, d, tgt, softcap, ws); rc) return rc;
+  if (!nll || !lse || !dh || !aligned16(dh)) return LMCE_EINVAL;
+  if (!std::isfinite(grad_scale)) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  unsigned* status = reinterpret_cast<unsigned*>(w + L.status);
+  if (int rc = dequant_impl(Wq, scales, V, d, group, wdeq, s, di.sms); rc) return rc;
+  if (softcap <= kFusedSoftcapMax)
+    return fd_launch(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, status, di.sms, s);
+  if (int rc = fwd_impl(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream,
+                        LMCE_WS_INT4);
+      rc)
+    return rc;
+  return bwd_launch(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, nullptr, 0, status,
+                    w + L.bwd, di.sms, s);
+}
+
 int bpb_reduce(const float* nll, const int32_t* bytes, const uint8_t* row_mask, int64_t N, lmce_bpb_acc* acc,
                void* ws, size_t ws_bytes, void* stream) {
   if (!nll || !bytes || !acc || !ws || N < 1) return LMCE_EINVAL;

@@ -107,6 +107,23 @@ def test_int4_host_validation(L):
     assert L.lmhead_int4_dequant(P(A + 3), P(A), 10, 512, 64, P(A), None) == EINVAL
 
 
+def test_fwd_bwd_int4_host_validation(L):
+    P = ctypes.c_void_p
+
+    def fb(Wq=A, group=64, nll=A, lse=A, dh=A, w=1.0, d=512, c=30.0, ws_bytes=1 << 40):
+        return L.lmhead_ce_fwd_bwd_int4(P(A), 512, P(Wq), P(A), group, 100, 200, d, P(A), None, c, w, P(nll),
+                                        P(lse), P(dh), P(A), ws_bytes, None)
+    assert fb(Wq=0) == EINVAL
+    assert fb(group=48) == EINVAL            # does not divide d
+    assert fb(nll=0) == EINVAL
+    assert fb(lse=0) == EINVAL
+    assert fb(dh=0) == EINVAL                # the int4 head is frozen: dh is the only gradient
+    assert fb(dh=A + 4) == EINVAL
+    assert fb(w=float("nan")) == EINVAL
+    assert fb(c=82.0) == ENOTSUP
+    assert fb(ws_bytes=L.lmce_workspace_bytes(100, 200, 512, 0)) == EINVAL   # no room for the dequantised head
+
+
 def test_bpb_reduce_validation(L):
     P = ctypes.c_void_p
     assert L.bpb_reduce(P(0), P(A), None, 10, P(A), P(A), 1 << 20, None) == EINVAL

@@ -91,6 +91,33 @@ def test_fwd_row_mask(lm, oracle_mod):
     assert np.abs(nll - ref).max() <= NLL_ATOL
 
 
+def test_fwd_eval_stream_call_sampled(lm, oracle_mod):
+    """One call of the sliding-window evaluation stream as `bench.py --table`
+    times it: 512 windows of 2048 rows (1,048,576 rows, 32,768 scored; V=8192,
+    d=512) through the compacting forward and bpb_reduce.  48 sampled scored
+    rows against the oracle, every unscored row 0, and the device's bpb sums
+    against the oracle's reduction of the device's nll."""
+    N = 512 * si.WINDOW
+    inp = si.make_inputs(4, N=N)
+    mask = inp["mask"]
+    d_inp = dev_inputs(inp)
+    nll, lse, ws = run_fwd(lm, d_inp, 30.0, mask=d_inp["mask"])
+    scored = np.nonzero(mask)[0]
+    assert scored.size == 512 * si.STRIDE
+    assert np.all(nll[mask == 0] == 0) and np.all(lse[mask == 0] == 0)
+    assert np.all(np.isfinite(nll[scored]))
+    rows = np.random.default_rng(4).choice(scored, 48, replace=False)
+    ref, ref_lse = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], 30.0, rows=rows)
+    assert np.abs(nll[rows] - ref).max() <= NLL_ATOL
+    assert np.abs(lse[rows] - ref_lse).max() <= NLL_ATOL
+    acc = lm.bpb_acc()
+    lm.bpb_reduce(torch.from_numpy(nll).cuda(), d_inp["nbytes"], acc, row_mask=d_inp["mask"], ws=ws)
+    s_nll, s_bytes, n = lm.read_bpb_acc(acc)
+    ref_bpb, ref_s_nll, ref_s_bytes, ref_n = oracle_mod.bpb(nll, inp["nbytes"], mask)
+    assert (s_bytes, n) == (ref_s_bytes, ref_n)
+    assert abs(s_nll - ref_s_nll) <= BPB_RTOL * abs(ref_s_nll)
+
+
 def test_fwd_all_masked(lm):
     N, V, d = 300, 500, 128
     inp = si.make_inputs(2, N=N, V=V, d=d)

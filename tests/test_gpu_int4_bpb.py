@@ -71,6 +71,68 @@ def test_int4_fwd_bwd_match_oracle(lm, oracle_mod, N, V):
         assert rel_fro(bf16_to_f64(dh)[rows], ref) <= GRAD_RTOL
 
 
+@pytest.mark.parametrize("N,V,c,masked", [
+    (300, 1000, 30.0, False),    # ragged N and V, the fused pass
+    (257, 700, 70.0, False),     # softcap above 60: forward and dh as two passes
+    (400, 600, 30.0, True),      # row mask
+    (130, 100, 30.0, False),     # V below one 128-column tile
+])
+def test_int4_fused_fwd_bwd_matches_oracle(lm, oracle_mod, N, V, c, masked):
+    d = 512
+    inp = si.make_inputs(5, N=N, V=V, d=d)
+    d_inp = dev_inputs(inp)
+    mask = (np.arange(N) % 7 != 3).astype(np.uint8) if masked else None
+    M = N if mask is None else int(mask.sum())
+    Wdeq = oracle_mod.dequant_int4(inp["Wq"], inp["scales"], d, 64)
+    ws = lm.workspace(N, V, d, lm.LMCE_WS_INT4 | (lm.LMCE_WS_MASKED if masked else 0))
+    nll = torch.full((N,), float("nan"), device="cuda")
+    lse = torch.full((N,), float("nan"), device="cuda")
+    dh = torch.full_like(d_inp["h"], float("nan"))
+    lm.lmhead_ce_fwd_bwd_int4(d_inp["h"], d_inp["Wq"], d_inp["scales"], 64, c, d_inp["tgt"], 1.0 / M, nll, lse, dh,
+                              row_mask=None if mask is None else torch.from_numpy(mask).cuda(), ws=ws)
+    assert lm.lmce_status(ws) == lm.LMCE_OK
+    ref_nll, ref_lse = oracle_mod.fwd(inp["h"], Wdeq, inp["tgt"], c, mask=mask)
+    assert np.abs(nll.cpu().numpy() - ref_nll).max() <= NLL_ATOL
+    assert np.abs(lse.cpu().numpy() - ref_lse).max() <= NLL_ATOL
+    ref_dh, _ = oracle_mod.bwd(inp["h"], Wdeq, inp["tgt"], c, ref_lse, 1.0 / M, mask=mask, want_dW=False)
+    got = bf16_to_f64(dh)
+    if mask is not None:
+        assert np.all(got[mask == 0] == 0)
+    assert rel_fro(got, ref_dh) <= GRAD_RTOL
+
+
+def test_int4_fused_full_size_sampled(lm, oracle_mod):
+    """The int4 head at full size (N=65536, V=8192, d=512): nll and dh of 32
+    sampled rows against the oracle, and nll against the two-call path
+    (lmhead_ce_fwd_int4 then lmhead_ce_bwd_int4) on every row."""
+    inp = si.make_inputs(5)
+    N, V, d = inp["N"], inp["V"], inp["d"]
+    d_inp = dev_inputs(inp)
+    ws = lm.workspace(N, V, d, lm.LMCE_WS_INT4)
+    nll = torch.empty(N, device="cuda")
+    lse = torch.empty(N, device="cuda")
+    dh = torch.empty_like(d_inp["h"])
+    lm.lmhead_ce_fwd_bwd_int4(d_inp["h"], d_inp["Wq"], d_inp["scales"], 64, 30.0, d_inp["tgt"], 1.0 / N, nll, lse,
+                              dh, ws=ws)
+    nll2 = torch.empty(N, device="cuda")
+    lse2 = torch.empty(N, device="cuda")
+    dh2 = torch.empty_like(d_inp["h"])
+    lm.lmhead_ce_fwd_int4(d_inp["h"], d_inp["Wq"], d_inp["scales"], 64, 30.0, d_inp["tgt"], nll2, lse2, ws=ws)
+    lm.lmhead_ce_bwd_int4(d_inp["h"], d_inp["Wq"], d_inp["scales"], 64, 30.0, d_inp["tgt"], lse2, 1.0 / N, dh2,
+                          ws=ws, nll=nll2)
+    assert lm.lmce_status(ws) == lm.LMCE_OK
+    n = nll.cpu().numpy()
+    assert np.all(np.isfinite(n))
+    assert np.abs(n - nll2.cpu().numpy()).max() <= NLL_ATOL
+    assert rel_fro(bf16_to_f64(dh), bf16_to_f64(dh2)) <= GRAD_RTOL
+    Wdeq = oracle_mod.dequant_int4(inp["Wq"], inp["scales"], d, 64)
+    rows = np.random.default_rng(5).choice(N, 32, replace=False)
+    ref_nll, ref_lse = oracle_mod.fwd(inp["h"], Wdeq, inp["tgt"], 30.0, rows=rows)
+    assert np.abs(n[rows] - ref_nll).max() <= NLL_ATOL
+    ref = oracle_mod.dh_rows(inp["h"], Wdeq, inp["tgt"], 30.0, rows, ref_lse, 1.0 / N)
+    assert rel_fro(bf16_to_f64(dh)[rows], ref) <= GRAD_RTOL
+
+
 def test_bpb_reduce_matches_oracle_and_is_deterministic(lm, oracle_mod):
     rng = np.random.default_rng(4)
     N = 100003
