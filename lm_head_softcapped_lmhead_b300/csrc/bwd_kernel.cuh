@@ -75,7 +75,13 @@ constexpr uint32_t ZSTAGE = ZSC * CHUNK;   // 64 KB
 // other (4 KB apart).
 constexpr int SLAB_ROWS = 32;
 constexpr int NSLAB = BT / SLAB_ROWS;
-constexpr int ASLOTS = 5;                  // A CTA: ring of slab slots (one tile + one slab)
+// A CTA shared memory: ASLOTS x 32 KB of Y slabs and NPS x 32 KB of P slots.
+// Measured at N=65536, V=8192, d=512 (FD / DW pass, ms): 5 slabs + 2 P slots
+// 1.084 / 1.332; 4 + 3: 1.076 / 1.325; 3 + 4: 1.060 / 1.301; 2 + 5: 1.047 /
+// 1.269; 1 + 6: 1.541 / 1.581.  Deep P buffering decouples the Z epilogue
+// from the A CTA's MMAs; half a tile of Y slabs in flight is enough.
+constexpr int ASLOTS = 2;                  // A CTA: ring of slab slots
+constexpr int NPS = 5;                     // A CTA: P slots (bf16 G tiles from the Z epilogue)
 constexpr uint32_t SLAB_CHUNK = SLAB_ROWS * KB * 2;  // 4 KB
 // Z CTA layout
 // Z CTA: the stationary block X lives in TMEM (columns 256-511, copied there
@@ -91,11 +97,28 @@ constexpr uint32_t REC_BYTES = 32;
 constexpr int FL_LIVE = 1, FL_TVALID = 2, FL_HIT = 4;
 // A CTA layout
 constexpr uint32_t A_Y = 0;                             // ring of ASLOTS slabs (32 x d each)
-constexpr uint32_t A_P = A_Y + ASLOTS * MAX_KC * SLAB_CHUNK;  // 2 P slots of 128 x 128 bf16
+constexpr uint32_t A_P = A_Y + ASLOTS * MAX_KC * SLAB_CHUNK;  // NPS P slots of 128 x 128 bf16
 constexpr uint32_t P_SLOT = 2 * CHUNK;                  // 32 KB
-constexpr uint32_t A_END = A_P + 2 * P_SLOT;
+constexpr uint32_t A_END = A_P + NPS * P_SLOT;
 constexpr uint32_t BAR_OFF = (Z_END > A_END ? Z_END : A_END);
 constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;
+// mbarrier indices (8 bytes each) from BAR_OFF; bytes 504..511 hold the TMEM
+// address and the abort flag.
+constexpr int B_ZY_FULL = 0;                      // [YSTAGES]
+constexpr int B_ZY_EMPTY = B_ZY_FULL + YSTAGES;   // [YSTAGES]
+constexpr int B_X_FREE = B_ZY_EMPTY + YSTAGES;
+constexpr int B_X_READY = B_X_FREE + 1;
+constexpr int B_ACC_FULL = B_X_READY + 1;         // [2]
+constexpr int B_ACC_EMPTY = B_ACC_FULL + 2;       // [2]
+constexpr int B_P_EMPTY = B_ACC_EMPTY + 2;        // [NPS]
+constexpr int B_P_FULL = B_P_EMPTY + NPS;         // [NPS]
+constexpr int B_AY_FULL = B_P_FULL + NPS;         // [ASLOTS]
+constexpr int B_AY_EMPTY = B_AY_FULL + ASLOTS;    // [ASLOTS]
+constexpr int B_MMA_DONE = B_AY_EMPTY + ASLOTS;
+constexpr int B_RD_FULL = B_MMA_DONE + 1;
+constexpr int B_RD_EMPTY = B_RD_FULL + 1;
+static_assert((B_RD_EMPTY + 1) * 8 <= 504, "mbarriers overlap the TMEM address slot");
+static_assert(SMEM_BYTES <= 232448, "shared memory above the 227 KB per-CTA limit");
 static_assert(Z_REC + (EPI_WARPS / 4) * BM * REC_BYTES <= BAR_OFF, "FD row records overlap the barriers");
 constexpr uint32_t Z_TMEM_COLS = 512;
 constexpr uint32_t A_TMEM_COLS = 512;
@@ -391,20 +414,20 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
   // Z CTA barriers
-  uint64_t* zy_full = bars + 0;     // [YSTAGES]
-  uint64_t* zy_empty = bars + 6;    // [YSTAGES]
-  uint64_t* x_free = bars + 12;     // Z: the previous unit's MMAs no longer read X in TMEM
-  uint64_t* x_ready = bars + 13;    // Z: X's tcgen05.cp have completed
-  uint64_t* acc_full = bars + 14;   // [2]  Z: z tiles; A: [0] = accumulator done
-  uint64_t* acc_empty = bars + 16;  // [2]  Z: z tiles; A: [0] = accumulator drained
-  uint64_t* p_empty = bars + 18;    // [2]  in Z, arrived by A's MMA commit
+  uint64_t* zy_full = bars + B_ZY_FULL;      // [YSTAGES]
+  uint64_t* zy_empty = bars + B_ZY_EMPTY;    // [YSTAGES]
+  uint64_t* x_free = bars + B_X_FREE;        // Z: the previous unit's MMAs no longer read X in TMEM
+  uint64_t* x_ready = bars + B_X_READY;      // Z: X's tcgen05.cp have completed
+  uint64_t* acc_full = bars + B_ACC_FULL;    // [2]  Z: z tiles; A: [0] = accumulator done
+  uint64_t* acc_empty = bars + B_ACC_EMPTY;  // [2]  Z: z tiles; A: [0] = accumulator drained
+  uint64_t* p_empty = bars + B_P_EMPTY;      // [NPS]  in Z, arrived by A's MMA commit
   // A CTA barriers
-  uint64_t* p_full = bars + 20;     // [2]  in A: A's expect_tx + the bytes of Z's st.async
-  uint64_t* ay_full = bars + 22;    // [ASLOTS] slab slots of the Y ring
-  uint64_t* ay_empty = bars + 28;   // [ASLOTS]
-  uint64_t* mma_done = bars + 34;
-  uint64_t* rd_full = bars + 35;    // FD, in A: the Z epilogue's row records are written
-  uint64_t* rd_empty = bars + 36;   // FD, in Z: the A drain has read them
+  uint64_t* p_full = bars + B_P_FULL;        // [NPS]  in A: A's expect_tx + the bytes of Z's st.async
+  uint64_t* ay_full = bars + B_AY_FULL;      // [ASLOTS] slab slots of the Y ring
+  uint64_t* ay_empty = bars + B_AY_EMPTY;    // [ASLOTS]
+  uint64_t* mma_done = bars + B_MMA_DONE;
+  uint64_t* rd_full = bars + B_RD_FULL;      // FD, in A: the Z epilogue's row records are written
+  uint64_t* rd_empty = bars + B_RD_EMPTY;    // FD, in Z: the A drain has read them
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 504);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 508);
 
@@ -425,6 +448,8 @@ __global__ void __launch_bounds__(THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(acc_full + i, 1);
       mbar_init(acc_empty + i, EPI_WARPS);
+    }
+    for (int i = 0; i < NPS; ++i) {
       mbar_init(p_empty + i, 1);
       mbar_init(p_full + i, 1);
     }
@@ -741,8 +766,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
             st_async_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3], pfull_slot);
           }
-          slot ^= 1;
-          if (slot == 0) sph ^= 1u;
+          if (++slot == NPS) {
+            slot = 0;
+            sph ^= 1u;
+          }
         }
         if (MODE == FD) {
           // Row record for the A drain, once it has read the previous one.
@@ -770,7 +797,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int rs = 0;
         uint32_t rph = 0;
         bool ok = true;
-        uint32_t pend = 0, pend_ph[ASLOTS] = {0, 0, 0, 0, 0};
+        uint32_t pend = 0, pend_ph[ASLOTS] = {};
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
@@ -810,9 +837,8 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t idesc_h0 = idesc_bf16_f32(128, 64 * nh0, false, true);
         const uint32_t idesc_h1 = idesc_bf16_f32(128, 64 * (nh1 > 0 ? nh1 : 1), false, true);
         // Each P slot completes when all its bytes (st.async from the Z CTA)
-        // have landed: arm both slots for their first use.
-        mbar_expect_tx(p_full + 0, P_SLOT);
-        mbar_expect_tx(p_full + 1, P_SLOT);
+        // have landed: arm every slot for its first use.
+        for (int i = 0; i < NPS; ++i) mbar_expect_tx(p_full + i, P_SLOT);
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
@@ -856,8 +882,10 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
             if (!ok) break;
             umma_commit_mc(p_empty + slot, static_cast<uint16_t>(1u << 0));  // P slot free (Z CTA)
-            slot ^= 1;
-            if (slot == 0) sph ^= 1u;
+            if (++slot == NPS) {
+              slot = 0;
+              sph ^= 1u;
+            }
           }
           if (ok) umma_commit(acc_full);  // accumulator of this unit complete
         }
