@@ -62,12 +62,12 @@ constexpr int BM = 128;   // stationary block (TMEM lanes)
 constexpr int BT = 128;   // streamed tile (z columns; K of the accumulation)
 constexpr int KB = 64;    // K elements per chunk
 constexpr int MAX_KC = 8; // d <= 512
-constexpr int YSTAGES = 3;  // Z ring: stages of four 64-column chunks (64 KB, one TMA load each)
-constexpr int ZSC = 4;      // chunks per Z ring stage
+constexpr int ZSC = 4;      // chunks per Z ring stage (64 KB, one TMA load)
 constexpr int EPI_WARPS = 16;  // Z: epilogue warps; A: drain warps
 constexpr int TMA_WARP = 16;
 constexpr int MMA_WARP = 17;
-constexpr int THREADS = 576;
+constexpr int FWD_WARP = 18;   // Z: forwards P tiles to the A CTA; A: acknowledges their arrival
+constexpr int THREADS = 608;
 constexpr uint32_t CHUNK = 128 * KB * 2;  // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t ZSTAGE = ZSC * CHUNK;   // 64 KB
 // The A CTA loads its Y tile in 4 slabs of 32 rows x d (one TMA load per
@@ -75,51 +75,66 @@ constexpr uint32_t ZSTAGE = ZSC * CHUNK;   // 64 KB
 // other (4 KB apart).
 constexpr int SLAB_ROWS = 32;
 constexpr int NSLAB = BT / SLAB_ROWS;
-// A CTA shared memory: ASLOTS x 32 KB of Y slabs and NPS x 32 KB of P slots.
-// Measured at N=65536, V=8192, d=512 (FD / DW pass, ms): 5 slabs + 2 P slots
-// 1.084 / 1.332; 4 + 3: 1.076 / 1.325; 3 + 4: 1.060 / 1.301; 2 + 5: 1.047 /
-// 1.269; 1 + 6: 1.541 / 1.581.  Deep P buffering decouples the Z epilogue
-// from the A CTA's MMAs; half a tile of Y slabs in flight is enough.
-constexpr int ASLOTS = 2;                  // A CTA: ring of slab slots
-constexpr int NPS = 5;                     // A CTA: P slots (bf16 G tiles from the Z epilogue)
 constexpr uint32_t SLAB_CHUNK = SLAB_ROWS * KB * 2;  // 4 KB
-// Z CTA layout
-// Z CTA: the stationary block X lives in TMEM (columns 256-511, copied there
-// from the ring with tcgen05.cp); shared memory is only the ring.
-constexpr uint32_t Z_Y = 0;                             // ring of YSTAGES stages
-constexpr uint32_t Z_END = Z_Y + YSTAGES * ZSTAGE;
-constexpr uint32_t Z_TMEM_X = 256;
+constexpr uint32_t P_SLOT = 2 * CHUNK;                // 32 KB: one 128 x 128 bf16 P tile
+constexpr uint32_t Z_TMEM_X = 256;  // Z: the stationary block X in TMEM columns 256-511
 // FD: per-row records of the Z epilogue, [column group][row] x 32 bytes:
 // {double sum of e^s over the non-target columns, float e^{s_t},
 //  1 - tanh_t^2, int target, int flags}.
-constexpr uint32_t Z_REC = Z_END;
 constexpr uint32_t REC_BYTES = 32;
 constexpr int FL_LIVE = 1, FL_TVALID = 2, FL_HIT = 4;
-// A CTA layout
-constexpr uint32_t A_Y = 0;                             // ring of ASLOTS slabs (32 x d each)
-constexpr uint32_t A_P = A_Y + ASLOTS * MAX_KC * SLAB_CHUNK;  // NPS P slots of 128 x 128 bf16
-constexpr uint32_t P_SLOT = 2 * CHUNK;                  // 32 KB
-constexpr uint32_t A_END = A_P + NPS * P_SLOT;
-constexpr uint32_t BAR_OFF = (Z_END > A_END ? Z_END : A_END);
-constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;
-// mbarrier indices (8 bytes each) from BAR_OFF; bytes 504..511 hold the TMEM
-// address and the abort flag.
-constexpr int B_ZY_FULL = 0;                      // [YSTAGES]
-constexpr int B_ZY_EMPTY = B_ZY_FULL + YSTAGES;   // [YSTAGES]
-constexpr int B_X_FREE = B_ZY_EMPTY + YSTAGES;
-constexpr int B_X_READY = B_X_FREE + 1;
-constexpr int B_ACC_FULL = B_X_READY + 1;         // [2]
-constexpr int B_ACC_EMPTY = B_ACC_FULL + 2;       // [2]
-constexpr int B_P_EMPTY = B_ACC_EMPTY + 2;        // [NPS]
-constexpr int B_P_FULL = B_P_EMPTY + NPS;         // [NPS]
-constexpr int B_AY_FULL = B_P_FULL + NPS;         // [ASLOTS]
-constexpr int B_AY_EMPTY = B_AY_FULL + ASLOTS;    // [ASLOTS]
-constexpr int B_MMA_DONE = B_AY_EMPTY + ASLOTS;
-constexpr int B_RD_FULL = B_MMA_DONE + 1;
-constexpr int B_RD_EMPTY = B_RD_FULL + 1;
-static_assert((B_RD_EMPTY + 1) * 8 <= 504, "mbarriers overlap the TMEM address slot");
-static_assert(SMEM_BYTES <= 232448, "shared memory above the 227 KB per-CTA limit");
-static_assert(Z_REC + (EPI_WARPS / 4) * BM * REC_BYTES <= BAR_OFF, "FD row records overlap the barriers");
+
+// Shared-memory plan of a mode.  The Z CTA holds the ring of Y stages (X is
+// in TMEM); the A CTA holds a ring of Y slabs and the P slots.  P tiles reach
+// the A CTA in one of two ways:
+//  * FD: each epilogue thread stores its 64 bytes straight into the P slot
+//    with st.async (the FD epilogue is light, and the stores overlap it);
+//  * DH, DW: the epilogue writes the tile into a local staging copy and the
+//    forwarder warp sends each 16 KB column chunk with one bulk DSMEM copy
+//    (their epilogues are heavier, and 2048 DSMEM stores per tile slow them).
+// Deep P buffering decouples the Z epilogue from the A CTA's MMAs; half a
+// tile of Y slabs in flight is enough.  Measured at N=65536, V=8192, d=512
+// (ms per pass): FD, st.async, 3 x 64 KB ring, 5 P slots: 1.044 (bulk copies
+// with 2 staging copies: 1.101); DW, bulk, 2 x 64 KB ring, 2 staging copies,
+// 4 P slots: 1.078 (st.async with 5 P slots: 1.273).
+template <int MODE>
+struct Cfg {
+  static constexpr bool kBulk = MODE != FD;
+  static constexpr int YSTAGES = kBulk ? 2 : 3;  // Z ring stages (64 KB)
+  static constexpr int NSTG = kBulk ? 2 : 0;     // Z: P staging copies
+  static constexpr int ASLOTS = 2;               // A: Y slab slots (32 KB)
+  static constexpr int NPS = kBulk ? 4 : 5;      // A: P slots (32 KB)
+  // Z CTA layout
+  static constexpr uint32_t Z_Y = 0;
+  static constexpr uint32_t Z_STG = Z_Y + YSTAGES * ZSTAGE;          // NSTG x 2 x 16 KB
+  static constexpr uint32_t Z_REC = Z_STG + NSTG * 2 * CHUNK;        // FD row records
+  static constexpr uint32_t Z_END = Z_REC + (MODE == FD ? (EPI_WARPS / 4) * BM * REC_BYTES : 0u);
+  // A CTA layout
+  static constexpr uint32_t A_Y = 0;
+  static constexpr uint32_t A_P = A_Y + ASLOTS * MAX_KC * SLAB_CHUNK;
+  static constexpr uint32_t A_END = A_P + NPS * P_SLOT;
+  static constexpr uint32_t BAR_OFF = (Z_END > A_END ? Z_END : A_END);
+  static constexpr uint32_t SMEM_BYTES = BAR_OFF + 512 + 1024;
+  // mbarrier indices (8 bytes each) from BAR_OFF; bytes 504..511 hold the
+  // TMEM address and the abort flag.
+  static constexpr int B_ZY_FULL = 0;                      // [YSTAGES]
+  static constexpr int B_ZY_EMPTY = B_ZY_FULL + YSTAGES;   // [YSTAGES]
+  static constexpr int B_X_FREE = B_ZY_EMPTY + YSTAGES;
+  static constexpr int B_X_READY = B_X_FREE + 1;
+  static constexpr int B_ACC_FULL = B_X_READY + 1;         // [2]
+  static constexpr int B_ACC_EMPTY = B_ACC_FULL + 2;       // [2]
+  static constexpr int B_P_EMPTY = B_ACC_EMPTY + 2;        // [NPS]
+  static constexpr int B_P_FULL = B_P_EMPTY + NPS;         // [NPS]
+  static constexpr int B_AY_FULL = B_P_FULL + NPS;         // [ASLOTS]
+  static constexpr int B_AY_EMPTY = B_AY_FULL + ASLOTS;    // [ASLOTS]
+  static constexpr int B_MMA_DONE = B_AY_EMPTY + ASLOTS;
+  static constexpr int B_RD_FULL = B_MMA_DONE + 1;
+  static constexpr int B_RD_EMPTY = B_RD_FULL + 1;
+  static constexpr int B_STG_FULL = B_RD_EMPTY + 1;        // [NSTG][2]
+  static constexpr int B_STG_EMPTY = B_STG_FULL + 2 * NSTG;  // [NSTG]
+  static_assert((B_STG_EMPTY + NSTG) * 8 <= 504, "mbarriers overlap the TMEM address slot");
+  static_assert(SMEM_BYTES <= 232448, "shared memory above the 227 KB per-CTA limit");
+};
 constexpr uint32_t Z_TMEM_COLS = 512;
 constexpr uint32_t A_TMEM_COLS = 512;
 constexpr uint32_t IDESC_Z = idesc_bf16_f32(128, BT, false, false);
@@ -410,26 +425,29 @@ __global__ void __launch_bounds__(THREADS, 1)
                const __grid_constant__ CUtensorMap tm_ys, const Params p) {
   // tm_x: X blocks and tm_y: Y tiles, box 64 x 128 x 4 (four chunks, 64 KB);
   // tm_ys: Y slabs, box 64 x 32 x KC.
+  using C = Cfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + BAR_OFF);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::BAR_OFF);
   // Z CTA barriers
-  uint64_t* zy_full = bars + B_ZY_FULL;      // [YSTAGES]
-  uint64_t* zy_empty = bars + B_ZY_EMPTY;    // [YSTAGES]
-  uint64_t* x_free = bars + B_X_FREE;        // Z: the previous unit's MMAs no longer read X in TMEM
-  uint64_t* x_ready = bars + B_X_READY;      // Z: X's tcgen05.cp have completed
-  uint64_t* acc_full = bars + B_ACC_FULL;    // [2]  Z: z tiles; A: [0] = accumulator done
-  uint64_t* acc_empty = bars + B_ACC_EMPTY;  // [2]  Z: z tiles; A: [0] = accumulator drained
-  uint64_t* p_empty = bars + B_P_EMPTY;      // [NPS]  in Z, arrived by A's MMA commit
+  uint64_t* zy_full = bars + C::B_ZY_FULL;      // [YSTAGES]
+  uint64_t* zy_empty = bars + C::B_ZY_EMPTY;    // [YSTAGES]
+  uint64_t* x_free = bars + C::B_X_FREE;        // Z: the previous unit's MMAs no longer read X in TMEM
+  uint64_t* x_ready = bars + C::B_X_READY;      // Z: X's tcgen05.cp have completed
+  uint64_t* acc_full = bars + C::B_ACC_FULL;    // [2]  Z: z tiles; A: [0] = accumulator done
+  uint64_t* acc_empty = bars + C::B_ACC_EMPTY;  // [2]  Z: z tiles; A: [0] = accumulator drained
+  uint64_t* p_empty = bars + C::B_P_EMPTY;      // [NPS]  in Z, arrived by A's MMA commit
   // A CTA barriers
-  uint64_t* p_full = bars + B_P_FULL;        // [NPS]  in A: A's expect_tx + the bytes of Z's st.async
-  uint64_t* ay_full = bars + B_AY_FULL;      // [ASLOTS] slab slots of the Y ring
-  uint64_t* ay_empty = bars + B_AY_EMPTY;    // [ASLOTS]
-  uint64_t* mma_done = bars + B_MMA_DONE;
-  uint64_t* rd_full = bars + B_RD_FULL;      // FD, in A: the Z epilogue's row records are written
-  uint64_t* rd_empty = bars + B_RD_EMPTY;    // FD, in Z: the A drain has read them
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + BAR_OFF + 504);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + BAR_OFF + 508);
+  uint64_t* p_full = bars + C::B_P_FULL;        // [NPS]  in A: A's expect_tx + the bytes of Z's st.async
+  uint64_t* ay_full = bars + C::B_AY_FULL;      // [ASLOTS] slab slots of the Y ring
+  uint64_t* ay_empty = bars + C::B_AY_EMPTY;    // [ASLOTS]
+  uint64_t* mma_done = bars + C::B_MMA_DONE;
+  uint64_t* rd_full = bars + C::B_RD_FULL;      // FD, in A: the Z epilogue's row records are written
+  uint64_t* rd_empty = bars + C::B_RD_EMPTY;    // FD, in Z: the A drain has read them
+  uint64_t* stg_full = bars + C::B_STG_FULL;    // [NSTG][2] in Z: the epilogue warps wrote a staging chunk
+  uint64_t* stg_empty = bars + C::B_STG_EMPTY;  // [NSTG] in Z: the A CTA has the staged tile (staging free)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::BAR_OFF + 504);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::BAR_OFF + 508);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -439,7 +457,7 @@ __global__ void __launch_bounds__(THREADS, 1)
   const bool is_z = (rank == 0);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < YSTAGES; ++i) {
+    for (int i = 0; i < C::YSTAGES; ++i) {
       mbar_init(zy_full + i, 1);
       mbar_init(zy_empty + i, 1);
     }
@@ -449,16 +467,18 @@ __global__ void __launch_bounds__(THREADS, 1)
       mbar_init(acc_full + i, 1);
       mbar_init(acc_empty + i, EPI_WARPS);
     }
-    for (int i = 0; i < NPS; ++i) {
+    for (int i = 0; i < C::NPS; ++i) {
       mbar_init(p_empty + i, 1);
       mbar_init(p_full + i, 1);
     }
-    for (int i = 0; i < ASLOTS; ++i) {
+    for (int i = 0; i < C::ASLOTS; ++i) {
       mbar_init(ay_full + i, 1);
       mbar_init(ay_empty + i, 1);
     }
     mbar_init(mma_done, 1);
     mbar_init(rd_full, EPI_WARPS * 32);   // every Z epilogue thread
+    for (int i = 0; i < 2 * C::NSTG; ++i) mbar_init(stg_full + i, EPI_WARPS / 2);  // the chunk's 8 warps
+    for (int i = 0; i < C::NSTG; ++i) mbar_init(stg_empty + i, 1);                 // the A CTA's acknowledgement
     mbar_init(rd_empty, EPI_WARPS * 32);  // every A drain thread
     *abort_flag = 0;
     fence_mbar_init();
@@ -485,15 +505,15 @@ __global__ void __launch_bounds__(THREADS, 1)
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        uint32_t pend = 0, pend_ph[YSTAGES] = {};
+        uint32_t pend = 0, pend_ph[C::YSTAGES] = {};
         const int nst = (p.KC + ZSC - 1) / ZSC;
         auto put = [&](const CUtensorMap* m, int row0, int s4) -> bool {
           if (!mbar_wait(zy_empty + stage, phase ^ 1u, abort_flag, p.status)) return false;
           mbar_expect_tx(zy_full + stage, ZSTAGE);
-          tma_load_3d(smem + Z_Y + stage * ZSTAGE, m, zy_full + stage, 0, row0, ZSC * s4);
+          tma_load_3d(smem + C::Z_Y + stage * ZSTAGE, m, zy_full + stage, 0, row0, ZSC * s4);
           pend |= 1u << stage;
           pend_ph[stage] = phase;
-          if (++stage == YSTAGES) {
+          if (++stage == C::YSTAGES) {
             stage = 0;
             phase ^= 1u;
           }
@@ -511,7 +531,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (!ok) {
           const long long c0 = clock64();
-          for (int s = 0; s < YSTAGES; ++s)
+          for (int s = 0; s < C::YSTAGES; ++s)
             if (pend & (1u << s))
               while (!mbar_try_wait(smem_u32(zy_full + s), pend_ph[s]) && clock64() - c0 < kWaitLimitCycles) {
               }
@@ -542,14 +562,14 @@ __global__ void __launch_bounds__(THREADS, 1)
             for (int c = 0; c < ZSC; ++c) {
               const int kc = ZSC * s4 + c;
               if (kc >= p.KC) break;
-              const uint32_t xa = smem_u32(smem + Z_Y + stage * ZSTAGE + c * CHUNK);
+              const uint32_t xa = smem_u32(smem + C::Z_Y + stage * ZSTAGE + c * CHUNK);
 #pragma unroll
               for (int k = 0; k < KB / 16; ++k)
                 tmem_cp_128x256b(tmem_base + Z_TMEM_X + static_cast<uint32_t>(kc * 32 + k * 8),
                                  sdesc_sw128(xa + k * 32, 16, 1024));
             }
             umma_commit(zy_empty + stage);
-            if (++stage == YSTAGES) {
+            if (++stage == C::YSTAGES) {
               stage = 0;
               phase ^= 1u;
             }
@@ -572,7 +592,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               tc_fence_after();
               // The issue loop stays short (descriptors advanced by constant
               // offsets, unrolled): one M=128 N=128 MMA is 64 tensor cycles.
-              const uint64_t b0 = sdesc_sw128(smem_u32(smem + Z_Y + stage * ZSTAGE), 16, 1024);
+              const uint64_t b0 = sdesc_sw128(smem_u32(smem + C::Z_Y + stage * ZSTAGE), 16, 1024);
               const uint32_t a0 = tmem_base + Z_TMEM_X + static_cast<uint32_t>(s4 * ZSC * 32);
               if (ZSC * (s4 + 1) <= p.KC) {
 #pragma unroll
@@ -591,7 +611,7 @@ __global__ void __launch_bounds__(THREADS, 1)
                                  (s4 | c | k) != 0 ? 1u : 0u);
               }
               umma_commit(zy_empty + stage);
-              if (++stage == YSTAGES) {
+              if (++stage == C::YSTAGES) {
                 stage = 0;
                 phase ^= 1u;
               }
@@ -606,6 +626,58 @@ __global__ void __launch_bounds__(THREADS, 1)
         const long long c0 = clock64();
         while (!mbar_try_wait(smem_u32(mma_done), 0) && clock64() - c0 < kWaitLimitCycles) {
         }
+      }
+    } else if (warp == FWD_WARP) {
+      if constexpr (C::kBulk) {
+       if (lane == 0) {
+        // ---- P forwarder: staging copy -> the A CTA's P slot ----
+        // Per tile, each 16 KB column chunk goes in one bulk DSMEM copy that
+        // completes the slot's mbarrier in the A CTA (which expects the whole
+        // tile), once that slot's previous tile has been consumed.  The A
+        // CTA acknowledges each landed tile on stg_empty, which frees the
+        // staging copy for the epilogue.
+        const uint32_t peer_p = mapa_shared(smem_u32(smem + C::A_P), 1);
+        const uint32_t peer_pfull = mapa_shared(smem_u32(p_full), 1);
+        const uint32_t stg = smem_u32(smem + C::Z_STG);
+        int slot = 0;
+        uint32_t sph = 0;
+        int issued = 0;  // tiles sent; tile n uses staging copy n % NSTG
+        bool ok = true;
+        for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
+          int blk, t0, t1;
+          unit_range(p, u, blk, t0, t1);
+          for (int i = 0; i < t1 - t0 && ok; ++i) {
+            const int set = issued % C::NSTG;
+            const uint32_t use_ph = static_cast<uint32_t>(issued / C::NSTG) & 1u;
+            for (int h = 0; h < 2 && ok; ++h) {
+              ok = mbar_wait(stg_full + 2 * set + h, use_ph, abort_flag, p.status);
+              if (ok && h == 0) ok = mbar_wait<true>(p_empty + slot, sph ^ 1u, abort_flag, p.status);
+              if (ok)
+                bulk_copy_to_peer(peer_p + static_cast<uint32_t>(slot) * P_SLOT + static_cast<uint32_t>(h) * CHUNK,
+                                  stg + static_cast<uint32_t>(2 * set + h) * CHUNK, CHUNK,
+                                  peer_pfull + static_cast<uint32_t>(slot) * 8u);
+            }
+            if (!ok) break;
+            ++issued;
+            if (++slot == C::NPS) {
+              slot = 0;
+              sph ^= 1u;
+            }
+          }
+        }
+        if (ok) {
+          // Every staging copy's last acknowledgement: no copy is in flight after them.
+          for (int set = 0; set < C::NSTG && set < issued && ok; ++set) {
+            const int uses = (issued - set + C::NSTG - 1) / C::NSTG;
+            ok = mbar_wait<true>(stg_empty + set, static_cast<uint32_t>(uses - 1) & 1u, abort_flag, p.status);
+          }
+        } else {
+          // Let copies already issued land before this CTA can leave.
+          const long long c0 = clock64();
+          while (clock64() - c0 < 200000) {
+          }
+        }
+       }
       }
     } else {
       // ---- Z epilogue: z tile -> P tile in the peer's shared memory ----
@@ -632,11 +704,13 @@ __global__ void __launch_bounds__(THREADS, 1)
       int cur_hit = -1, pf_hit = -1;
       float cur_pm1 = 0.f, pf_pm1 = 0.f;
       const int use_pm1 = p.nll_in != nullptr;
-      const uint32_t peer_p = mapa_shared(smem_u32(smem + A_P), 1);
-      const uint32_t peer_pfull = mapa_shared(smem_u32(p_full), 1);
+      const uint32_t stg = smem_u32(smem + C::Z_STG);                 // bulk modes
+      const uint32_t peer_p = mapa_shared(smem_u32(smem + C::A_P), 1);  // FD
+      const uint32_t peer_pfull = mapa_shared(smem_u32(p_full), 1);     // FD
       const uint32_t peer_rd_full = mapa_shared(smem_u32(rd_full), 1);
       int acc = 0, slot = 0;
       uint32_t aph = 0, sph = 0;
+      int staged = 0;  // bulk modes: tiles staged; tile n uses staging copy n % NSTG
       bool ok = true;
       int fd_units = 0;
       for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
@@ -753,22 +827,45 @@ __global__ void __launch_bounds__(THREADS, 1)
             else
               g_chunk_dw<false>(r, kc, cur_nl, cur_hit, m, use_pm1, cur_pm1, packed);
           }
-          // Four swizzled 16-byte DSMEM stores into the P slot, once the A
-          // CTA's MMA no longer reads it.
-          ok = mbar_wait<true>(p_empty + slot, sph ^ 1u, abort_flag, p.status);
-          if (!ok) break;
-          const uint32_t dst_row = peer_p + static_cast<uint32_t>(slot) * P_SLOT +
-                                   static_cast<uint32_t>(cq >> 1) * CHUNK + static_cast<uint32_t>(m) * 128u;
-          const uint32_t pfull_slot = peer_pfull + static_cast<uint32_t>(slot) * 8u;
+          if constexpr (C::kBulk) {
+            // Four swizzled 16-byte stores into the staging copy (the P slot
+            // layout), once that copy's previous tile has reached the A CTA;
+            // the forwarder warp then sends each 64-column chunk in one bulk
+            // copy.
+            const int set = staged % C::NSTG;
+            ok = mbar_wait<true>(stg_empty + set, (static_cast<uint32_t>(staged / C::NSTG) & 1u) ^ 1u, abort_flag,
+                                 p.status);
+            if (!ok) break;
+            const uint32_t dst_row =
+                stg + static_cast<uint32_t>(2 * set + (cq >> 1)) * CHUNK + static_cast<uint32_t>(m) * 128u;
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const uint32_t unit = static_cast<uint32_t>((cq & 1) * 4 + v);
-            const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
-            st_async_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3], pfull_slot);
-          }
-          if (++slot == NPS) {
-            slot = 0;
-            sph ^= 1u;
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t unit = static_cast<uint32_t>((cq & 1) * 4 + v);
+              const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
+              st_shared_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
+            }
+            fence_proxy_async_smem();  // visible to the bulk copy (async proxy)
+            __syncwarp();
+            if (lane == 0) mbar_arrive(stg_full + 2 * set + (cq >> 1));
+            ++staged;
+          } else {
+            // Four swizzled 16-byte DSMEM stores into the P slot, once the A
+            // CTA's MMA no longer reads it.
+            ok = mbar_wait<true>(p_empty + slot, sph ^ 1u, abort_flag, p.status);
+            if (!ok) break;
+            const uint32_t dst_row = peer_p + static_cast<uint32_t>(slot) * P_SLOT +
+                                     static_cast<uint32_t>(cq >> 1) * CHUNK + static_cast<uint32_t>(m) * 128u;
+            const uint32_t pfull_slot = peer_pfull + static_cast<uint32_t>(slot) * 8u;
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+              const uint32_t unit = static_cast<uint32_t>((cq & 1) * 4 + v);
+              const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
+              st_async_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3], pfull_slot);
+            }
+            if (++slot == C::NPS) {
+              slot = 0;
+              sph ^= 1u;
+            }
           }
         }
         if (MODE == FD) {
@@ -778,7 +875,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = mbar_wait<true>(rd_empty, static_cast<uint32_t>(fd_units - 1) & 1u, abort_flag, p.status);
             if (!ok) break;
           }
-          uint4* rec = reinterpret_cast<uint4*>(smem + Z_REC + (static_cast<uint32_t>(cq) * BM + m) * REC_BYTES);
+          uint4* rec = reinterpret_cast<uint4*>(smem + C::Z_REC + (static_cast<uint32_t>(cq) * BM + m) * REC_BYTES);
           const unsigned long long sb = static_cast<unsigned long long>(__double_as_longlong(s_acc));
           rec[0] = make_uint4(static_cast<uint32_t>(sb), static_cast<uint32_t>(sb >> 32), __float_as_uint(rec_tg.e),
                               __float_as_uint(rec_tg.om));
@@ -797,7 +894,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         int rs = 0;
         uint32_t rph = 0;
         bool ok = true;
-        uint32_t pend = 0, pend_ph[ASLOTS] = {};
+        uint32_t pend = 0, pend_ph[C::ASLOTS] = {};
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
@@ -808,10 +905,10 @@ __global__ void __launch_bounds__(THREADS, 1)
               ok = mbar_wait(ay_empty + rs, rph ^ 1u, abort_flag, p.status);
               if (!ok) break;
               mbar_expect_tx(ay_full + rs, p.KC * SLAB_CHUNK);
-              tma_load_3d(smem + A_Y + rs * p.KC * SLAB_CHUNK, &tm_ys, ay_full + rs, 0, t * BT + sl * SLAB_ROWS, 0);
+              tma_load_3d(smem + C::A_Y + rs * p.KC * SLAB_CHUNK, &tm_ys, ay_full + rs, 0, t * BT + sl * SLAB_ROWS, 0);
               pend |= 1u << rs;
               pend_ph[rs] = rph;
-              if (++rs == ASLOTS) {
+              if (++rs == C::ASLOTS) {
                 rs = 0;
                 rph ^= 1u;
               }
@@ -820,7 +917,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         if (!ok) {
           const long long c0 = clock64();
-          for (int s = 0; s < ASLOTS; ++s)
+          for (int s = 0; s < C::ASLOTS; ++s)
             if (pend & (1u << s))
               while (!mbar_try_wait(smem_u32(ay_full + s), pend_ph[s]) && clock64() - c0 < kWaitLimitCycles) {
               }
@@ -838,7 +935,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         const uint32_t idesc_h1 = idesc_bf16_f32(128, 64 * (nh1 > 0 ? nh1 : 1), false, true);
         // Each P slot completes when all its bytes (st.async from the Z CTA)
         // have landed: arm every slot for its first use.
-        for (int i = 0; i < NPS; ++i) mbar_expect_tx(p_full + i, P_SLOT);
+        for (int i = 0; i < C::NPS; ++i) mbar_expect_tx(p_full + i, P_SLOT);
         for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
           int blk, t0, t1;
           unit_range(p, u, blk, t0, t1);
@@ -854,7 +951,7 @@ __global__ void __launch_bounds__(THREADS, 1)
             mbar_expect_tx(p_full + slot, P_SLOT);  // arm the slot's next use
             fence_proxy_async_smem();
             tc_fence_after();
-            const uint64_t pdesc = sdesc_sw128(smem_u32(smem + A_P + slot * P_SLOT), 16, 1024);
+            const uint64_t pdesc = sdesc_sw128(smem_u32(smem + C::A_P + slot * P_SLOT), 16, 1024);
             for (int sl = 0; sl < NSLAB && ok; ++sl) {
               ok = mbar_wait(ay_full + rs, rph, abort_flag, p.status);
               if (!ok) break;
@@ -862,7 +959,7 @@ __global__ void __launch_bounds__(THREADS, 1)
               // The slab's two K steps of 16 rows (2 KB apart); P: chunk sl / 2,
               // K columns 32 (sl % 2) + 16 kk (32 bytes per step).  MN-major B:
               // N = 64 nh columns of d in chunks 4 KB apart inside the slab.
-              const uint64_t bd0 = sdesc_sw128(smem_u32(smem + A_Y + rs * p.KC * SLAB_CHUNK), SLAB_CHUNK, 1024);
+              const uint64_t bd0 = sdesc_sw128(smem_u32(smem + C::A_Y + rs * p.KC * SLAB_CHUNK), SLAB_CHUNK, 1024);
               const uint64_t ad0 = pdesc + static_cast<uint64_t>(((sl >> 1) * CHUNK + (sl & 1) * 64) >> 4);
 #pragma unroll
               for (int kk = 0; kk < SLAB_ROWS / 16; ++kk) {
@@ -875,14 +972,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                             bd + static_cast<uint64_t>((nh0 * SLAB_CHUNK) >> 4), idesc_h1, accf);
               }
               umma_commit(ay_empty + rs);
-              if (++rs == ASLOTS) {
+              if (++rs == C::ASLOTS) {
                 rs = 0;
                 rph ^= 1u;
               }
             }
             if (!ok) break;
             umma_commit_mc(p_empty + slot, static_cast<uint16_t>(1u << 0));  // P slot free (Z CTA)
-            if (++slot == NPS) {
+            if (++slot == C::NPS) {
               slot = 0;
               sph ^= 1u;
             }
@@ -894,6 +991,32 @@ __global__ void __launch_bounds__(THREADS, 1)
         while (!mbar_try_wait(smem_u32(mma_done), 0) && clock64() - c0 < kWaitLimitCycles) {
         }
       }
+    } else if (warp == FWD_WARP) {
+      if constexpr (C::kBulk) {
+       if (lane == 0) {
+        // ---- P acknowledgements: each tile's bytes have landed ----
+        // The Z CTA's staging copy is free once the bulk copies into the P
+        // slot have completed; the slots are visited in the MMA warp's order.
+        const uint32_t z_stg_empty = mapa_shared(smem_u32(stg_empty), 0);
+        int slot = 0, n = 0;
+        uint32_t sph = 0;
+        bool ok = true;
+        for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
+          int blk, t0, t1;
+          unit_range(p, u, blk, t0, t1);
+          for (int i = 0; i < t1 - t0 && ok; ++i) {
+            ok = mbar_wait<true>(p_full + slot, sph, abort_flag, p.status);
+            if (!ok) break;
+            mbar_arrive_cluster(z_stg_empty + static_cast<uint32_t>(n % C::NSTG) * 8u);
+            ++n;
+            if (++slot == C::NPS) {
+              slot = 0;
+              sph ^= 1u;
+            }
+          }
+        }
+       }
+      }
     } else {
       // ---- A drain: accumulator -> dh / dW ----
       // Warp w drains TMEM lanes 32 (w % 4) .. +31 and the 32-column chunks
@@ -903,7 +1026,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int m = q * 32 + lane;
       constexpr int NPART = EPI_WARPS / 4;
       uint32_t fph = 0, rph = 0;
-      const uint32_t z_rec = mapa_shared(smem_u32(smem + Z_REC), 0);
+      const uint32_t z_rec = mapa_shared(smem_u32(smem + C::Z_REC), 0);
       const uint32_t z_rd_empty = mapa_shared(smem_u32(rd_empty), 0);
       for (int u = cluster; u < p.n_units; u += n_clusters) {
         int blk, t0, t1;
@@ -1107,11 +1230,11 @@ inline size_t scratch_bytes(long long N, long long V, long long d) {
 }
 
 inline int setup_attributes() {
-  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+  cudaError_t e = cudaFuncSetAttribute(bwd_kernel<DH>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<DH>::SMEM_BYTES);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(bwd_kernel<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(bwd_kernel<DW>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<DW>::SMEM_BYTES);
   if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(bwd_kernel<FD>, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    e = cudaFuncSetAttribute(bwd_kernel<FD>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<FD>::SMEM_BYTES);
   if (e != cudaSuccess) {
     set_last_error(std::string("cudaFuncSetAttribute(bwd): ") + cudaGetErrorString(e));
     return 3;
@@ -1119,14 +1242,15 @@ inline int setup_attributes() {
   return 0;
 }
 
-// Co-resident 2-CTA clusters for this kernel (cached per process).
+// Co-resident 2-CTA clusters for this kernel (cached per process), for the
+// mode with the most shared memory (every mode runs one CTA per SM).
 inline int max_clusters(int sms) {
   static int cached = 0;
   if (cached) return cached;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2));
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<FD>::SMEM_BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -1135,7 +1259,7 @@ inline int max_clusters(int sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, bwd_kernel<DH>, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, bwd_kernel<FD>, &cfg) != cudaSuccess || n <= 0) {
     (void)cudaGetLastError();
     n = sms / 2;
   }
@@ -1149,7 +1273,7 @@ inline int launch_mode(const CUtensorMap& tx, const CUtensorMap& ty, const CUten
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * clusters);
   cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Cfg<MODE>::SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;

@@ -308,6 +308,19 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
                "r"(a), "r"(b), "r"(c), "r"(d), "r"(mbar)
                : "memory");
 }
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+// Bulk copy of `bytes` (a multiple of 16, both addresses 16-byte aligned)
+// from this CTA's shared memory (`src`) to shared::cluster address `dst` in
+// another CTA of the cluster; performs complete_tx(bytes) on the mbarrier at
+// shared::cluster address `mbar` in that CTA once the data has landed.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes, uint32_t mbar) {
+  asm volatile("cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   dst),
+               "r"(src), "r"(bytes), "r"(mbar)
+               : "memory");
+}
 // 16-byte load from shared::cluster address `addr` (possibly another CTA's).
 __device__ __forceinline__ uint4 ld_cluster_v4(uint32_t addr) {
   uint4 v;
