@@ -87,19 +87,22 @@ constexpr int FL_LIVE = 1, FL_TVALID = 2, FL_HIT = 4;
 // Shared-memory plan of a mode.  The Z CTA holds the ring of Y stages (X is
 // in TMEM); the A CTA holds a ring of Y slabs and the P slots.  P tiles reach
 // the A CTA in one of two ways:
-//  * FD: each epilogue thread stores its 64 bytes straight into the P slot
-//    with st.async (the FD epilogue is light, and the stores overlap it);
-//  * DH, DW: the epilogue writes the tile into a local staging copy and the
+//  * FD, DH: each epilogue thread stores its 64 bytes straight into the P
+//    slot with st.async (these epilogues hold the row's data in registers and
+//    are light, so the stores overlap them);
+//  * DW: the epilogue writes the tile into a local staging copy and the
 //    forwarder warp sends each 16 KB column chunk with one bulk DSMEM copy
-//    (their epilogues are heavier, and 2048 DSMEM stores per tile slow them).
+//    (its epilogue, which broadcasts per-column data, is heavier, and 2048
+//    DSMEM stores per tile slow it).
 // Deep P buffering decouples the Z epilogue from the A CTA's MMAs; half a
 // tile of Y slabs in flight is enough.  Measured at N=65536, V=8192, d=512
 // (ms per pass): FD, st.async, 3 x 64 KB ring, 5 P slots: 1.044 (bulk copies
 // with 2 staging copies: 1.101); DW, bulk, 2 x 64 KB ring, 2 staging copies,
-// 4 P slots: 1.078 (st.async with 5 P slots: 1.273).
+// 4 P slots: 1.078 (st.async with 5 P slots: 1.273); DH (dh only): st.async
+// 0.983, bulk 1.025.
 template <int MODE>
 struct Cfg {
-  static constexpr bool kBulk = MODE != FD;
+  static constexpr bool kBulk = MODE == DW;
   static constexpr int YSTAGES = kBulk ? 2 : 3;  // Z ring stages (64 KB)
   static constexpr int NSTG = kBulk ? 2 : 0;     // Z: P staging copies
   static constexpr int ASLOTS = 2;               // A: Y slab slots (32 KB)
