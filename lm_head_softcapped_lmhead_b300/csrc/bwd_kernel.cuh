@@ -15,9 +15,11 @@
 //    operand Y in 128-row tiles through a ring of 64 KB TMA loads, computes
 //    z = X Y^T (tcgen05, A from TMEM, M=128 N=128, double-buffered in TMEM),
 //    and its 16 epilogue warps (one 32-column chunk each per tile) turn each
-//    z tile into the bf16 tile P = -G (DH) or -G^T (DW); P is stored
-//    straight into the peer CTA's shared memory (DSMEM, st.async), in the
-//    128B-swizzled K-major layout the MMA reads.
+//    z tile into the bf16 tile P = -G (DH) or -G^T (DW) in the 128B-swizzled
+//    K-major layout the A CTA's MMA reads.  P reaches the peer CTA's shared
+//    memory (DSMEM) by st.async from the epilogue warps (FD, DH), or (DW)
+//    through a local staging copy that a forwarder warp sends in two bulk
+//    copies per tile.
 //  * rank 1, the A CTA: loads the same Y tile in 32-row slabs (as the
 //    MN-major B operand) and accumulates acc (128 x d fp32, all 512 TMEM
 //    columns) += P Y with tcgen05 M=128 N=d/2; after the last tile its 16
