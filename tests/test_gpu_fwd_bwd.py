@@ -161,3 +161,28 @@ def test_fwd_bwd_deterministic(lm):
     r2 = run_train(lm, d_inp, 30.0, 1 / 2048)
     for a, b in zip(r1[1:], r2[1:]):
         assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("c", [30.0, 70.0])
+def test_fwd_bwd_strided_h_and_dh(lm, oracle_mod, c):
+    """h and dh as views into wider buffers (row stride 320 for d = 256):
+    both passes read h and write dh with the caller's row stride, and the
+    columns past d of dh's buffer are left as they were.  c = 70 takes the
+    forward + dh route."""
+    N, V, d, ld = 300, 700, 256, 320
+    inp = si.make_inputs(2, N=N, V=V, d=d)
+    d_inp = dev_inputs(inp)
+    wide = torch.zeros((N, ld), dtype=torch.bfloat16, device="cuda")
+    wide[:, :d] = d_inp["h"]
+    h = wide[:, :d]
+    dwide = torch.full((N, ld), 7.0, dtype=torch.bfloat16, device="cuda")
+    dh = dwide[:, :d]
+    nll = torch.full((N,), float("nan"), device="cuda")
+    lse = torch.full((N,), float("nan"), device="cuda")
+    dW = torch.full((V, d), float("nan"), device="cuda")
+    ws = lm.workspace(N, V, d)
+    w = 1.0 / N
+    lm.lmhead_ce_fwd_bwd(h, d_inp["W"], d_inp["tgt"], c, w, nll, lse, dh=dh, dW=dW, ws=ws)
+    assert lm.lmce_status(ws) == lm.LMCE_OK
+    assert torch.all(dwide[:, d:] == 7.0)
+    check_against_oracle(oracle_mod, inp, c, w, nll, lse, dh.contiguous(), dW)
