@@ -186,3 +186,33 @@ def test_fwd_bwd_strided_h_and_dh(lm, oracle_mod, c):
     assert lm.lmce_status(ws) == lm.LMCE_OK
     assert torch.all(dwide[:, d:] == 7.0)
     check_against_oracle(oracle_mod, inp, c, w, nll, lse, dh.contiguous(), dW)
+
+
+@pytest.mark.parametrize("N,V,d", [
+    (1, 1, 64),        # one row, one class: nll = 0 and every gradient is 0
+    (1, 3000, 512),    # a single row against a ragged vocabulary
+    (2000, 1, 128),    # one class, many rows
+    (3, 2, 64),        # tiny in every dimension
+])
+def test_fwd_bwd_degenerate_shapes(lm, oracle_mod, N, V, d):
+    inp = si.make_inputs(2, N=N, V=V, d=d)
+    w = 1.0 / N
+    st, nll, lse, dh, dW = run_train(lm, dev_inputs(inp), 30.0, w)
+    assert st == lm.LMCE_OK
+    check_against_oracle(oracle_mod, inp, 30.0, w, nll, lse, dh, dW)
+    if V == 1:
+        assert torch.all(nll == 0)
+        assert torch.all(dh.float() == 0) and torch.all(dW == 0)
+
+
+def test_fwd_bwd_all_rows_masked(lm):
+    """No scored row: nll, lse and dh are 0 and dW is left as it was."""
+    N, V, d = 300, 500, 128
+    inp = si.make_inputs(2, N=N, V=V, d=d)
+    init = torch.randn(V, d, device="cuda")
+    mask = torch.zeros(N, dtype=torch.uint8, device="cuda")
+    st, nll, lse, dh, dW = run_train(lm, dev_inputs(inp), 30.0, 0.0, mask=mask, dW_init=init)
+    assert st == lm.LMCE_OK
+    assert torch.all(nll == 0) and torch.all(lse == 0)
+    assert torch.all(dh.float() == 0)
+    assert torch.equal(dW, init)
