@@ -21,6 +21,11 @@ Functions and the passages they follow (page title, section):
   Parameter Golf", section "Training loop": bf16 mixed-precision training).
 * :func:`dequant_int4` -- per-group int4 head ("HYDRA Golf" stack list:
   "per-group compression" of int4 weights), symmetric, group 64, fp16 scales.
+* :func:`embed_bwd` -- the tied table's gradient through the input embedding:
+  each position's embedding gradient is added to its token's row ("[AGENT
+  TASK] OpenAI Parameter Golf", architecture experiments table, row "Tied
+  embeddings": input/output embedding sharing; "parameter-golf README",
+  leaderboard row "Naive Baseline": TiedEmbeddings).
 
 Parity pins for every function live in ``tests/test_oracle_pins.py``.
 """
@@ -68,6 +73,8 @@ def _load():
         lib.oracle_bpb.restype = ctypes.c_double
         lib.oracle_dequant_int4.argtypes = [P, P, I64, I64, I64, P]
         lib.oracle_dequant_int4.restype = ctypes.c_int
+        lib.oracle_embed_bwd_f64.argtypes = [P, P, I64, I64, I64, P]
+        lib.oracle_embed_bwd_f64.restype = ctypes.c_int
         lib.oracle_bf16_to_f64_array.argtypes = [P, P, I64]
         lib.oracle_bf16_to_f64_array.restype = None
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
@@ -200,4 +207,17 @@ def dequant_int4(Wq, scales_f16_bits, d, group=64):
     rc = _load().oracle_dequant_int4(_ptr(Wq), _ptr(sc), V, d, group, _ptr(out))
     if rc != 0:
         raise OracleError(f"oracle_dequant_int4 returned {rc}")
+    return out
+
+
+def embed_bwd(ids, g, V):
+    """[V, d] float64: out[ids[i]] += g[i] for every row i, in row order, from
+    zeros.  g: [N, d] float64 or bf16 bits; ids: [N] int64 in [0, V)."""
+    g = _as_f64(g)
+    ids = _c(ids, np.int64)
+    N, d = g.shape
+    out = np.zeros((V, d), dtype=np.float64)
+    rc = _load().oracle_embed_bwd_f64(_ptr(ids), _ptr(g), N, V, d, _ptr(out))
+    if rc != 0:
+        raise OracleError(f"oracle_embed_bwd_f64 returned {rc}")
     return out

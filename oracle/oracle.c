@@ -318,6 +318,27 @@ int oracle_dequant_int4(const uint8_t* Wq, const uint16_t* scales, int64_t V,
   return ORACLE_OK;
 }
 
+/* ---- gradient of the tied table through the input embedding ----------- */
+
+/* With tied embeddings the table W is both the output head and the input
+ * embedding, so its gradient also receives, for every input position i, the
+ * gradient g_i of the loss with respect to that position's embedding row:
+ *   out[ids[i], :] += g[i, :]   for i = 0 .. N-1, in row order.
+ * out: [V, d] doubles, added to (the caller zero-fills it for the sum alone).
+ * Returns ORACLE_EDATA, with out untouched, if an id is outside [0, V). */
+int oracle_embed_bwd_f64(const int64_t* ids, const double* g, int64_t N,
+                         int64_t V, int64_t d, double* out) {
+  if (!ids || !g || !out || N < 0 || V <= 0 || d <= 0) return ORACLE_EINVAL;
+  for (int64_t i = 0; i < N; ++i)
+    if (ids[i] < 0 || ids[i] >= V) return ORACLE_EDATA;
+  for (int64_t i = 0; i < N; ++i) {
+    double* row = out + ids[i] * d;
+    const double* gi = g + i * d;
+    for (int64_t k = 0; k < d; ++k) row[k] += gi[k];
+  }
+  return ORACLE_OK;
+}
+
 int oracle_num_threads(void) {
 #ifdef _OPENMP
   return omp_get_max_threads();

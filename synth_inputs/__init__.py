@@ -146,3 +146,16 @@ def make_inputs(cfg: int, seed: int | None = None, N: int | None = None,
     if spec.get("int4"):
         out["Wq"], out["scales"] = quantize_int4_rtn(out["W"], INT4_GROUP)
     return out
+
+
+def make_embed_inputs(N: int = 65536, V: int = 8192, d: int = D_MODEL, seed: int = 2001,
+                      g_scale: float = 1e-2) -> dict:
+    """Seeded inputs of the tied table's input-embedding gradient: the
+    positions' token ids (Zipf(1.1) over the vocabulary, like the targets)
+    and the loss gradient with respect to each position's embedding row
+    (N(0, g_scale^2), rounded to bf16).  Returns ids (int64 [N]) and g
+    (uint16 bf16 bits [N, d])."""
+    rng_i, rng_g = [np.random.Generator(np.random.PCG64(s)) for s in np.random.SeedSequence(seed).spawn(2)]
+    ids = zipf_ids(rng_i, N, V, 1.1)
+    g = rng_g.standard_normal((N, d), dtype=np.float32) * np.float32(g_scale)
+    return dict(ids=ids, g=f32_to_bf16_bits(g), N=N, V=V, d=d)

@@ -316,3 +316,54 @@ def test_golden_fixtures(oracle_mod):
         assert np.allclose(nll, case["nll"], rtol=0, atol=1e-12)
         b, *_ = oracle_mod.bpb(nll, inp["nbytes"])
         assert b == pytest.approx(case["bpb"], rel=1e-13)
+
+
+# ---- tied table gradient through the input embedding ----------------------
+
+def test_embed_bwd_permutation_places_rows(oracle_mod):
+    """Ids forming a permutation put every gradient row, unchanged, in its
+    token's row (catches indexing by position instead of by id)."""
+    rng = np.random.default_rng(11)
+    V, d = 37, 8
+    ids = rng.permutation(V)
+    g = rng.standard_normal((V, d))
+    out = oracle_mod.embed_bwd(ids, g, V)
+    assert np.array_equal(out[ids], g)
+
+
+def test_embed_bwd_single_id_closed_form(oracle_mod):
+    """All N rows on one id, row i = i * e_k: that token's row is
+    N (N - 1) / 2 at component k and 0 elsewhere; every other row is 0
+    (catches a dropped first or last row)."""
+    N, V, d, k, v = 101, 5, 6, 2, 3
+    g = np.zeros((N, d))
+    g[:, k] = np.arange(N)
+    out = oracle_mod.embed_bwd(np.full(N, v), g, V)
+    want = np.zeros((V, d))
+    want[v, k] = N * (N - 1) / 2
+    assert np.array_equal(out, want)
+
+
+def test_embed_bwd_invariants(oracle_mod):
+    """Integer-valued rows (sums exact in fp64): reordering rows together
+    with their ids changes nothing, the total over the table equals the total
+    over the rows, and tokens that never occur get zero rows (catches rows
+    added to the wrong token or lost)."""
+    rng = np.random.default_rng(12)
+    N, V, d = 500, 40, 16
+    ids = si.zipf_ids(rng, N, V - 5, 1.1)  # the last 5 ids never occur
+    g = rng.integers(-50, 51, size=(N, d)).astype(np.float64)
+    out = oracle_mod.embed_bwd(ids, g, V)
+    perm = rng.permutation(N)
+    assert np.array_equal(oracle_mod.embed_bwd(ids[perm], g[perm], V), out)
+    assert np.array_equal(out.sum(axis=0), g.sum(axis=0))
+    assert np.all(out[V - 5:] == 0)
+    counts = np.bincount(ids, minlength=V)
+    assert np.array_equal(out[:, 0] != 0, (out[:, 0] != 0) & (counts > 0))
+
+
+def test_embed_bwd_rejects_out_of_range_id(oracle_mod):
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.embed_bwd(np.array([0, 3]), np.ones((2, 4)), 3)
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.embed_bwd(np.array([-1]), np.ones((1, 4)), 3)
