@@ -537,6 +537,28 @@ def run_table(args):
         tf = lambda k: k * M * V * d / (ms * 1e-3) / 1e12 / peak  # noqa: E731
         rows.append((cfg, what, N, V, M / ms * 1e3, ms, tf(exec_f), tf(model_f), o_rate, S))
         del inp
+    # The tied table's gradient through the input embedding (HBM-bound):
+    # the training micro-batch's input positions, Zipf token ids.
+    e = si.make_embed_inputs()
+    eN, eV, ed = e["N"], e["V"], e["d"]
+    e_ids = torch.from_numpy(e["ids"]).to(dev)
+    e_g = bf(e["g"])
+    e_dW = torch.zeros((eV, ed), device=dev)
+    e_ws = lm.workspace(eN, eV, ed, lm.LMCE_WS_EMBED, device=dev)
+    e_ms = gpu_ms(lambda: lm.lmhead_tied_embed_bwd(e_ids, e_g, e_dW, ws=e_ws, stream=stream))
+    if lm.lmce_status(e_ws) != lm.LMCE_OK:
+        raise RuntimeError("tied-embedding gradient: device status not OK")
+    touched = int(np.count_nonzero(np.bincount(e["ids"], minlength=eV)))
+    e_bytes = eN * ed * 2 + eN * 8 + 2 * touched * ed * 4
+    g64 = oracle.widen_bf16(e["g"])
+    t0 = time.perf_counter()
+    oracle.embed_bwd(e["ids"], g64, eV)
+    o_s = time.perf_counter() - t0
+    hbm = measured_peaks()[2]
+    notes.append(f"tied-embedding gradient (N={eN}, V={eV}, d={ed}, Zipf ids, {touched} tokens touched): "
+                 f"{e_ms:.4f} ms, {eN / e_ms / 1e3:.2f} M tokens/s, {e_bytes / 1e6:.1f} MB algorithmic, "
+                 f"{e_bytes / (e_ms * 1e-3) / 1e9:.0f} GB/s = {e_bytes / (e_ms * 1e-3) / 1e9 / hbm:.3f} of the "
+                 f"measured {hbm:.0f} GB/s; oracle {eN / o_s:.0f} tokens/s (all {eN} rows)")
     print(f"bf16 peak {peak} TFLOP/s ({measured_peaks()[3]}); oracle threads {oracle.num_threads()}")
     print("| Workload | Call | GPU tokens/s | GPU ms per call | executed FLOPs / peak | model FLOPs / peak "
           "| Oracle tokens/s (sample rows) |")

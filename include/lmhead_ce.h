@@ -81,6 +81,7 @@ enum lmce_status_code {
 /* Workspace flags. */
 #define LMCE_WS_MASKED 1u /* room for row-mask compaction (masked forward) */
 #define LMCE_WS_INT4 2u   /* room for the dequantised bf16 copy of an int4 head */
+#define LMCE_WS_EMBED 4u  /* room for lmhead_tied_embed_bwd (counting sort, piece sums) */
 
 /* Accumulator of the bits-per-byte sums (device memory for bpb_reduce). */
 typedef struct lmce_bpb_acc {
@@ -178,6 +179,24 @@ LMCE_API int lmhead_ce_fwd_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8
                            int group, int64_t N, int64_t V, int64_t d, const int64_t* tgt,
                            const uint8_t* row_mask, float softcap, float grad_scale, float* nll, float* lse,
                            lmce_bf16* dh, void* ws, size_t ws_bytes, void* stream);
+
+/* Gradient of the tied table through the input embedding.  With tied
+ * embeddings W is also the input embedding table ("[AGENT TASK] OpenAI
+ * Parameter Golf", architecture experiments table, row "Tied embeddings";
+ * "parameter-golf README", leaderboard row "Naive Baseline":
+ * TiedEmbeddings), so the table's gradient is the head's dW (from
+ * lmhead_ce_bwd or lmhead_ce_fwd_bwd) plus, for every input position i, the
+ * gradient g_i of the loss with respect to that position's embedding row:
+ *   dW[ids[i], :] += g[i, :]   for i = 0 .. N-1.
+ * Inputs: ids [N] int64 (the input tokens), g [N, d] bf16 with row stride
+ * ldg elements (ldg % 8 == 0, 16-byte aligned).  dW [V, d] fp32 is added to.
+ * Deterministic: each token's rows are summed in row order in fp32 (in
+ * pieces of at most 64 rows, added in order), then added to dW once.  A row
+ * whose id is outside [0, V) is skipped and sets LMCE_EDATA in the status
+ * word.  Needs a workspace sized with LMCE_WS_EMBED; d as for the head
+ * (a multiple of 64, at most 512). */
+LMCE_API int lmhead_tied_embed_bwd(const int64_t* ids, const lmce_bf16* g, int64_t ldg, int64_t N, int64_t V,
+                          int64_t d, float* dW, void* ws, size_t ws_bytes, void* stream);
 
 /* Bits-per-byte sums (tproger news, "Rules and metric").  Adds, over rows with
  * row_mask != 0 (all rows if NULL), sum nll (fp64), sum bytes and the row

@@ -25,12 +25,13 @@ LIB_PATH = os.path.join(_HERE, "liblmhead_ce.so")
 LMCE_OK, LMCE_EINVAL, LMCE_ENOTSUP, LMCE_ECUDA, LMCE_EDATA, LMCE_ETIMEOUT = range(6)
 LMCE_WS_MASKED = 1
 LMCE_WS_INT4 = 2
+LMCE_WS_EMBED = 4
 
 EXPORTS = (
     "lmce_workspace_bytes", "lmce_workspace_init", "lmce_softcap_max", "lmhead_ce_fwd", "lmhead_ce_bwd",
     "lmhead_ce_fwd_int4", "lmhead_ce_bwd_int4", "bpb_reduce", "lmce_bpb", "lmhead_int4_dequant",
     "lmce_status", "lmce_last_cuda_error", "lmce_strerror", "lmce_launch_count", "lmhead_ce_fwd_noalloc",
-    "lmhead_ce_fwd_bwd", "lmhead_ce_fwd_bwd_int4",
+    "lmhead_ce_fwd_bwd", "lmhead_ce_fwd_bwd_int4", "lmhead_tied_embed_bwd",
 )
 
 _lib = None
@@ -70,6 +71,7 @@ def lib():
             "lmhead_ce_bwd_int4": ([P, I64, P, P, I, I64, I64, I64, P, P, F, P, P, F, P, P, SZ, P], I),
             "lmhead_ce_fwd_bwd_int4": ([P, I64, P, P, I, I64, I64, I64, P, P, F, F, P, P, P, P, SZ, P], I),
             "bpb_reduce": ([P, P, P, I64, P, P, SZ, P], I),
+            "lmhead_tied_embed_bwd": ([P, P, I64, I64, I64, I64, P, P, SZ, P], I),
             "lmce_bpb": ([ctypes.POINTER(_BpbAcc), ctypes.POINTER(ctypes.c_double)], I),
             "lmhead_int4_dequant": ([P, P, I64, I64, I, P, P], I),
             "lmce_status": ([P, P, ctypes.POINTER(ctypes.c_int)], I),
@@ -209,6 +211,19 @@ def lmhead_ce_fwd_bwd_int4(h, Wq, scales, group, softcap, tgt, grad_scale, nll, 
                                       _p(row_mask), float(softcap), float(grad_scale), _p(nll), _p(lse), _p(dh),
                                       _p(ws), ws.numel(), _stream(stream))
     _check(rc, "lmhead_ce_fwd_bwd_int4")
+
+
+def lmhead_tied_embed_bwd(ids, g, dW, ws=None, stream=None):
+    """dW[ids[i]] += g[i] for every row i (the tied table's gradient through
+    the input embedding).  ids [N] int64, g [N, d] bf16, dW [V, d] fp32."""
+    _bf16_bits(g, "g")
+    N, d = g.shape
+    V = dW.shape[0]
+    if dW.dtype != torch.float32 or dW.dim() != 2 or dW.shape[1] != d or not dW.is_contiguous():
+        raise ValueError("dW must be a contiguous [V, d] float32 tensor")
+    rc = lib().lmhead_tied_embed_bwd(_p(ids), _p(g), g.stride(0), N, V, d, _p(dW), _p(ws), ws.numel(),
+                                     _stream(stream))
+    _check(rc, "lmhead_tied_embed_bwd")
 
 
 def bpb_acc(device="cuda") -> torch.Tensor:

@@ -16,6 +16,7 @@
 #include "../../include/lmhead_ce.h"
 #include "aux_kernels.cuh"
 #include "bwd_kernel.cuh"
+#include "embed_kernels.cuh"
 #include "fwd_kernel.cuh"
 
 namespace {
@@ -44,6 +45,7 @@ struct Layout {
   size_t tgt_c = 0;     // masked: [N] int64 compacted targets
   size_t h_c = 0;       // masked: [N, d] bf16 compacted rows
   size_t wdeq = 0;      // int4: [V, d] bf16 dequantised head
+  size_t embed = 0;     // tied-embedding gradient: counting sort and piece sums
   size_t bwd = 0;       // backward scratch
   size_t total = 0;
 };
@@ -76,6 +78,10 @@ Layout make_layout(int64_t N, int64_t V, int64_t d, unsigned flags) {
   if (flags & LMCE_WS_INT4) {
     L.wdeq = o;
     o = up(o + 2 * V * d);
+  }
+  if (flags & LMCE_WS_EMBED) {
+    L.embed = o;
+    o = up(o + lmce::embk::layout(N, V, d).total);
   }
   L.bwd = o;
   o = up(o + lmce::bwdk::scratch_bytes(N, V, d));
@@ -514,6 +520,48 @@ int lmhead_int4_dequant(const uint8_t* Wq, const lmce_f16* scales, int64_t V, in
   DevInfo di;
   if (int rc = dev_info(&di); rc) return rc;
   return dequant_impl(Wq, scales, V, d, group, out, static_cast<cudaStream_t>(stream), di.sms);
+}
+
+int lmhead_tied_embed_bwd(const int64_t* ids, const lmce_bf16* g, int64_t ldg, int64_t N, int64_t V, int64_t d,
+                          float* dW, void* ws, size_t ws_bytes, void* stream) {
+  if (!ids || !g || !dW || !ws) return LMCE_EINVAL;
+  if (N < 1 || V < 1 || d < 1) return LMCE_EINVAL;
+  if (N > (int64_t(1) << 30) || V > (int64_t(1) << 30)) return LMCE_EINVAL;
+  if (d % 64 != 0 || d > 512) return LMCE_ENOTSUP;
+  if (ldg < d || ldg % 8 != 0) return LMCE_EINVAL;
+  if (!aligned16(g) || !aligned16(dW) || !aligned16(ws)) return LMCE_EINVAL;
+  const Layout L = make_layout(N, V, d, LMCE_WS_EMBED);
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  namespace ek = lmce::embk;
+  const ek::Layout E = ek::layout(N, V, d);
+  char* w = static_cast<char*>(ws);
+  char* e = w + L.embed;
+  unsigned* status = reinterpret_cast<unsigned*>(w + L.status);
+  int* hist = reinterpret_cast<int*>(e + E.hist);
+  int* offs = reinterpret_cast<int*>(e + E.offs);
+  int* pbase = reinterpret_cast<int*>(e + E.pbase);
+  int* perm = reinterpret_cast<int*>(e + E.perm);
+  float* part = reinterpret_cast<float*>(e + E.part);
+  const int R = static_cast<int>(ek::chunk_rows(N)), C = static_cast<int>(ek::n_chunks(N));
+  const int n = static_cast<int>(N), v = static_cast<int>(V), dd = static_cast<int>(d);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaError_t err = cudaMemsetAsync(hist, 0, sizeof(int) * static_cast<size_t>(C) * V, s);
+  if (err != cudaSuccess) return cuda_fail(err, "tied_embed memset");
+  const int vblocks = static_cast<int>(std::min<int64_t>(cdiv(V, 256), int64_t(di.sms) * 4));
+  lmce::count_launches(7);
+  ek::count_kernel<<<C, 256, 0, s>>>(ids, n, v, R, hist, status);
+  ek::totals_kernel<<<vblocks, 256, 0, s>>>(hist, C, v, offs, pbase);
+  ek::scan_kernel<<<1, 1024, 0, s>>>(offs, pbase, v);
+  ek::bases_kernel<<<vblocks, 256, 0, s>>>(hist, C, v, offs);
+  ek::place_kernel<<<static_cast<int>(cdiv(C, 8)), 256, 0, s>>>(ids, n, v, R, C, hist, perm);
+  ek::pieces_kernel<<<di.sms * 8, 256, 0, s>>>(g, ldg, dd, v, offs, pbase, perm, part);
+  ek::combine_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(V, 8), int64_t(di.sms) * 8)), 256, 0, s>>>(
+      part, pbase, v, dd, dW);
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return cuda_fail(err, "tied_embed launch");
+  return LMCE_OK;
 }
 
 int lmce_status(void* ws, void* stream, int* code) {

@@ -124,6 +124,25 @@ def test_fwd_bwd_int4_host_validation(L):
     assert fb(ws_bytes=L.lmce_workspace_bytes(100, 200, 512, 0)) == EINVAL   # no room for the dequantised head
 
 
+def test_tied_embed_host_validation(L):
+    P = ctypes.c_void_p
+
+    def eb(ids=A, g=A, ldg=512, N=100, V=200, d=512, dW=A, ws_bytes=1 << 40):
+        return L.lmhead_tied_embed_bwd(P(ids), P(g), ldg, N, V, d, P(dW), P(A), ws_bytes, None)
+    assert eb(ids=0) == EINVAL
+    assert eb(g=0) == EINVAL
+    assert eb(dW=0) == EINVAL
+    assert eb(N=0) == EINVAL
+    assert eb(V=0) == EINVAL
+    assert eb(d=96) == ENOTSUP
+    assert eb(ldg=500) == EINVAL              # below d
+    assert eb(ldg=516) == EINVAL              # not a multiple of 8
+    assert eb(g=A + 2) == EINVAL              # rows read as 16-byte vectors
+    assert eb(dW=A + 4) == EINVAL
+    assert eb(ws_bytes=L.lmce_workspace_bytes(100, 200, 512, 0)) == EINVAL  # no room for the sort
+    assert L.lmce_workspace_bytes(100, 200, 512, 4) > L.lmce_workspace_bytes(100, 200, 512, 0)
+
+
 def test_bpb_reduce_validation(L):
     P = ctypes.c_void_p
     assert L.bpb_reduce(P(0), P(A), None, 10, P(A), P(A), 1 << 20, None) == EINVAL
