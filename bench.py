@@ -50,9 +50,10 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="target CPU time of the oracle sample")
     ap.add_argument("--profile", action="store_true",
                     help="for profiler captures: exactly W warm-up steps, no clock sampling, no e2e leg")
-    ap.add_argument("--profile-step", choices=["train", "fwd"], default="train",
+    ap.add_argument("--profile-step", choices=["train", "fwd", "embed"], default="train",
                     help="with --profile: the step to run; fwd = the evaluation forward (lmhead_ce_fwd + "
-                         "bpb_reduce) on the same batch")
+                         "bpb_reduce) on the same batch; embed = the tied-embedding gradient "
+                         "(lmhead_tied_embed_bwd) of the batch's input positions")
     ap.add_argument("--table", action="store_true",
                     help="instead of the JSON line: a markdown table of every workload's call throughput "
                          "(one GPU) beside the oracle's on a sample (host cores)")
@@ -159,12 +160,24 @@ def run_ours(args, rank, world, local_rank):
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
+    if args.profile_step == "embed":
+        e = si.make_embed_inputs(seed=2001 + 7919 * rank)
+        e_ids = torch.from_numpy(e["ids"]).to(dev)
+        e_g = torch.from_numpy(e["g"].view(np.int16)).view(torch.bfloat16).to(dev)
+        e_ws = lm.workspace(e["N"], e["V"], e["d"], lm.LMCE_WS_EMBED, device=dev)
+
     # One step: forward + dh in one pass, the bits-per-byte sums, then the dW
     # pass (which needs the forward's lse), each call bracketed by events.
     def step(events=None):
         ev = events or [None] * 4
         if ev[0] is not None:
             ev[0].record(stream)
+        if args.profile_step == "embed":
+            lm.lmhead_tied_embed_bwd(e_ids, e_g, dW, ws=e_ws, stream=stream)
+            for e_ev in ev[1:]:
+                if e_ev is not None:
+                    e_ev.record(stream)
+            return
         if args.profile_step == "fwd":
             lm.lmhead_ce_fwd(h, W, tgt, SOFTCAP, nll, lse, ws=ws, stream=stream)
             lm.bpb_reduce(nll, nbytes, acc, ws=ws, stream=stream)
