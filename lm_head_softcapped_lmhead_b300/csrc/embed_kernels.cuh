@@ -12,10 +12,12 @@
 // rows are summed in row order, in fp32, in pieces of at most kPieceRows rows
 // (so that a hot token's rows are summed by many warps), and the pieces of a
 // token are added in order before the one addition into dW.
-//   1. count:   per row chunk, the rows of each token (integer atomics);
-//   2. totals:  per token, its row count and its number of pieces;
+//   1. count:   per token and row chunk, the rows (integer atomics),
+//               stored token-major (hist[v][c]);
+//   2. totals:  per token (one warp), its row count and its number of pieces;
 //   3. scan:    exclusive scans of the two over the tokens (one block);
-//   4. bases:   per chunk and token, where its rows start in the sorted order;
+//   4. bases:   per token (one warp, an exclusive scan over its chunks), where
+//               each chunk's rows of it start in the sorted order;
 //   5. place:   one warp per chunk walks its rows in order and writes each row
 //               index at its token's next slot (a stable counting sort);
 //   6. pieces:  one warp per piece sums its rows (bf16 -> fp32) in order;
@@ -51,7 +53,7 @@ inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 inline Layout layout(long long N, long long V, long long d) {
   Layout L{};
   size_t o = 0;
-  L.hist = o;   // [chunks][V] int: counts, then bases, then cursors
+  L.hist = o;   // [V][chunks] int: counts, then bases, then cursors
   o = up256(o + sizeof(int) * static_cast<size_t>(n_chunks(N)) * static_cast<size_t>(V));
   L.offs = o;   // [V + 1] int: first sorted position of each token
   o = up256(o + sizeof(int) * static_cast<size_t>(V + 1));
@@ -67,8 +69,8 @@ inline Layout layout(long long N, long long V, long long d) {
 
 __device__ __forceinline__ bool id_ok(long long v, int V) { return v >= 0 && v < V; }
 
-// 1. hist[c][v] = rows of chunk c with id v.
-__global__ void count_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int* __restrict__ hist,
+// 1. hist[v][c] = rows of chunk c with id v.
+__global__ void count_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int C, int* __restrict__ hist,
                              unsigned* status) {
   const int c = blockIdx.x;
   const int i0 = c * R, i1 = min(N, i0 + R);
@@ -78,18 +80,25 @@ __global__ void count_kernel(const int64_t* __restrict__ ids, int N, int V, int 
       atomicOr(status, ST_EDATA);
       continue;
     }
-    atomicAdd(hist + static_cast<size_t>(c) * V + v, 1);
+    atomicAdd(hist + static_cast<size_t>(v) * C + c, 1);
   }
 }
 
-// 2. offs[v] = rows of token v, pbase[v] = its pieces (scanned in place next).
+// 2. offs[v] = rows of token v, pbase[v] = its pieces (scanned in place next);
+//    one warp per token.
 __global__ void totals_kernel(const int* __restrict__ hist, int C, int V, int* __restrict__ offs,
                               int* __restrict__ pbase) {
-  for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < V; v += gridDim.x * blockDim.x) {
+  const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
+  for (int v = blockIdx.x * warps + (threadIdx.x >> 5); v < V; v += gridDim.x * warps) {
+    const int* h = hist + static_cast<size_t>(v) * C;
     int t = 0;
-    for (int c = 0; c < C; ++c) t += hist[static_cast<size_t>(c) * V + v];
-    offs[v] = t;
-    pbase[v] = (t + kPieceRows - 1) / kPieceRows;
+    for (int c = lane; c < C; c += 32) t += h[c];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+    if (lane == 0) {
+      offs[v] = t;
+      pbase[v] = (t + kPieceRows - 1) / kPieceRows;
+    }
   }
 }
 
@@ -135,15 +144,24 @@ __global__ void scan_kernel(int* __restrict__ offs, int* __restrict__ pbase, int
   }
 }
 
-// 4. hist[c][v] <- offs[v] + rows of token v in chunks before c.
+// 4. hist[v][c] <- offs[v] + rows of token v in chunks before c; one warp
+//    per token, 32 chunks at a time (warp exclusive scan plus a carry).
 __global__ void bases_kernel(int* __restrict__ hist, int C, int V, const int* __restrict__ offs) {
-  for (int v = blockIdx.x * blockDim.x + threadIdx.x; v < V; v += gridDim.x * blockDim.x) {
+  const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
+  for (int v = blockIdx.x * warps + (threadIdx.x >> 5); v < V; v += gridDim.x * warps) {
+    int* h = hist + static_cast<size_t>(v) * C;
     int run = offs[v];
-    for (int c = 0; c < C; ++c) {
-      int* h = hist + static_cast<size_t>(c) * V + v;
-      const int n = *h;
-      *h = run;
-      run += n;
+    for (int c0 = 0; c0 < C; c0 += 32) {
+      const int c = c0 + lane;
+      const int n = c < C ? h[c] : 0;
+      int x = n;  // inclusive scan over the lanes
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (c < C) h[c] = run + x - n;
+      run += __shfl_sync(0xffffffffu, x, 31);
     }
   }
 }
@@ -158,7 +176,7 @@ __global__ void place_kernel(const int64_t* __restrict__ ids, int N, int V, int 
   const int lane = threadIdx.x & 31;
   if (c >= C) return;
   const int i0 = c * R, i1 = min(N, i0 + R);
-  int* hc = hist + static_cast<size_t>(c) * V;
+  int* hc = hist + c;  // hc[v * C]: this chunk's cursor of token v
   for (int b = i0; b < i1; b += 32) {
     const int i = b + lane;
     const long long v = i < i1 ? ids[i] : -1;
@@ -168,11 +186,12 @@ __global__ void place_kernel(const int64_t* __restrict__ ids, int N, int V, int 
     int slot = 0;
     if (ok) {
       const unsigned below = peers & ((1u << lane) - 1u);
-      slot = hc[v] + __popc(below);
+      slot = hc[static_cast<size_t>(v) * C] + __popc(below);
       perm[slot] = i;
     }
     __syncwarp();
-    if (ok && (peers & ((1u << lane) - 1u)) == 0u) hc[v] += __popc(peers);  // the group's lowest lane
+    if (ok && (peers & ((1u << lane) - 1u)) == 0u)  // the group's lowest lane
+      hc[static_cast<size_t>(v) * C] += __popc(peers);
     __syncwarp();
   }
 }

@@ -549,12 +549,12 @@ int lmhead_tied_embed_bwd(const int64_t* ids, const lmce_bf16* g, int64_t ldg, i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   cudaError_t err = cudaMemsetAsync(hist, 0, sizeof(int) * static_cast<size_t>(C) * V, s);
   if (err != cudaSuccess) return cuda_fail(err, "tied_embed memset");
-  const int vblocks = static_cast<int>(std::min<int64_t>(cdiv(V, 256), int64_t(di.sms) * 4));
+  const int wblocks = static_cast<int>(std::min<int64_t>(cdiv(V, 8), int64_t(di.sms) * 8));  // a warp per token
   lmce::count_launches(7);
-  ek::count_kernel<<<C, 256, 0, s>>>(ids, n, v, R, hist, status);
-  ek::totals_kernel<<<vblocks, 256, 0, s>>>(hist, C, v, offs, pbase);
+  ek::count_kernel<<<C, 256, 0, s>>>(ids, n, v, R, C, hist, status);
+  ek::totals_kernel<<<wblocks, 256, 0, s>>>(hist, C, v, offs, pbase);
   ek::scan_kernel<<<1, 1024, 0, s>>>(offs, pbase, v);
-  ek::bases_kernel<<<vblocks, 256, 0, s>>>(hist, C, v, offs);
+  ek::bases_kernel<<<wblocks, 256, 0, s>>>(hist, C, v, offs);
   ek::place_kernel<<<static_cast<int>(cdiv(C, 8)), 256, 0, s>>>(ids, n, v, R, C, hist, perm);
   ek::pieces_kernel<<<di.sms * 8, 256, 0, s>>>(g, ldg, dd, v, offs, pbase, perm, part);
   ek::combine_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(V, 8), int64_t(di.sms) * 8)), 256, 0, s>>>(
