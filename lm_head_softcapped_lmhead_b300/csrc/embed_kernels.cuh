@@ -255,31 +255,52 @@ __global__ void pieces_kernel(const uint16_t* __restrict__ g, long long ldg, int
   }
 }
 
-// 7. dW[v][:] += sum of token v's pieces, in piece order (one warp per token).
+// 7. dW[v][:] += sum of token v's pieces, in piece order (one warp per token;
+//    lane l holds the float4 groups l, l + 32, l + 64, l + 96 of a row).  The
+//    loads of several pieces are in flight at once; each element's additions
+//    stay in piece order.
 __global__ void combine_kernel(const float* __restrict__ part, const int* __restrict__ pbase, int V, int d,
                                float* __restrict__ dW) {
   const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int ng = d / 4;  // float4 groups of a row
+  const int ng = d / 4;  // float4 groups of a row (at most 128)
   for (int v = blockIdx.x * warps + (threadIdx.x >> 5); v < V; v += gridDim.x * warps) {
     const int p0 = pbase[v], p1 = pbase[v + 1];
     if (p0 == p1) continue;
-    for (int j = lane; j < ng; j += 32) {
-      float4 s = reinterpret_cast<const float4*>(part + static_cast<size_t>(p0) * d)[j];
-      for (int p = p0 + 1; p < p1; ++p) {
-        const float4 x = reinterpret_cast<const float4*>(part + static_cast<size_t>(p) * d)[j];
-        s.x += x.x;
-        s.y += x.y;
-        s.z += x.z;
-        s.w += x.w;
+    float4 s[4];
+    const float4* b0 = reinterpret_cast<const float4*>(part + static_cast<size_t>(p0) * d);
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = lane + 32 * q;
+      s[q] = j < ng ? b0[j] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+#pragma unroll 4
+    for (int p = p0 + 1; p < p1; ++p) {
+      const float4* b = reinterpret_cast<const float4*>(part + static_cast<size_t>(p) * d);
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = lane + 32 * q;
+        if (j < ng) {
+          const float4 x = b[j];
+          s[q].x += x.x;
+          s[q].y += x.y;
+          s[q].z += x.z;
+          s[q].w += x.w;
+        }
       }
-      float4* o = reinterpret_cast<float4*>(dW + static_cast<size_t>(v) * d) + j;
-      float4 a = *o;
-      a.x += s.x;
-      a.y += s.y;
-      a.z += s.z;
-      a.w += s.w;
-      *o = a;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = lane + 32 * q;
+      if (j < ng) {
+        float4* o = reinterpret_cast<float4*>(dW + static_cast<size_t>(v) * d) + j;
+        float4 a = *o;
+        a.x += s[q].x;
+        a.y += s[q].y;
+        a.z += s[q].z;
+        a.w += s[q].w;
+        *o = a;
+      }
     }
   }
 }
