@@ -21,6 +21,25 @@ Functions and the passages they follow (page title, section):
   Parameter Golf", section "Training loop": bf16 mixed-precision training).
 * :func:`dequant_int4` -- per-group int4 head ("HYDRA Golf" stack list:
   "per-group compression" of int4 weights), symmetric, group 64, fp16 scales.
+* :func:`dW_rows` -- the head's dW for listed vocabulary rows only (same
+  definition as :func:`bwd`), for sampled checks at full size.
+* :func:`bpb_lut` -- bits per byte with the byte count of each scored token
+  from a per-id table ("parameter-golf README" leaderboard rows "SP8192 +
+  CaseOps + ..." (byte-sidecar BPB accounting) and "CaseOps Tokenizer + ..."
+  (validation byte sidecars); "HYDRA Golf" submission conditions:
+  tokenizer-aware validation BPB).
+* :func:`dequant_int8_rows`, :func:`dequant_int4_asym`, :func:`dequant_f16`
+  -- more storage formats of the tied table ("parameter-golf README"
+  leaderboard rows "Mixed Quant + Sliding Window Eval" (int8 embeddings),
+  "VarLen Attention + Fused MLP + ..." (int7 embeddings), "fp16 Embed" (FP16
+  tied embedding); "HYDRA Golf" stack list: "LQER asymmetric int4,
+  per-group compression").
+* :func:`rmsnorm_fwd` / :func:`rmsnorm_bwd` -- the normalisation in front of
+  the head and its backward ("parameter-golf README" leaderboard row "11L
+  Partial RoPE + LN Scale + EMA + XSA4": layerwise LN scale; RMSNorm with an
+  optional gain).
+* A softcap of 0 means no cap (s = z) in :func:`fwd`, :func:`bwd`,
+  :func:`dh_rows` and :func:`dW_rows`.
 * :func:`embed_bwd` -- the tied table's gradient through the input embedding:
   each position's embedding gradient is added to its token's row ("[AGENT
   TASK] OpenAI Parameter Golf", architecture experiments table, row "Tied
@@ -75,6 +94,20 @@ def _load():
         lib.oracle_dequant_int4.restype = ctypes.c_int
         lib.oracle_embed_bwd_f64.argtypes = [P, P, I64, I64, I64, P]
         lib.oracle_embed_bwd_f64.restype = ctypes.c_int
+        lib.oracle_dW_rows_f64.argtypes = [P, P, I64, I64, I64, P, P, D, P, D, P, I64, P]
+        lib.oracle_dW_rows_f64.restype = ctypes.c_int
+        lib.oracle_bpb_lut.argtypes = [P, P, P, I64, P, I64, P, P, P, P]
+        lib.oracle_bpb_lut.restype = ctypes.c_double
+        lib.oracle_dequant_int8_rows.argtypes = [P, P, I64, I64, P]
+        lib.oracle_dequant_int8_rows.restype = ctypes.c_int
+        lib.oracle_dequant_int4_asym.argtypes = [P, P, P, I64, I64, I64, P]
+        lib.oracle_dequant_int4_asym.restype = ctypes.c_int
+        lib.oracle_dequant_f16.argtypes = [P, I64, P]
+        lib.oracle_dequant_f16.restype = ctypes.c_int
+        lib.oracle_rmsnorm_fwd_f64.argtypes = [P, P, D, I64, I64, P, P]
+        lib.oracle_rmsnorm_fwd_f64.restype = ctypes.c_int
+        lib.oracle_rmsnorm_bwd_f64.argtypes = [P, P, D, P, I64, I64, P, P]
+        lib.oracle_rmsnorm_bwd_f64.restype = ctypes.c_int
         lib.oracle_bf16_to_f64_array.argtypes = [P, P, I64]
         lib.oracle_bf16_to_f64_array.restype = None
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
@@ -221,3 +254,102 @@ def embed_bwd(ids, g, V):
     if rc != 0:
         raise OracleError(f"oracle_embed_bwd_f64 returned {rc}")
     return out
+
+
+def dW_rows(h, W, tgt, softcap, lse, grad_scale, vrows, mask=None):
+    """[len(vrows), d] float64: rows vrows of dW for L = grad_scale * sum nll_i
+    (lse: every row's, as from :func:`fwd`)."""
+    h = _as_f64(h)
+    W = _as_f64(W)
+    N, d = h.shape
+    V = W.shape[0]
+    tgt = _c(tgt, np.int64)
+    mask = _c(mask, np.uint8)
+    lse = _c(lse, np.float64)
+    vrows = _c(vrows, np.int64)
+    out = np.zeros((vrows.size, d), dtype=np.float64)
+    rc = _load().oracle_dW_rows_f64(_ptr(h), _ptr(W), N, V, d, _ptr(tgt), _ptr(mask), float(softcap),
+                                    _ptr(lse), float(grad_scale), _ptr(vrows), vrows.size, _ptr(out))
+    if rc != 0:
+        raise OracleError(f"oracle_dW_rows_f64 returned {rc}")
+    return out
+
+
+def bpb_lut(nll, tgt, lut, mask=None):
+    """(bpb, sum_nll, sum_bytes, n_scored) with bytes_i = lut[tgt[i]]."""
+    nll = _c(nll, np.float64)
+    tgt = _c(tgt, np.int64)
+    lut = _c(lut, np.int32)
+    mask = _c(mask, np.uint8)
+    sn = ctypes.c_double()
+    sb = ctypes.c_int64()
+    n = ctypes.c_int64()
+    err = ctypes.c_int()
+    v = _load().oracle_bpb_lut(_ptr(nll), _ptr(tgt), _ptr(lut), lut.size, _ptr(mask), nll.size,
+                               ctypes.byref(sn), ctypes.byref(sb), ctypes.byref(n), ctypes.byref(err))
+    if err.value != 0:
+        raise OracleError(f"oracle_bpb_lut: error {err.value}")
+    return float(v), float(sn.value), int(sb.value), int(n.value)
+
+
+def dequant_int8_rows(q, scales_f16_bits):
+    """bf16 bits [V, d] of round_to_bf16(q * scale_row); q int8 [V, d]."""
+    q = _c(q, np.int8)
+    sc = _c(scales_f16_bits, np.uint16)
+    V, d = q.shape
+    out = np.zeros((V, d), dtype=np.uint16)
+    rc = _load().oracle_dequant_int8_rows(_ptr(q), _ptr(sc), V, d, _ptr(out))
+    if rc != 0:
+        raise OracleError(f"oracle_dequant_int8_rows returned {rc}")
+    return out
+
+
+def dequant_int4_asym(Wq, scales_f16_bits, zeros, d, group=64):
+    """bf16 bits [V, d] of round_to_bf16((q - zero) * scale), unsigned codes."""
+    Wq = _c(Wq, np.uint8)
+    sc = _c(scales_f16_bits, np.uint16)
+    zp = _c(zeros, np.uint8)
+    V = Wq.shape[0]
+    out = np.zeros((V, d), dtype=np.uint16)
+    rc = _load().oracle_dequant_int4_asym(_ptr(Wq), _ptr(sc), _ptr(zp), V, d, group, _ptr(out))
+    if rc != 0:
+        raise OracleError(f"oracle_dequant_int4_asym returned {rc}")
+    return out
+
+
+def dequant_f16(w_f16_bits):
+    """bf16 bits of round_to_bf16(w) for fp16 bits w (any shape)."""
+    w = _c(w_f16_bits, np.uint16)
+    out = np.zeros(w.shape, dtype=np.uint16)
+    rc = _load().oracle_dequant_f16(_ptr(w), w.size, _ptr(out))
+    if rc != 0:
+        raise OracleError(f"oracle_dequant_f16 returned {rc}")
+    return out
+
+
+def rmsnorm_fwd(x, g, eps):
+    """(h [N, d], rinv [N]) float64: h = g * x / sqrt(mean(x^2) + eps);
+    x float64 or bf16 bits; g [d] or None (no gain)."""
+    x = _as_f64(x)
+    g = None if g is None else _as_f64(np.asarray(g))
+    N, d = x.shape
+    h = np.zeros((N, d), dtype=np.float64)
+    rinv = np.zeros(N, dtype=np.float64)
+    rc = _load().oracle_rmsnorm_fwd_f64(_ptr(x), _ptr(g), float(eps), N, d, _ptr(h), _ptr(rinv))
+    if rc != 0:
+        raise OracleError(f"oracle_rmsnorm_fwd_f64 returned {rc}")
+    return h, rinv
+
+
+def rmsnorm_bwd(x, g, eps, dh):
+    """(dx [N, d], dg [d]) float64, given dh = dL/dh of :func:`rmsnorm_fwd`."""
+    x = _as_f64(x)
+    g = None if g is None else _as_f64(np.asarray(g))
+    dh = _c(dh, np.float64)
+    N, d = x.shape
+    dx = np.zeros((N, d), dtype=np.float64)
+    dg = np.zeros(d, dtype=np.float64)
+    rc = _load().oracle_rmsnorm_bwd_f64(_ptr(x), _ptr(g), float(eps), _ptr(dh), N, d, _ptr(dx), _ptr(dg))
+    if rc != 0:
+        raise OracleError(f"oracle_rmsnorm_bwd_f64 returned {rc}")
+    return dx, dg

@@ -15,6 +15,12 @@
  *            p_ij = exp(s_ij - lse_i)
  *   dh     = dZ W,  dW = dZ^T h                      (training backward)
  *   W_deq  = bf16_rne(q * scale)                     (per-group int4 head)
+ *   c = 0 means no cap: s_ij = z_ij, d s / d z = 1
+ *   bpb with bytes_i = lut[t_i]                      (per-id byte lengths)
+ *   W_deq  = bf16_rne(q * scale_v)                   (int8 / int7 rows)
+ *   W_deq  = bf16_rne((q - zero) * scale)            (asymmetric int4)
+ *   W_deq  = bf16_rne(w_fp16)                        (fp16 tied head)
+ *   h      = g * x / sqrt(mean(x^2) + eps)           (RMSNorm prologue)
  *
  * Sources (page title, section):
  *  - "parameter-golf: Parameter Golf: The OpenAI Repo Where Model Size Becomes
@@ -33,7 +39,21 @@
  *  - "parameter-golf README", Leaderboard, row "Sliding Window Eval": stride
  *    64 evaluation, realised here as a row mask.
  *  - "HYDRA Golf" site, stack list: "LQER asymmetric int4, per-group
- *    compression"; the symmetric per-group-64 fp16-scale reading is used.
+ *    compression"; the symmetric per-group-64 fp16-scale reading is used
+ *    for the int4 head, and the asymmetric one (unsigned codes, an integer
+ *    zero point per group) for oracle_dequant_int4_asym.
+ *  - "parameter-golf README", Leaderboard, rows "Mixed Quant + Sliding
+ *    Window Eval" (int8 embeddings), "VarLen Attention + Fused MLP +
+ *    Multi-Phase Global SGD TTT" (int7 embeddings) and "fp16 Embed" (FP16
+ *    tied embedding): more storage formats of the tied table.
+ *  - "parameter-golf README", Leaderboard, rows "SP8192 + CaseOps + ..."
+ *    (byte-sidecar BPB accounting) and "CaseOps Tokenizer + ..." (validation
+ *    byte sidecars); "HYDRA Golf", submission conditions (tokenizer-aware
+ *    validation BPB): the byte count of a scored token comes from the
+ *    tokenizer, i.e. a per-id table gathered by the target.
+ *  - "parameter-golf README", Leaderboard, row "11L Partial RoPE + LN Scale
+ *    + EMA + XSA4" (layerwise LN scale): the hidden states reach the head
+ *    through a normalisation, read as RMSNorm with an optional gain.
  *
  * No blocking, fusion or reordering: every function is the definition
  * written out with plain loops (OpenMP over independent rows only), with the
@@ -115,7 +135,7 @@ static void fwd_row(const double* hi, const double* W, int64_t V, int64_t d,
     const double* wj = W + j * d;
     double z = 0.0;
     for (int64_t k = 0; k < d; ++k) z += hi[k] * wj[k];
-    s[j] = c * tanh(z / c);
+    s[j] = (c > 0.0) ? c * tanh(z / c) : z;   /* c == 0: no cap */
     if (s[j] > m) m = s[j];
   }
   double sum = 0.0;
@@ -133,7 +153,7 @@ int oracle_fwd_f64(const double* h, const double* W, int64_t N, int64_t V,
                    double c, const int64_t* rows, int64_t n_rows,
                    double* nll, double* lse) {
   if (!h || !W || !tgt || !nll || !lse || N <= 0 || V <= 0 || d <= 0 ||
-      !(c > 0.0))
+      !(c >= 0.0))
     return ORACLE_EINVAL;
   int64_t n_out = rows ? n_rows : N;
   for (int64_t r = 0; r < n_out; ++r) {
@@ -190,7 +210,8 @@ double oracle_bpb(const double* nll, const int32_t* bytes, const uint8_t* mask,
 
 /* ---- backward ---------------------------------------------------------- */
 
-/* dz for one row given its lse: dz_j = w (p_j - [j==t]) (1 - tanh^2(z_j/c)).
+/* dz for one row given its lse: dz_j = w (p_j - [j==t]) (1 - tanh^2(z_j/c))
+ * (with c == 0, no cap: dz_j = w (p_j - [j==t])).
  * Chain rule of nll = lse - s_t through s = c tanh(z/c):
  *   d nll / d s_j = p_j - [j == t],   d s_j / d z_j = 1 - tanh^2(z_j / c). */
 static void dz_row(const double* hi, const double* W, int64_t V, int64_t d,
@@ -199,8 +220,9 @@ static void dz_row(const double* hi, const double* W, int64_t V, int64_t d,
     const double* wj = W + j * d;
     double z = 0.0;
     for (int64_t k = 0; k < d; ++k) z += hi[k] * wj[k];
-    double th = tanh(z / c);
-    double s = c * th;
+    /* c == 0: no cap, s = z and d s / d z = 1 */
+    double th = (c > 0.0) ? tanh(z / c) : 0.0;
+    double s = (c > 0.0) ? c * th : z;
     double p = exp(s - lse);
     double g = p - (j == t ? 1.0 : 0.0);
     dz[j] = w * g * (1.0 - th * th);
@@ -214,7 +236,7 @@ int oracle_bwd_f64(const double* h, const double* W, int64_t N, int64_t V,
                    int64_t d, const int64_t* tgt, const uint8_t* mask,
                    double c, const double* lse, double w, double* dh,
                    double* dW) {
-  if (!h || !W || !tgt || !lse || N <= 0 || V <= 0 || d <= 0 || !(c > 0.0))
+  if (!h || !W || !tgt || !lse || N <= 0 || V <= 0 || d <= 0 || !(c >= 0.0))
     return ORACLE_EINVAL;
   for (int64_t i = 0; i < N; ++i) {
     if (mask && !mask[i]) continue;
@@ -257,7 +279,7 @@ int oracle_dh_rows_f64(const double* h, const double* W, int64_t N, int64_t V,
                        int64_t d, const int64_t* tgt, const uint8_t* mask,
                        double c, const int64_t* rows, int64_t n_rows,
                        const double* lse_rows, double w, double* dh_rows) {
-  if (!h || !W || !tgt || !rows || !lse_rows || !dh_rows || !(c > 0.0))
+  if (!h || !W || !tgt || !rows || !lse_rows || !dh_rows || !(c >= 0.0))
     return ORACLE_EINVAL;
   int err = 0;
 #pragma omp parallel
@@ -335,6 +357,166 @@ int oracle_embed_bwd_f64(const int64_t* ids, const double* g, int64_t N,
     double* row = out + ids[i] * d;
     const double* gi = g + i * d;
     for (int64_t k = 0; k < d; ++k) row[k] += gi[k];
+  }
+  return ORACLE_OK;
+}
+
+/* dW for the n_vrows listed vocabulary rows only (full-size sampled
+ * checks): out[r, :] = sum over unmasked rows i of dz_{i, vrows[r]} h_i,
+ * with dz as in dz_row (needs every row's lse).  Sums over i in row order. */
+int oracle_dW_rows_f64(const double* h, const double* W, int64_t N, int64_t V,
+                       int64_t d, const int64_t* tgt, const uint8_t* mask,
+                       double c, const double* lse, double w,
+                       const int64_t* vrows, int64_t n_vrows, double* out) {
+  if (!h || !W || !tgt || !lse || !vrows || !out || N <= 0 || V <= 0 ||
+      d <= 0 || !(c >= 0.0))
+    return ORACLE_EINVAL;
+  for (int64_t i = 0; i < N; ++i) {
+    if (mask && !mask[i]) continue;
+    if (tgt[i] < 0 || tgt[i] >= V) return ORACLE_EDATA;
+  }
+  for (int64_t r = 0; r < n_vrows; ++r)
+    if (vrows[r] < 0 || vrows[r] >= V) return ORACLE_EINVAL;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (int64_t r = 0; r < n_vrows; ++r) {
+    const int64_t j = vrows[r];
+    const double* wj = W + j * d;
+    double* o = out + r * d;
+    for (int64_t k = 0; k < d; ++k) o[k] = 0.0;
+    for (int64_t i = 0; i < N; ++i) {
+      if (mask && !mask[i]) continue;
+      const double* hi = h + i * d;
+      double z = 0.0;
+      for (int64_t k = 0; k < d; ++k) z += hi[k] * wj[k];
+      double th = (c > 0.0) ? tanh(z / c) : 0.0;
+      double s = (c > 0.0) ? c * th : z;
+      double p = exp(s - lse[i]);
+      double g = p - (j == tgt[i] ? 1.0 : 0.0);
+      double dz = w * g * (1.0 - th * th);
+      for (int64_t k = 0; k < d; ++k) o[k] += dz * hi[k];
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* ---- bits per byte with per-id byte lengths --------------------------- */
+
+/* As oracle_bpb, with the byte count of row i taken from the tokenizer's
+ * per-id table: bytes_i = lut[tgt[i]] (the bytes of the scored token).
+ * Returns NAN bpb if the byte sum is 0, and sets *err = ORACLE_EDATA (bpb
+ * NAN) if a scored row's target is outside [0, V). */
+double oracle_bpb_lut(const double* nll, const int64_t* tgt,
+                      const int32_t* lut, int64_t V, const uint8_t* mask,
+                      int64_t N, double* sum_nll_out, int64_t* sum_bytes_out,
+                      int64_t* n_out, int* err) {
+  double sn = 0.0;
+  int64_t sb = 0, n = 0;
+  if (err) *err = ORACLE_OK;
+  for (int64_t i = 0; i < N; ++i) {
+    if (mask && !mask[i]) continue;
+    if (tgt[i] < 0 || tgt[i] >= V) {
+      if (err) *err = ORACLE_EDATA;
+      return NAN;
+    }
+    sn += nll[i];
+    sb += lut[tgt[i]];
+    n += 1;
+  }
+  if (sum_nll_out) *sum_nll_out = sn;
+  if (sum_bytes_out) *sum_bytes_out = sb;
+  if (n_out) *n_out = n;
+  if (sb == 0) return NAN;
+  return sn / (log(2.0) * (double)sb);
+}
+
+/* ---- more storage formats of the tied table --------------------------- */
+
+/* int8 rows (int7 is the same storage with |q| <= 63): q [V, d] signed
+ * bytes, one IEEE binary16 scale per row; out[v, k] = bf16_rne(q * s_v). */
+int oracle_dequant_int8_rows(const int8_t* q, const uint16_t* scales,
+                             int64_t V, int64_t d, uint16_t* out) {
+  if (!q || !scales || !out || V <= 0 || d <= 0) return ORACLE_EINVAL;
+  for (int64_t v = 0; v < V; ++v) {
+    double sc = oracle_f16_to_f64(scales[v]);
+    for (int64_t k = 0; k < d; ++k)
+      out[v * d + k] = oracle_f64_to_bf16_rne((double)q[v * d + k] * sc);
+  }
+  return ORACLE_OK;
+}
+
+/* Asymmetric per-group int4: unsigned codes q in [0, 15] (element 2m in the
+ * low nibble of byte m), one binary16 scale and one integer zero point
+ * z in [0, 15] (a byte) per group of `group` elements along d;
+ * out[v, k] = bf16_rne((q - z) * scale). */
+int oracle_dequant_int4_asym(const uint8_t* Wq, const uint16_t* scales,
+                             const uint8_t* zeros, int64_t V, int64_t d,
+                             int64_t group, uint16_t* out) {
+  if (!Wq || !scales || !zeros || !out || V <= 0 || d <= 0 || group <= 0 ||
+      d % 2 != 0 || d % group != 0)
+    return ORACLE_EINVAL;
+  int64_t ng = d / group;
+  for (int64_t v = 0; v < V; ++v) {
+    for (int64_t k = 0; k < d; ++k) {
+      uint8_t byte = Wq[v * (d / 2) + k / 2];
+      int q = (k % 2 == 0) ? (byte & 0xF) : (byte >> 4);
+      int z = zeros[v * ng + k / group];
+      double sc = oracle_f16_to_f64(scales[v * ng + k / group]);
+      out[v * d + k] = oracle_f64_to_bf16_rne((double)(q - z) * sc);
+    }
+  }
+  return ORACLE_OK;
+}
+
+/* fp16 tied table: out = bf16_rne(w) element by element. */
+int oracle_dequant_f16(const uint16_t* w, int64_t n, uint16_t* out) {
+  if (!w || !out || n < 0) return ORACLE_EINVAL;
+  for (int64_t i = 0; i < n; ++i)
+    out[i] = oracle_f64_to_bf16_rne(oracle_f16_to_f64(w[i]));
+  return ORACLE_OK;
+}
+
+/* ---- RMSNorm prologue --------------------------------------------------- */
+
+/* h_i = g * x_i * rinv_i with rinv_i = 1 / sqrt(mean_k x_ik^2 + eps)
+ * (g == NULL: no gain).  rinv may be NULL. */
+int oracle_rmsnorm_fwd_f64(const double* x, const double* g, double eps,
+                           int64_t N, int64_t d, double* h, double* rinv) {
+  if (!x || !h || N <= 0 || d <= 0 || !(eps >= 0.0)) return ORACLE_EINVAL;
+  for (int64_t i = 0; i < N; ++i) {
+    const double* xi = x + i * d;
+    double ss = 0.0;
+    for (int64_t k = 0; k < d; ++k) ss += xi[k] * xi[k];
+    double r = 1.0 / sqrt(ss / (double)d + eps);
+    if (rinv) rinv[i] = r;
+    for (int64_t k = 0; k < d; ++k) h[i * d + k] = (g ? g[k] : 1.0) * xi[k] * r;
+  }
+  return ORACLE_OK;
+}
+
+/* Backward of the RMSNorm above, given dh = dL/dh:
+ *   dx_ik = rinv_i (g_k dh_ik) - x_ik rinv_i^3 / d * sum_m g_m dh_im x_im
+ *   dg_k  = sum_i dh_ik x_ik rinv_i          (in row order; dg may be NULL)
+ * (chain rule of h_ik = g_k x_ik rinv_i, d rinv_i / d x_ik =
+ * -rinv_i^3 x_ik / d). */
+int oracle_rmsnorm_bwd_f64(const double* x, const double* g, double eps,
+                           const double* dh, int64_t N, int64_t d, double* dx,
+                           double* dg) {
+  if (!x || !dh || !dx || N <= 0 || d <= 0 || !(eps >= 0.0))
+    return ORACLE_EINVAL;
+  if (dg)
+    for (int64_t k = 0; k < d; ++k) dg[k] = 0.0;
+  for (int64_t i = 0; i < N; ++i) {
+    const double* xi = x + i * d;
+    const double* gi = dh + i * d;
+    double ss = 0.0;
+    for (int64_t k = 0; k < d; ++k) ss += xi[k] * xi[k];
+    double r = 1.0 / sqrt(ss / (double)d + eps);
+    double dot = 0.0;
+    for (int64_t k = 0; k < d; ++k) dot += (g ? g[k] : 1.0) * gi[k] * xi[k];
+    for (int64_t k = 0; k < d; ++k)
+      dx[i * d + k] = r * (g ? g[k] : 1.0) * gi[k] - xi[k] * r * r * r / (double)d * dot;
+    if (dg)
+      for (int64_t k = 0; k < d; ++k) dg[k] += gi[k] * xi[k] * r;
   }
   return ORACLE_OK;
 }

@@ -148,6 +148,29 @@ def make_inputs(cfg: int, seed: int | None = None, N: int | None = None,
     return out
 
 
+STREAM_CHUNK_WINDOWS = 32  # a chunk of the evaluation stream: 32 windows, 65,536 rows, 2,048 scored
+
+
+def stream_chunk_seed(k: int) -> int:
+    """Seed of chunk k of the sliding-window evaluation stream (cfg 4)."""
+    return 1004 + 1_000_003 * (int(k) + 1)
+
+
+def make_stream_chunk(k: int, windows: int = STREAM_CHUNK_WINDOWS) -> dict:
+    """Chunk k of the sliding-window evaluation stream: `windows` windows of
+    2048 rows, the last 64 of each scored (row mask), drawn as cfg 4 with the
+    chunk's own seed.  Same keys as make_inputs."""
+    return make_inputs(4, seed=stream_chunk_seed(k), N=windows * WINDOW)
+
+
+def make_byte_lut(V: int, seed: int = 3001, hi: int = 12) -> np.ndarray:
+    """A synthetic per-id byte-length table (int32 [V], uniform in 1..hi).
+    The real table comes from the tokenizer, which is not available; the
+    lengths follow the configs' per-token byte counts (U{1..12})."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    return rng.integers(1, hi + 1, size=V, dtype=np.int64).astype(np.int32)
+
+
 def make_embed_inputs(N: int = 65536, V: int = 8192, d: int = D_MODEL, seed: int = 2001,
                       g_scale: float = 1e-2) -> dict:
     """Seeded inputs of the tied table's input-embedding gradient: the

@@ -367,3 +367,212 @@ def test_embed_bwd_rejects_out_of_range_id(oracle_mod):
         oracle_mod.embed_bwd(np.array([0, 3]), np.ones((2, 4)), 3)
     with pytest.raises(oracle_mod.OracleError):
         oracle_mod.embed_bwd(np.array([-1]), np.ones((1, 4)), 3)
+
+
+# ---- dW on listed vocabulary rows ------------------------------------------
+
+@pytest.mark.parametrize("c", [30.0, 2.0, 0.0])
+def test_dW_rows_matches_full(oracle_mod, c):
+    """The per-row dW (for full-size sampled checks) equals the rows of the
+    full backward, which finite differences pin; rows listed out of order
+    and repeated, first and last included, with masked rows (catches a wrong
+    vocabulary row, a dropped mask or a transposed product)."""
+    inp = si.make_inputs(2, N=40, V=90, d=64, w_scale=20.0)
+    mask = (np.arange(40) % 7 != 3).astype(np.uint8)
+    _, lse = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], c, mask=mask)
+    _, dW = oracle_mod.bwd(inp["h"], inp["W"], inp["tgt"], c, lse, 0.3, mask=mask, want_dh=False)
+    vrows = np.array([89, 0, 17, int(inp["tgt"][5]), 17])
+    got = oracle_mod.dW_rows(inp["h"], inp["W"], inp["tgt"], c, lse, 0.3, vrows, mask=mask)
+    assert np.allclose(got, dW[vrows], rtol=0, atol=1e-15)
+
+
+# ---- no cap (softcap 0) ----------------------------------------------------
+
+def test_uncapped_matches_torch_cross_entropy(oracle_mod):
+    """softcap = 0 means no cap: nll equals torch's fp64 cross_entropy of the
+    plain logits, and dh, dW equal torch autograd of that loss (catches a cap
+    left in, or a (1 - tanh^2) factor left in the gradient)."""
+    rng = np.random.default_rng(21)
+    N, V, d, w = 13, 29, 10, 0.21
+    h, W, t = _rand_case(rng, N, V, d, zscale=30.0, c=0.0)
+    nll, lse = oracle_mod.fwd(h, W, t, 0.0)
+    th = torch.from_numpy(h).requires_grad_(True)
+    tW = torch.from_numpy(W).requires_grad_(True)
+    ref = torch.nn.functional.cross_entropy(th @ tW.T, torch.from_numpy(t), reduction="none")
+    assert np.allclose(nll, ref.detach().numpy(), rtol=0, atol=1e-11)
+    assert ref.detach().numpy().max() > 20.0  # logits far beyond any cap of ~c = 30
+    (w * ref.sum()).backward()
+    dh, dW = oracle_mod.bwd(h, W, t, 0.0, lse, w)
+    assert np.allclose(dh, th.grad.numpy(), rtol=0, atol=1e-11)
+    assert np.allclose(dW, tW.grad.numpy(), rtol=0, atol=1e-11)
+    rows = np.array([4, 0])
+    assert np.allclose(oracle_mod.dh_rows(h, W, t, 0.0, rows, lse[rows], w), dh[rows], rtol=0, atol=1e-15)
+
+
+# ---- bits per byte with per-id byte lengths ----------------------------------
+
+def test_bpb_lut_closed_forms(oracle_mod):
+    """A uniform table of b bytes gives sum nll / (ln 2 * b * n); with the
+    table materialised per row (bytes_i = lut[t_i]) it equals the per-row
+    bpb; masked rows count nothing (catches a table indexed by position
+    instead of by target, or a mask ignored)."""
+    rng = np.random.default_rng(22)
+    N, V = 300, 50
+    nll = rng.random(N) * 5
+    t = rng.integers(0, V, N)
+    mask = (rng.random(N) > 0.3).astype(np.uint8)
+    b, sn, sb, n = oracle_mod.bpb_lut(nll, t, np.full(V, 3, np.int32), mask)
+    M = int(mask.sum())
+    assert (sb, n) == (3 * M, M)
+    assert sn == pytest.approx(float(nll[mask == 1].sum()), rel=1e-15)
+    assert b == pytest.approx(sn / (math.log(2) * 3 * M), rel=1e-15)
+    lut = rng.integers(1, 13, V).astype(np.int32)
+    b1 = oracle_mod.bpb_lut(nll, t, lut, mask)
+    b2 = oracle_mod.bpb(nll, lut[t], mask)
+    assert b1 == b2
+    # zero logits: nll = ln V on every row, so bpb = n log2 V / sum lut[t]
+    b3, *_ = oracle_mod.bpb_lut(np.full(N, math.log(V)), t, lut)
+    assert b3 == pytest.approx(N * math.log2(V) / float(lut[t].sum()), rel=1e-13)
+    with pytest.raises(oracle_mod.OracleError):
+        oracle_mod.bpb_lut(nll, np.where(np.arange(N) == 7, V, t), lut)
+
+
+# ---- more storage formats of the tied table ------------------------------------
+
+def _all_finite_f16():
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    f = bits.view(np.float16)
+    return bits[np.isfinite(f)]
+
+
+def test_dequant_int8_rows_brute_force(oracle_mod):
+    """Every int8 code (-128..127) times every finite fp16 scale, bit-equal
+    to torch: the fp32 product is exact (at most 7 + 11 significant bits),
+    then torch's float -> bfloat16 is the one RNE rounding (catches a double
+    rounding through bf16 scales, a sign or an unsigned byte read)."""
+    sc = _all_finite_f16()
+    q = np.arange(-128, 128, dtype=np.int8)
+    V = sc.size
+    Q = np.tile(q, (V, 1))
+    got = oracle_mod.dequant_int8_rows(Q, sc)
+    ref = (torch.from_numpy(Q.astype(np.float32))
+           * torch.from_numpy(sc.view(np.float16).astype(np.float32))[:, None]).to(torch.bfloat16)
+    assert np.array_equal(got, ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_dequant_int4_asym_brute_force(oracle_mod):
+    """Every unsigned code and zero point (16 x 16) times every finite fp16
+    scale, bit-equal to torch's (q - z) * s rounded once to bf16 (catches
+    nibble order, a signed read of unsigned codes, or a zero point applied
+    after the scale)."""
+    sc = _all_finite_f16()
+    d, group = 256, 256
+    qs = np.arange(16)
+    q_all, z_all = np.meshgrid(qs, qs, indexing="ij")
+    q_row = q_all.reshape(-1)            # 256 codes along d
+    z_vals = np.arange(16, dtype=np.uint8)
+    V = sc.size * 16
+    Q = np.tile(q_row, (V, 1))
+    Wq = (Q[:, 0::2] | (Q[:, 1::2] << 4)).astype(np.uint8)
+    scales = np.repeat(sc, 16)[:, None]
+    zeros = np.tile(z_vals, sc.size)[:, None]
+    got = oracle_mod.dequant_int4_asym(Wq, scales, zeros, d, group)
+    ref = (torch.from_numpy((Q - zeros.astype(np.int64)).astype(np.float32))
+           * torch.from_numpy(scales.view(np.float16).astype(np.float32))).to(torch.bfloat16)
+    assert np.array_equal(got, ref.view(torch.int16).numpy().view(np.uint16))
+
+
+def test_dequant_f16_all_patterns(oracle_mod):
+    """All 65,536 fp16 patterns: bit-equal to torch's float16 -> bfloat16 for
+    every non-NaN pattern, NaN stays NaN (catches truncation instead of RNE,
+    lost subnormals or signs)."""
+    bits = np.arange(65536, dtype=np.uint32).astype(np.uint16)
+    got = oracle_mod.dequant_f16(bits)
+    ref = torch.from_numpy(bits.view(np.float16)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    nan = np.isnan(bits.view(np.float16))
+    assert np.array_equal(got[~nan], ref[~nan])
+    assert np.all(np.isnan(si.bf16_bits_to_f32(got[nan])))
+
+
+# ---- RMSNorm in front of the head ---------------------------------------------
+
+def test_rmsnorm_fwd_matches_torch_and_closed_forms(oracle_mod):
+    """Against torch's fp64 rms_norm with a gain (an independent routine);
+    a constant row a gives g * a / sqrt(a^2 + eps); with eps = 0 the output
+    does not depend on the row's scale (catches a mean taken as a sum, eps
+    outside the root, or the gain dropped)."""
+    rng = np.random.default_rng(23)
+    N, d, eps = 9, 24, 1e-6
+    x = rng.standard_normal((N, d)) * 3
+    g = rng.standard_normal(d)
+    h, rinv = oracle_mod.rmsnorm_fwd(x, g, eps)
+    ref = torch.nn.functional.rms_norm(torch.from_numpy(x), (d,), torch.from_numpy(g), eps)
+    assert np.allclose(h, ref.numpy(), rtol=0, atol=1e-13)
+    assert np.allclose(rinv, 1 / np.sqrt((x * x).mean(axis=1) + eps), rtol=1e-15)
+    a = -0.7
+    hc, _ = oracle_mod.rmsnorm_fwd(np.full((1, d), a), g, 0.01)
+    assert np.allclose(hc[0], g * a / math.sqrt(a * a + 0.01), rtol=1e-15)
+    h1, _ = oracle_mod.rmsnorm_fwd(x, None, 0.0)
+    h2, _ = oracle_mod.rmsnorm_fwd(x * 37.5, None, 0.0)
+    assert np.allclose(h1, h2, rtol=0, atol=1e-14)
+
+
+def test_rmsnorm_bwd_finite_differences(oracle_mod):
+    """Central differences (step 1e-6) of L = sum(R * rmsnorm(x; g)) for a
+    fixed random R pin dx and dg; with no gain and eps = 0 every dx row is
+    orthogonal to its x row (the output is scale-free) (catches a dropped
+    r^3 term, a wrong sign or dg summed without the 1/r factor)."""
+    rng = np.random.default_rng(24)
+    N, d, eps = 3, 5, 1e-3
+    x = rng.standard_normal((N, d))
+    g = rng.standard_normal(d)
+    R = rng.standard_normal((N, d))
+    dx, dg = oracle_mod.rmsnorm_bwd(x, g, eps, R)
+
+    def L(xx, gg):
+        return float((R * oracle_mod.rmsnorm_fwd(xx, gg, eps)[0]).sum())
+
+    step = 1e-6
+    fd_x = np.zeros_like(x)
+    for idx in np.ndindex(*x.shape):
+        xp = x.copy(); xp[idx] += step
+        xm = x.copy(); xm[idx] -= step
+        fd_x[idx] = (L(xp, g) - L(xm, g)) / (2 * step)
+    fd_g = np.zeros_like(g)
+    for k in range(d):
+        gp = g.copy(); gp[k] += step
+        gm = g.copy(); gm[k] -= step
+        fd_g[k] = (L(x, gp) - L(x, gm)) / (2 * step)
+    assert np.abs(dx - fd_x).max() <= 1e-8 * max(1.0, np.abs(fd_x).max())
+    assert np.abs(dg - fd_g).max() <= 1e-8 * max(1.0, np.abs(fd_g).max())
+    dx0, _ = oracle_mod.rmsnorm_bwd(x, None, 0.0, R)
+    assert np.abs((dx0 * x).sum(axis=1)).max() <= 1e-13
+
+
+# ---- stored full-size fixtures ------------------------------------------------
+
+def test_full_size_golden_reproduces(oracle_mod):
+    """tests/golden/full_size.json (written by make_golden.py --full from the
+    oracle only): re-running the oracle reproduces the forward + backward
+    batch's sums and two of its dW rows, and two chunks of the evaluation
+    stream, so an accidental change of the oracle shows up on CPU."""
+    with open(os.path.join(GOLDEN, "full_size.json")) as f:
+        g = json.load(f)
+    e = g["cfg2"]
+    inp = si.make_inputs(2)
+    nll, lse = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], e["softcap"])
+    b, sn, sb, n = oracle_mod.bpb(nll, inp["nbytes"])
+    assert (sb, n) == (e["sum_bytes"], e["n_scored"])
+    assert sn == pytest.approx(e["sum_nll"], rel=1e-12) and b == pytest.approx(e["bpb"], rel=1e-12)
+    sel = [0, 7]
+    rows = oracle_mod.dW_rows(inp["h"], inp["W"], inp["tgt"], e["softcap"], lse, e["grad_scale"],
+                              np.array([e["vrows"][i] for i in sel]))
+    assert np.allclose(rows, np.array([e["dW_rows"][i] for i in sel]), rtol=1e-9, atol=1e-15)
+    st = g["cfg4_stream"]
+    for c in (st["chunks"][0], st["chunks"][-1]):
+        ch = si.make_stream_chunk(c["k"])
+        sel = np.nonzero(ch["mask"])[0]
+        nll, _ = oracle_mod.fwd(ch["h"], ch["W"], ch["tgt"], st["softcap"], rows=sel)
+        _, sn, sb, n = oracle_mod.bpb(nll, ch["nbytes"][sel])
+        assert (sb, n) == (c["sum_bytes"], c["n_scored"])
+        assert sn == pytest.approx(c["sum_nll"], rel=1e-12)
