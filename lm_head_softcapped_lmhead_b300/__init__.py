@@ -26,12 +26,17 @@ LMCE_OK, LMCE_EINVAL, LMCE_ENOTSUP, LMCE_ECUDA, LMCE_EDATA, LMCE_ETIMEOUT = rang
 LMCE_WS_MASKED = 1
 LMCE_WS_INT4 = 2
 LMCE_WS_EMBED = 4
+LMCE_WS_QHEAD = 2
+LMCE_WS_RMSNORM = 8
+LMCE_QHEAD_INT4, LMCE_QHEAD_INT4_ASYM, LMCE_QHEAD_INT8_ROW, LMCE_QHEAD_FP16 = 1, 2, 3, 4
 
 EXPORTS = (
     "lmce_workspace_bytes", "lmce_workspace_init", "lmce_softcap_max", "lmhead_ce_fwd", "lmhead_ce_bwd",
     "lmhead_ce_fwd_int4", "lmhead_ce_bwd_int4", "bpb_reduce", "lmce_bpb", "lmhead_int4_dequant",
     "lmce_status", "lmce_last_cuda_error", "lmce_strerror", "lmce_launch_count", "lmhead_ce_fwd_noalloc",
-    "lmhead_ce_fwd_bwd", "lmhead_ce_fwd_bwd_int4", "lmhead_tied_embed_bwd",
+    "lmhead_ce_fwd_bwd", "lmhead_ce_fwd_bwd_int4", "lmhead_tied_embed_bwd", "lmhead_ce_fwd_q", "lmhead_ce_bwd_q",
+    "lmhead_ce_fwd_bwd_q", "lmhead_qhead_dequant", "lmhead_rmsnorm_fwd", "lmhead_rmsnorm_bwd",
+    "lmhead_ce_fwd_rmsnorm", "lmhead_ce_fwd_bwd_rmsnorm", "bpb_reduce_lut", "lmce_wait_selftest",
 )
 
 _lib = None
@@ -44,6 +49,11 @@ class LmceError(RuntimeError):
         if code == LMCE_ECUDA:
             msg += f": {last_cuda_error()}"
         super().__init__(msg)
+
+
+class _QHead(ctypes.Structure):
+    _fields_ = [("format", ctypes.c_int), ("group", ctypes.c_int), ("codes", ctypes.c_void_p),
+                ("scales", ctypes.c_void_p), ("zeros", ctypes.c_void_p)]
 
 
 class _BpbAcc(ctypes.Structure):
@@ -78,6 +88,18 @@ def lib():
             "lmce_last_cuda_error": ([], ctypes.c_char_p),
             "lmce_strerror": ([I], ctypes.c_char_p),
             "lmce_launch_count": ([], ctypes.c_ulonglong),
+            "lmhead_ce_fwd_q": ([P, I64, ctypes.POINTER(_QHead), I64, I64, I64, P, P, F, P, P, P, SZ, P], I),
+            "lmhead_ce_bwd_q": ([P, I64, ctypes.POINTER(_QHead), I64, I64, I64, P, P, F, P, P, F, P, P, SZ, P], I),
+            "lmhead_ce_fwd_bwd_q": ([P, I64, ctypes.POINTER(_QHead), I64, I64, I64, P, P, F, F, P, P, P, P, SZ, P],
+                                    I),
+            "lmhead_qhead_dequant": ([ctypes.POINTER(_QHead), I64, I64, P, P], I),
+            "lmhead_rmsnorm_fwd": ([P, I64, P, F, I64, I64, P, I64, P, P], I),
+            "lmhead_rmsnorm_bwd": ([P, I64, P, P, P, I64, I64, I64, P, I64, P, I, P, SZ, P], I),
+            "lmhead_ce_fwd_rmsnorm": ([P, I64, P, F, P, I64, I64, I64, P, P, F, P, P, P, SZ, P], I),
+            "lmhead_ce_fwd_bwd_rmsnorm": ([P, I64, P, F, P, I64, I64, I64, P, P, F, F, P, P, P, I64, P, P, I, P, SZ,
+                                           P], I),
+            "bpb_reduce_lut": ([P, P, P, I64, P, I64, P, P, SZ, P], I),
+            "lmce_wait_selftest": ([ctypes.c_longlong, I, P, SZ, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -264,3 +286,103 @@ def lmce_status(ws, stream=None) -> int:
     code = ctypes.c_int()
     _check(lib().lmce_status(_p(ws), _stream(stream), ctypes.byref(code)), "lmce_status")
     return code.value
+
+
+# ---- quantised / fp16 heads ----------------------------------------------------
+def qhead(fmt, codes, scales=None, zeros=None, group=64):
+    """A head description for the *_q calls: fmt one of LMCE_QHEAD_*, codes /
+    scales / zeros CUDA tensors (see include/lmhead_ce.h).  Keep the tensors
+    alive while the calls that use it run."""
+    return _QHead(int(fmt), int(group), codes.data_ptr(), None if scales is None else scales.data_ptr(),
+                  None if zeros is None else zeros.data_ptr())
+
+
+def lmhead_qhead_dequant(head, V, d, out, stream=None):
+    _check(lib().lmhead_qhead_dequant(ctypes.byref(head), V, d, _p(out), _stream(stream)), "lmhead_qhead_dequant")
+
+
+def lmhead_ce_fwd_q(h, head, V, softcap, tgt, nll, lse=None, row_mask=None, ws=None, stream=None):
+    _bf16_bits(h, "h")
+    N, d = h.shape
+    rc = lib().lmhead_ce_fwd_q(_p(h), h.stride(0), ctypes.byref(head), N, V, d, _p(tgt), _p(row_mask),
+                               float(softcap), _p(nll), _p(lse), _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "lmhead_ce_fwd_q")
+
+
+def lmhead_ce_bwd_q(h, head, V, softcap, tgt, lse, grad_scale, dh, row_mask=None, ws=None, stream=None, nll=None):
+    _bf16_bits(h, "h")
+    N, d = h.shape
+    if dh.stride(0) != h.stride(0):
+        raise ValueError("dh must have the same row stride as h")
+    rc = lib().lmhead_ce_bwd_q(_p(h), h.stride(0), ctypes.byref(head), N, V, d, _p(tgt), _p(row_mask),
+                               float(softcap), _p(lse), _p(nll), float(grad_scale), _p(dh), _p(ws), ws.numel(),
+                               _stream(stream))
+    _check(rc, "lmhead_ce_bwd_q")
+
+
+def lmhead_ce_fwd_bwd_q(h, head, V, softcap, tgt, grad_scale, nll, lse, dh, row_mask=None, ws=None, stream=None):
+    _bf16_bits(h, "h")
+    N, d = h.shape
+    if dh.stride(0) != h.stride(0):
+        raise ValueError("dh must have the same row stride as h")
+    rc = lib().lmhead_ce_fwd_bwd_q(_p(h), h.stride(0), ctypes.byref(head), N, V, d, _p(tgt), _p(row_mask),
+                                   float(softcap), float(grad_scale), _p(nll), _p(lse), _p(dh), _p(ws), ws.numel(),
+                                   _stream(stream))
+    _check(rc, "lmhead_ce_fwd_bwd_q")
+
+
+# ---- RMSNorm in front of the head ------------------------------------------------
+def lmhead_rmsnorm_fwd(x, g, eps, h, rinv, stream=None):
+    _bf16_bits(x, "x")
+    _bf16_bits(h, "h")
+    N, d = x.shape
+    rc = lib().lmhead_rmsnorm_fwd(_p(x), x.stride(0), _p(g), float(eps), N, d, _p(h), h.stride(0), _p(rinv),
+                                  _stream(stream))
+    _check(rc, "lmhead_rmsnorm_fwd")
+
+
+def lmhead_rmsnorm_bwd(x, g, rinv, dh, dx, dg=None, accumulate_dg=False, ws=None, stream=None):
+    _bf16_bits(x, "x")
+    _bf16_bits(dh, "dh")
+    _bf16_bits(dx, "dx")
+    N, d = x.shape
+    rc = lib().lmhead_rmsnorm_bwd(_p(x), x.stride(0), _p(g), _p(rinv), _p(dh), dh.stride(0), N, d, _p(dx),
+                                  dx.stride(0), _p(dg), int(bool(accumulate_dg)), _p(ws),
+                                  0 if ws is None else ws.numel(), _stream(stream))
+    _check(rc, "lmhead_rmsnorm_bwd")
+
+
+def lmhead_ce_fwd_rmsnorm(x, g, eps, W, tgt, softcap, nll, lse=None, row_mask=None, ws=None, stream=None):
+    _bf16_bits(x, "x")
+    _bf16_bits(W, "W")
+    N, d = x.shape
+    V = W.shape[0]
+    rc = lib().lmhead_ce_fwd_rmsnorm(_p(x), x.stride(0), _p(g), float(eps), _p(W), N, V, d, _p(tgt), _p(row_mask),
+                                     float(softcap), _p(nll), _p(lse), _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "lmhead_ce_fwd_rmsnorm")
+
+
+def lmhead_ce_fwd_bwd_rmsnorm(x, g, eps, W, tgt, softcap, grad_scale, nll, lse, dx=None, dg=None, dW=None,
+                              accumulate=False, row_mask=None, ws=None, stream=None):
+    _bf16_bits(x, "x")
+    _bf16_bits(W, "W")
+    N, d = x.shape
+    V = W.shape[0]
+    rc = lib().lmhead_ce_fwd_bwd_rmsnorm(_p(x), x.stride(0), _p(g), float(eps), _p(W), N, V, d, _p(tgt),
+                                         _p(row_mask), float(softcap), float(grad_scale), _p(nll), _p(lse), _p(dx),
+                                         0 if dx is None else dx.stride(0), _p(dg), _p(dW), int(bool(accumulate)),
+                                         _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "lmhead_ce_fwd_bwd_rmsnorm")
+
+
+# ---- bits per byte with per-id byte lengths, bounded-wait self-test ----------------
+def bpb_reduce_lut(nll, tgt, lut, acc, row_mask=None, ws=None, stream=None):
+    N = nll.numel()
+    rc = lib().bpb_reduce_lut(_p(nll), _p(tgt), _p(lut), lut.numel(), _p(row_mask), N, _p(acc), _p(ws), ws.numel(),
+                              _stream(stream))
+    _check(rc, "bpb_reduce_lut")
+
+
+def lmce_wait_selftest(limit_cycles, arrive, ws, stream=None):
+    rc = lib().lmce_wait_selftest(int(limit_cycles), int(bool(arrive)), _p(ws), ws.numel(), _stream(stream))
+    _check(rc, "lmce_wait_selftest")

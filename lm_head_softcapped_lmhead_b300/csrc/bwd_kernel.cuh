@@ -45,6 +45,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <string>
 
 #include "ptx.cuh"
@@ -1247,11 +1248,12 @@ inline int setup_attributes() {
   return 0;
 }
 
-// Co-resident 2-CTA clusters for this kernel (cached per process), for the
-// mode with the most shared memory (every mode runs one CTA per SM).
-inline int max_clusters(int sms) {
-  static int cached = 0;
-  if (cached) return cached;
+// Co-resident 2-CTA clusters for this kernel on device `dev` (cached per
+// device), for the mode with the most shared memory (every mode runs one CTA
+// per SM).
+inline int max_clusters(int dev, int sms) {
+  static int cached[64] = {};
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2));
   cfg.blockDim = dim3(THREADS);
@@ -1268,7 +1270,7 @@ inline int max_clusters(int sms) {
     (void)cudaGetLastError();
     n = sms / 2;
   }
-  cached = n;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
   return n;
 }
 
@@ -1298,7 +1300,8 @@ inline int launch_mode(const CUtensorMap& tx, const CUtensorMap& ty, const CUten
 
 inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long N, long long V, long long d,
                   const int64_t* tgt, const uint8_t* mask, float c, const float* lse, const float* nll, float w,
-                  uint16_t* dh, float* dW, int accumulate, unsigned* status, void* scratch, int sms, cudaStream_t s) {
+                  uint16_t* dh, float* dW, int accumulate, unsigned* status, void* scratch, int dev, int sms,
+                  cudaStream_t s) {
   const uint32_t kc = static_cast<uint32_t>(d / KB);
   CUtensorMap tm_hx, tm_wx, tm_hy, tm_wy, tm_hs, tm_ws;
   if (int rc = make_map_bf16_3d(&tm_hx, h, d, N, ldh * 2, BM, ZSC); rc) return rc;
@@ -1307,7 +1310,7 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
   if (int rc = make_map_bf16_3d(&tm_wy, W, d, V, d * 2, BT, ZSC); rc) return rc;
   if (int rc = make_map_bf16_3d(&tm_hs, h, d, N, ldh * 2, SLAB_ROWS, kc); rc) return rc;
   if (int rc = make_map_bf16_3d(&tm_ws, W, d, V, d * 2, SLAB_ROWS, kc); rc) return rc;
-  const int clusters_max = max_clusters(sms);
+  const int clusters_max = max_clusters(dev, sms);
   Params p{};
   p.N = static_cast<int>(N);
   p.V = static_cast<int>(V);
@@ -1317,11 +1320,24 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
   p.mask = mask;
   p.lse = lse;
   p.nll_in = nll;
-  p.inv_c = 1.0f / c;
-  p.cl2e = c * kLog2e;
   p.w = -w;  // the P tiles hold -G
-  p.zlim2 = (kTanhXmax * c) * (kTanhXmax * c);
-  scaled_tanh2_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
+  if (c > 0.0f) {
+    p.inv_c = 1.0f / c;
+    p.cl2e = c * kLog2e;
+    p.zlim2 = (kTanhXmax * c) * (kTanhXmax * c);
+    scaled_tanh2_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
+  } else {
+    // No cap (softcap 0): the epilogue runs with c = 1e30, where in fp32
+    // -tanh(z/c) = -z/c exactly enough that c log2(e) tanh(z/c) = z log2(e)
+    // (to one rounding of the two constants), tanh^2 underflows so
+    // 1 - tanh^2 = 1, and the polynomial's range check never triggers.
+    const float ce = 1e30f;
+    p.inv_c = 1.0f / ce;
+    p.cl2e = ce * kLog2e;
+    p.zlim2 = HUGE_VALF;
+    p.q[0] = -p.inv_c;
+    for (int i = 1; i < kTanhTerms2; ++i) p.q[i] = 0.0f;
+  }
   p.status = status;
   if (dh) {
     Params q = p;
@@ -1367,12 +1383,12 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
 // [N, ldh] bf16, for L = grad_scale * sum of nll over the scored rows.
 inline int launch_fd(const uint16_t* h, long long ldh, const uint16_t* W, long long N, long long V, long long d,
                      const int64_t* tgt, const uint8_t* mask, float c, float grad_scale, float* nll, float* lse,
-                     uint16_t* dh, unsigned* status, int sms, cudaStream_t s) {
+                     uint16_t* dh, unsigned* status, int dev, int sms, cudaStream_t s) {
   CUtensorMap tm_hx, tm_wy, tm_ws;
   if (int rc = make_map_bf16_3d(&tm_hx, h, d, N, ldh * 2, BM, ZSC); rc) return rc;
   if (int rc = make_map_bf16_3d(&tm_wy, W, d, V, d * 2, BT, ZSC); rc) return rc;
   if (int rc = make_map_bf16_3d(&tm_ws, W, d, V, d * 2, SLAB_ROWS, static_cast<uint32_t>(d / KB)); rc) return rc;
-  const int clusters_max = max_clusters(sms);
+  const int clusters_max = max_clusters(dev, sms);
   Params p{};
   p.N = static_cast<int>(N);
   p.V = static_cast<int>(V);

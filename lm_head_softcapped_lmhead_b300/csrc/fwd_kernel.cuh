@@ -30,7 +30,9 @@
 //    logit: e = 2^(c log2(e) tanh(z/c)) with tanh from the minimax
 //    polynomial (packed fp32x2), summed in fp32 over the segment.  No running
 //    max is needed: |s| < c, so S = sum e^s lies in (V e^-c, V e^c) and
-//    cannot overflow for the accepted c (the host rejects c > c_max(V)).
+//    cannot overflow for c <= c_max(V).  Softcap 0 (no cap) and larger
+//    softcaps take the online form (kOnline): a running maximum per segment,
+//    partials (S, m) with S = sum 2^{a - m}.
 //  * outputs: per (segment, column half) the partial sum over the non-target
 //    columns into part[2 s + half][row], s = the segment's first tile inside
 //    its row pair (< VT); the target's term e^{s_t} into st[row] by the one
@@ -82,7 +84,8 @@ struct Params {
   float zlim2;          // (kTanhXmax * c)^2: range of the polynomial in z^2
   float k[kTanhTerms];  // c log2(e) C_i / c^(2i+1): 2^(z P(z^2)) = e^(c tanh(z/c))
   float* part;          // [2 maxseg][N_pad] partial sums of e^s over the non-target columns
-  float* st;            // [N] e^{s_t}, the target column's term
+  float* partm;         // online form: [2 maxseg][N_pad] base-2 running maxima of the partials
+  float* st;            // [N] e^{s_t}, the target column's term (online form: a_t = s_t log2 e)
   unsigned* status;
 };
 
@@ -184,6 +187,92 @@ __device__ __forceinline__ void chunk_terms(const uint32_t (&r)[32], const float
   }
 }
 
+// ---- online (running-maximum) form --------------------------------------------
+// For softcap 0 (no cap: the host passes c = 1e30, where c tanh(z/c) equals z
+// in fp32) and for softcaps beyond the fixed-shift range, where sum_j e^{s_j}
+// may leave the fp32 range.  Per chunk, a_j = s_j log2(e) for the 32
+// columns; the thread's segment state (m, S) keeps S = sum 2^{a_j - m} over
+// the non-target columns seen so far, m the largest a_j seen.
+__device__ __noinline__ ChunkF32 chunk_a_slow(ChunkF32 r, float c, float inv_c) {
+  ChunkF32 o;
+  const float cl2e = c * kLog2e;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) o.v[j] = __float_as_uint(cl2e * tanh_any(__uint_as_float(r.v[j]) * inv_c));
+  return o;
+}
+
+template <bool kHit>
+__device__ __forceinline__ void chunk_online(const uint32_t (&r)[32], const float2 (&k)[kTanhTerms], const Params& p,
+                                             int lim, int rel, float& m, float& S, float& at) {
+  const float kNegInf = __int_as_float(0xff800000);
+  float a[32];
+  float2 su = make_float2(0.f, 0.f);
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
+    const float2 u = __fmul2_rn(z, z);
+    su = __fadd2_rn(su, u);
+    const float2 v = poly_z2(z, u, k);
+    a[2 * j] = v.x;
+    a[2 * j + 1] = v.y;
+  }
+  if (__any_sync(0xffffffffu, !(su.x + su.y <= p.zlim2))) {
+    ChunkF32 c;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) c.v[j] = r[j];
+    const ChunkF32 o = chunk_a_slow(c, p.c, p.inv_c);
+#pragma unroll
+    for (int j = 0; j < 32; ++j) a[j] = __uint_as_float(o.v[j]);
+  }
+#pragma unroll
+  for (int j = 0; j < 32; ++j) {
+    if (lim < 32 && j >= lim) a[j] = kNegInf;
+    if (kHit && j == rel) {
+      at = a[j];
+      a[j] = kNegInf;
+    }
+  }
+  float M = kNegInf;
+#pragma unroll
+  for (int j = 0; j < 32; j += 2) M = fmax3(M, a[j], a[j + 1]);
+  if (M > m) {
+    S *= ex2_approx(m - M);  // m = -inf: S is still 0
+    m = M;
+  }
+  if (M > kNegInf) {
+    float2 s0 = make_float2(0.f, 0.f), s1 = s0;
+    const float2 nm = make_float2(-m, -m);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float2 d = __fadd2_rn(make_float2(a[2 * j], a[2 * j + 1]), nm);
+      const float2 e = make_float2(ex2_approx(d.x), ex2_approx(d.y));
+      if (j & 1)
+        s1 = __fadd2_rn(s1, e);
+      else
+        s0 = __fadd2_rn(s0, e);
+    }
+    S += (s0.x + s0.y) + (s1.x + s1.y);
+  }
+}
+
+__device__ __forceinline__ void chunk_terms_online(const uint32_t (&r)[32], const float2 (&k)[kTanhTerms],
+                                                   const Params& p, int lim, long long relw, float& m, float& S,
+                                                   float& st_val, bool& st_hit) {
+  const int rel = (relw >= 0 && relw < 32) ? static_cast<int>(relw) : -1;
+  if (__any_sync(0xffffffffu, rel >= 0)) {
+    float at = 0.f;
+    if (lim > 0) chunk_online<true>(r, k, p, lim, rel, m, S, at);
+    if (rel >= 0) {
+      st_val = at;
+      st_hit = true;
+    }
+  } else {
+    float at = 0.f;
+    if (lim > 0) chunk_online<false>(r, k, p, lim, -1, m, S, at);
+  }
+}
+
+template <bool kOnline>
 __global__ void __launch_bounds__(THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                const Params p) {
@@ -360,6 +449,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     int row = 0;
     long long t = -1;
     float seg_sum = 0.f;
+    float seg_m = __int_as_float(0xff800000);  // online form: the segment's running maximum (base 2)
     for (long long g = g_begin; g < g_end; ++g) {
       const int rbp = static_cast<int>(g / p.VT);
       const int vt = static_cast<int>(g % p.VT);
@@ -368,6 +458,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         t = (row < n_rows) ? p.tgt[row] : -1;
         cur_rbp = rbp;
         seg_sum = 0.f;
+        seg_m = __int_as_float(0xff800000);
       }
       if (!mbar_wait(acc_full + acc, aph, abort_flag, p.status)) break;
       tc_fence_after();
@@ -386,7 +477,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         tmem_ld32(tbase + (ch + 1) * 32, rc);
         {
           const int cbase = col0 + ch * 32;
-          chunk_terms(ra, k2, p, min(32, p.V - cbase), t - cbase, seg_sum, st_val, st_hit);
+          if (kOnline)
+            chunk_terms_online(ra, k2, p, min(32, p.V - cbase), t - cbase, seg_m, seg_sum, st_val, st_hit);
+          else
+            chunk_terms(ra, k2, p, min(32, p.V - cbase), t - cbase, seg_sum, st_val, st_hit);
         }
         tmem_ld_wait();
         reg_fence32(rc);
@@ -404,7 +498,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         {
           const int cbase = col0 + (ch + 1) * 32;
-          chunk_terms(rc, k2, p, min(32, p.V - cbase), t - cbase, seg_sum, st_val, st_hit);
+          if (kOnline)
+            chunk_terms_online(rc, k2, p, min(32, p.V - cbase), t - cbase, seg_m, seg_sum, st_val, st_hit);
+          else
+            chunk_terms(rc, k2, p, min(32, p.V - cbase), t - cbase, seg_sum, st_val, st_hit);
         }
         if (ch + 2 < 4) {
           tmem_ld_wait();
@@ -420,6 +517,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           const long long g0 = static_cast<long long>(rbp) * p.VT;
           const int slot = static_cast<int>(g_begin > g0 ? g_begin - g0 : 0);
           p.part[static_cast<size_t>(2 * slot + hc) * p.N_pad + row] = seg_sum;
+          if (kOnline) p.partm[static_cast<size_t>(2 * slot + hc) * p.N_pad + row] = seg_m;
         }
       }
       acc ^= 1;
@@ -438,10 +536,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// Co-resident 2-CTA clusters of fwd_kernel (cached per process).
-inline int max_clusters(int sms) {
-  static int cached = 0;
-  if (cached) return cached;
+// Co-resident 2-CTA clusters of fwd_kernel on device `dev` (cached per
+// device; both forms have the same shape and shared memory).
+inline int max_clusters(int dev, int sms) {
+  static int cached[64] = {};
+  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2));
   cfg.blockDim = dim3(THREADS);
@@ -454,15 +553,16 @@ inline int max_clusters(int sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel, &cfg) != cudaSuccess || n <= 0) {
+  if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel<false>, &cfg) != cudaSuccess || n <= 0) {
     (void)cudaGetLastError();
     n = sms / 2;
   }
-  cached = n;
+  if (dev >= 0 && dev < 64) cached[dev] = n;
   return n;
 }
 
-inline int launch(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const Params& p, int pairs, cudaStream_t s) {
+inline int launch(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const Params& p, int pairs, cudaStream_t s,
+                  bool online = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
   cfg.blockDim = dim3(THREADS);
@@ -475,7 +575,8 @@ inline int launch(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const Params
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = cudaLaunchKernelEx(&cfg, fwd_kernel, tm_h, tm_w, p);
+  cudaError_t e = online ? cudaLaunchKernelEx(&cfg, fwd_kernel<true>, tm_h, tm_w, p)
+                         : cudaLaunchKernelEx(&cfg, fwd_kernel<false>, tm_h, tm_w, p);
   if (e != cudaSuccess) {
     set_last_error(std::string("fwd_kernel launch: ") + cudaGetErrorString(e));
     return 3;

@@ -30,6 +30,7 @@ int cuda_fail(cudaError_t e, const char* what) {
 }
 
 constexpr size_t kAlign = 256;
+constexpr int kNormBlocks = 296;  // fixed grid of the RMSNorm backward (the gain's partial sums)
 size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
@@ -37,7 +38,7 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 struct Layout {
   size_t status = 0;    // unsigned status word (sticky until lmce_status)
   size_t bpb = 0;       // kBpbBlocks partials
-  size_t part = 0;      // forward: [2 VT][N_pad] fp32 partial sums
+  size_t part = 0;      // forward: [2 VT][N_pad] fp32 partial sums, then [2 VT][N_pad] running maxima
   size_t st = 0;        // forward: [N_pad] fp32 target logits
   size_t blkcnt = 0;    // masked: per-block counts / offsets
   size_t nscored = 0;   // masked: live row count
@@ -46,6 +47,10 @@ struct Layout {
   size_t h_c = 0;       // masked: [N, d] bf16 compacted rows
   size_t wdeq = 0;      // int4: [V, d] bf16 dequantised head
   size_t embed = 0;     // tied-embedding gradient: counting sort and piece sums
+  size_t hn = 0;        // RMSNorm: [N, d] bf16 normalised rows
+  size_t dhn = 0;       // RMSNorm: [N, d] bf16 gradient of the normalised rows
+  size_t rinv = 0;      // RMSNorm: [N] fp32 reciprocal RMS
+  size_t dgp = 0;       // RMSNorm: [kNormBlocks][d] fp32 partials of the gain's gradient
   size_t bwd = 0;       // backward scratch
   size_t total = 0;
 };
@@ -59,8 +64,8 @@ Layout make_layout(int64_t N, int64_t V, int64_t d, unsigned flags) {
   o = up(o + sizeof(lmce::BpbPartial) * lmce::kBpbBlocks);
   const int64_t N_pad = cdiv(N, lmce::fwdk::PAIR_ROWS) * lmce::fwdk::PAIR_ROWS;
   const int64_t VT = cdiv(V, lmce::fwdk::BN);
-  L.part = o;  // at most VT clusters cover one row pair: 2 VT slots per row
-  o = up(o + sizeof(float) * 2 * VT * N_pad);
+  L.part = o;  // at most VT clusters cover one row pair: 2 VT slots per row (sums, then maxima)
+  o = up(o + sizeof(float) * 2 * 2 * VT * N_pad);
   L.st = o;
   o = up(o + sizeof(float) * N_pad);
   if (flags & LMCE_WS_MASKED) {
@@ -82,6 +87,16 @@ Layout make_layout(int64_t N, int64_t V, int64_t d, unsigned flags) {
   if (flags & LMCE_WS_EMBED) {
     L.embed = o;
     o = up(o + lmce::embk::layout(N, V, d).total);
+  }
+  if (flags & LMCE_WS_RMSNORM) {
+    L.dgp = o;
+    o = up(o + sizeof(float) * kNormBlocks * d);
+    L.rinv = o;
+    o = up(o + sizeof(float) * N);
+    L.hn = o;
+    o = up(o + 2 * N * d);
+    L.dhn = o;
+    o = up(o + 2 * N * d);
   }
   L.bwd = o;
   o = up(o + lmce::bwdk::scratch_bytes(N, V, d));
@@ -117,9 +132,12 @@ int dev_info(DevInfo* out) {
       g_last_err = "device is not sm_103 (compute capability 10.3)";
       return LMCE_ENOTSUP;
     }
-    if ((e = cudaFuncSetAttribute(lmce::fwdk::fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if ((e = cudaFuncSetAttribute(lmce::fwdk::fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   lmce::fwdk::SMEM_BYTES)) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
+    if ((e = cudaFuncSetAttribute(lmce::fwdk::fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  lmce::fwdk::SMEM_BYTES)) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(fwd, online)");
     if (int rc = lmce::bwdk::setup_attributes(); rc != 0) return rc;
     sms[dev] = n;
     ready[dev] = true;
@@ -219,6 +237,12 @@ float softcap_max(int64_t V) {
   return static_cast<float>(a < b ? a : b);
 }
 
+// Softcap c: 0 (no cap) or a finite c > 0.  Up to softcap_max(V) the
+// forward sums e^s with a fixed shift; 0 and larger caps take the online
+// (running-maximum) form.
+bool softcap_ok(float c) { return c >= 0.0f && std::isfinite(c); }
+bool softcap_online(float c, int64_t V) { return !(c > 0.0f) || c > softcap_max(V); }
+
 // Shared shape / pointer checks of the forward and backward.
 int check_common(const void* h, int64_t ldh, const void* W, int64_t N, int64_t V, int64_t d, const int64_t* tgt,
                  float softcap, void* ws) {
@@ -228,20 +252,36 @@ int check_common(const void* h, int64_t ldh, const void* W, int64_t N, int64_t V
   if (d % 64 != 0 || d > 512) return LMCE_ENOTSUP;
   if (ldh < d || ldh % 8 != 0) return LMCE_EINVAL;
   if (!aligned16(h) || !aligned16(W) || !aligned16(ws)) return LMCE_EINVAL;
-  if (!(softcap > 0.0f) || !(softcap <= softcap_max(V))) return LMCE_ENOTSUP;
+  if (!softcap_ok(softcap)) return LMCE_ENOTSUP;
   return LMCE_OK;
 }
 
 int bwd_launch(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
                const int64_t* tgt, const uint8_t* mask, float c, const float* lse, const float* nll, float w,
-               lmce_bf16* dh, float* dW, int accumulate, unsigned* status, void* scratch, int sms, cudaStream_t s) {
-  return lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, mask, c, lse, nll, w, dh, dW, accumulate, status, scratch, sms,
-                            s);
+               lmce_bf16* dh, float* dW, int accumulate, unsigned* status, void* scratch, const DevInfo& di,
+               cudaStream_t s) {
+  return lmce::bwdk::launch(h, ldh, W, N, V, d, tgt, mask, c, lse, nll, w, dh, dW, accumulate, status, scratch,
+                            di.dev, di.sms, s);
 }
 int fd_launch(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
               const int64_t* tgt, const uint8_t* mask, float c, float grad_scale, float* nll, float* lse,
-              lmce_bf16* dh, unsigned* status, int sms, cudaStream_t s) {
-  return lmce::bwdk::launch_fd(h, ldh, W, N, V, d, tgt, mask, c, grad_scale, nll, lse, dh, status, sms, s);
+              lmce_bf16* dh, unsigned* status, const DevInfo& di, cudaStream_t s) {
+  return lmce::bwdk::launch_fd(h, ldh, W, N, V, d, tgt, mask, c, grad_scale, nll, lse, dh, status, di.dev, di.sms, s);
+}
+
+// The one-pass forward + dh (FD) accumulates unnormalised terms: only for
+// 0 < c <= kFusedSoftcapMax.
+bool use_fd(float c) { return c > 0.0f && c <= kFusedSoftcapMax; }
+
+// Forward kernel parameters for softcap c (0 = no cap: c = 1e30, where
+// c tanh(z/c) equals z in fp32 and the polynomial's range check never
+// triggers).
+void fwd_params_softcap(lmce::fwdk::Params& p, float c) {
+  const float ce = c > 0.0f ? c : 1e30f;
+  p.inv_c = 1.0f / ce;
+  p.c = ce;
+  p.zlim2 = c > 0.0f ? (lmce::kTanhXmax * c) * (lmce::kTanhXmax * c) : HUGE_VALF;
+  lmce::scaled_tanh_coeffs(static_cast<double>(ce) * 1.4426950408889634, 1.0 / static_cast<double>(ce), p.k);
 }
 
 int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
@@ -300,48 +340,175 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
   p.VT = static_cast<int>(cdiv(V, lmce::fwdk::BN));
   p.N_pad = static_cast<int>(cdiv(N, lmce::fwdk::PAIR_ROWS) * lmce::fwdk::PAIR_ROWS);
   p.tgt = tg;
-  p.inv_c = 1.0f / c;
-  p.c = c;
-  p.zlim2 = (lmce::kTanhXmax * c) * (lmce::kTanhXmax * c);
-  lmce::scaled_tanh_coeffs(static_cast<double>(c) * 1.4426950408889634, 1.0 / static_cast<double>(c), p.k);
+  fwd_params_softcap(p, c);
   p.part = reinterpret_cast<float*>(w + L.part);
+  p.partm = p.part + static_cast<size_t>(2) * p.VT * p.N_pad;
   p.st = reinterpret_cast<float*>(w + L.st);
   p.status = status;
   p.maxseg = p.VT;
+  const bool online = softcap_online(c, V);
 
   const int64_t T_max = cdiv(N, lmce::fwdk::PAIR_ROWS) * p.VT;
-  const int pairs = static_cast<int>(std::min<int64_t>(T_max, lmce::fwdk::max_clusters(di.sms)));
+  const int pairs = static_cast<int>(std::min<int64_t>(T_max, lmce::fwdk::max_clusters(di.dev, di.sms)));
   lmce::count_launches(2);
-  if (int rc = lmce::fwdk::launch(tm_h, tm_w, p, pairs, s); rc) return rc;
+  if (int rc = lmce::fwdk::launch(tm_h, tm_w, p, pairs, s, online); rc) return rc;
   cudaError_t e = cudaSuccess;
   const int fblocks = static_cast<int>(std::min<int64_t>(cdiv(N, 256), int64_t(di.sms) * 4));
-  lmce::fwd_finalize_kernel<<<fblocks, 256, 0, s>>>(p.part, p.VT, pairs, lmce::fwdk::PAIR_ROWS, p.N_pad, p.st, tg,
-                                                    nrows_dev,
-                                                    static_cast<int>(N), static_cast<int>(V), idx, nll, lse, status);
+  if (online)
+    lmce::fwd_finalize_online_kernel<<<fblocks, 256, 0, s>>>(p.part, p.partm, p.VT, pairs, lmce::fwdk::PAIR_ROWS,
+                                                             p.N_pad, p.st, tg, nrows_dev, static_cast<int>(N),
+                                                             static_cast<int>(V), idx, nll, lse, status);
+  else
+    lmce::fwd_finalize_kernel<<<fblocks, 256, 0, s>>>(p.part, p.VT, pairs, lmce::fwdk::PAIR_ROWS, p.N_pad, p.st, tg,
+                                                      nrows_dev, static_cast<int>(N), static_cast<int>(V), idx, nll,
+                                                      lse, status);
   e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "fwd_finalize launch");
   return LMCE_OK;
 }
 
-int dequant_impl(const uint8_t* Wq, const lmce_f16* scales, int64_t V, int64_t d, int group, lmce_bf16* out,
-                 cudaStream_t s, int sms) {
-  const int64_t total = V * (d / 16);
-  const int blocks = static_cast<int>(std::min<int64_t>(cdiv(total, 256), int64_t(sms) * 8));
+// Validates a quantised / fp16 head description (pointer alignment as the
+// dequantisation kernels read them: 8-byte int4 code words, 16-byte int8 and
+// fp16 vectors).
+int check_qhead(const lmce_qhead* hd, int64_t V, int64_t d) {
+  if (!hd || !hd->codes || V < 1 || d < 1 || d % 64 != 0) return LMCE_EINVAL;
+  const uintptr_t q = reinterpret_cast<uintptr_t>(hd->codes);
+  const uintptr_t sc = reinterpret_cast<uintptr_t>(hd->scales);
+  switch (hd->format) {
+    case LMCE_QHEAD_INT4:
+    case LMCE_QHEAD_INT4_ASYM:
+      if (!hd->scales || (q & 7u) != 0 || (sc & 1u) != 0) return LMCE_EINVAL;
+      if (hd->group < 16 || hd->group % 16 != 0 || d % hd->group != 0) return LMCE_EINVAL;
+      if (hd->format == LMCE_QHEAD_INT4_ASYM && !hd->zeros) return LMCE_EINVAL;
+      return LMCE_OK;
+    case LMCE_QHEAD_INT8_ROW:
+      if (!hd->scales || (q & 15u) != 0 || (sc & 1u) != 0) return LMCE_EINVAL;
+      return LMCE_OK;
+    case LMCE_QHEAD_FP16:
+      if ((q & 15u) != 0) return LMCE_EINVAL;
+      return LMCE_OK;
+    default:
+      return LMCE_EINVAL;
+  }
+}
+
+// out [V, d] bf16 = the dequantised head (bit-exact: one RNE rounding).
+int qhead_dequant_impl(const lmce_qhead* hd, int64_t V, int64_t d, lmce_bf16* out, cudaStream_t s, int sms) {
+  const int64_t per16 = V * (d / 16);
+  const int blocks = static_cast<int>(std::min<int64_t>(cdiv(per16, 256), int64_t(sms) * 8));
+  const auto* sc = reinterpret_cast<const __half*>(hd->scales);
+  auto* o = reinterpret_cast<__nv_bfloat16*>(out);
   lmce::count_launches(1);
-  lmce::dequant_int4_kernel<<<blocks, 256, 0, s>>>(Wq, reinterpret_cast<const __half*>(scales),
-                                                   static_cast<int>(V), static_cast<int>(d), group,
-                                                   reinterpret_cast<__nv_bfloat16*>(out));
+  switch (hd->format) {
+    case LMCE_QHEAD_INT4:
+      lmce::dequant_int4_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint8_t*>(hd->codes), sc,
+                                                       static_cast<int>(V), static_cast<int>(d), hd->group, o);
+      break;
+    case LMCE_QHEAD_INT4_ASYM:
+      lmce::dequant_int4_asym_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint8_t*>(hd->codes), sc, hd->zeros,
+                                                            static_cast<int>(V), static_cast<int>(d), hd->group, o);
+      break;
+    case LMCE_QHEAD_INT8_ROW:
+      lmce::dequant_int8_rows_kernel<<<blocks, 256, 0, s>>>(static_cast<const int8_t*>(hd->codes), sc,
+                                                            static_cast<int>(V), static_cast<int>(d), o);
+      break;
+    default: {
+      const int64_t n8 = V * d / 8;
+      const int b8 = static_cast<int>(std::min<int64_t>(cdiv(n8, 256), int64_t(sms) * 8));
+      lmce::dequant_f16_kernel<<<b8, 256, 0, s>>>(static_cast<const uint4*>(hd->codes), n8,
+                                                  reinterpret_cast<uint4*>(out));
+    }
+  }
   cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return cuda_fail(e, "dequant_int4 launch");
+  if (e != cudaSuccess) return cuda_fail(e, "head dequantisation launch");
   return LMCE_OK;
 }
 
-int check_int4(const uint8_t* Wq, const lmce_f16* scales, int group, int64_t V, int64_t d) {
-  if (!Wq || !scales) return LMCE_EINVAL;
-  if (V < 1 || d < 1) return LMCE_EINVAL;
-  if (group < 16 || group % 16 != 0 || d % group != 0) return LMCE_EINVAL;
-  if ((reinterpret_cast<uintptr_t>(Wq) & 7u) != 0 || (reinterpret_cast<uintptr_t>(scales) & 1u) != 0)
-    return LMCE_EINVAL;
+lmce_qhead int4_head(const uint8_t* Wq, const lmce_f16* scales, int group) {
+  lmce_qhead hd{};
+  hd.format = LMCE_QHEAD_INT4;
+  hd.group = group;
+  hd.codes = Wq;
+  hd.scales = scales;
+  hd.zeros = nullptr;
+  return hd;
+}
+
+// Training step (lmhead_ce_fwd_bwd) on a workspace laid out with
+// extra_flags (so that the backward's scratch does not overlap the other
+// uses of the same workspace).
+int fwd_bwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
+                 const int64_t* tgt, const uint8_t* row_mask, float softcap, float grad_scale, float* nll, float* lse,
+                 lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes, void* stream,
+                 unsigned extra_flags) {
+  if (int rc = check_common(h, ldh, W, N, V, d, tgt, softcap, ws); rc) return rc;
+  if (!nll || !lse) return LMCE_EINVAL;
+  if (dh && !aligned16(dh)) return LMCE_EINVAL;
+  if (dW && !aligned16(dW)) return LMCE_EINVAL;
+  if (!std::isfinite(grad_scale)) return LMCE_EINVAL;
+  const Layout L = make_layout(N, V, d, (row_mask ? LMCE_WS_MASKED : 0u) | extra_flags);
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  char* w = static_cast<char*>(ws);
+  unsigned* status = reinterpret_cast<unsigned*>(w + L.status);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dh && use_fd(softcap)) {
+    // Forward and dh in one pass over the vocabulary.
+    if (int rc = fd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, status, di, s); rc)
+      return rc;
+  } else {
+    if (int rc = fwd_impl(h, ldh, W, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, extra_flags);
+        rc)
+      return rc;
+    if (dh) {
+      if (int rc = bwd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, nullptr, 0,
+                              status, w + L.bwd, di, s);
+          rc)
+        return rc;
+    }
+  }
+  if (dW) {
+    if (int rc = bwd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, nullptr, dW,
+                            accumulate_dW, status, w + L.bwd, di, s);
+        rc)
+      return rc;
+  }
+  return LMCE_OK;
+}
+
+int check_norm(const lmce_bf16* x, int64_t ldx, const float* g, int64_t N, int64_t d) {
+  if (!x || N < 1 || d < 1 || N > (int64_t(1) << 30)) return LMCE_EINVAL;
+  if (d % 64 != 0 || d > 512) return LMCE_ENOTSUP;
+  if (ldx < d || ldx % 8 != 0 || !aligned16(x)) return LMCE_EINVAL;
+  if (g && (reinterpret_cast<uintptr_t>(g) & 3u) != 0) return LMCE_EINVAL;
+  return LMCE_OK;
+}
+
+int rmsnorm_fwd_impl(const lmce_bf16* x, int64_t ldx, const float* g, float eps, int64_t N, int64_t d, lmce_bf16* h,
+                     int64_t ldh, float* rinv, cudaStream_t s, int sms) {
+  const int blocks = static_cast<int>(std::min<int64_t>(cdiv(N, lmce::kNormWarps), int64_t(sms) * 8));
+  lmce::count_launches(1);
+  lmce::rmsnorm_fwd_kernel<<<blocks, lmce::kNormWarps * 32, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), ldx, g, eps, static_cast<int>(N), static_cast<int>(d),
+      reinterpret_cast<__nv_bfloat16*>(h), ldh, rinv);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "rmsnorm_fwd launch");
+  return LMCE_OK;
+}
+
+int rmsnorm_bwd_impl(const lmce_bf16* x, int64_t ldx, const float* g, const float* rinv, const lmce_bf16* dh,
+                     int64_t lddh, int64_t N, int64_t d, lmce_bf16* dx, int64_t lddx, float* dg, int accumulate_dg,
+                     float* dgp, cudaStream_t s) {
+  lmce::count_launches(dg ? 2 : 1);
+  lmce::rmsnorm_bwd_kernel<<<kNormBlocks, lmce::kNormWarps * 32, 0, s>>>(
+      reinterpret_cast<const __nv_bfloat16*>(x), ldx, g, rinv, reinterpret_cast<const __nv_bfloat16*>(dh), lddh,
+      static_cast<int>(N), static_cast<int>(d), reinterpret_cast<__nv_bfloat16*>(dx), lddx, dg ? dgp : nullptr);
+  if (dg)
+    lmce::rmsnorm_dg_reduce_kernel<<<static_cast<int>(cdiv(d, 256)), 256, 0, s>>>(dgp, kNormBlocks,
+                                                                                 static_cast<int>(d), accumulate_dg, dg);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "rmsnorm_bwd launch");
   return LMCE_OK;
 }
 
@@ -384,110 +551,180 @@ int lmhead_ce_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N
   if (int rc = dev_info(&di); rc) return rc;
   char* w = static_cast<char*>(ws);
   return bwd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, dW, accumulate_dW,
-                    reinterpret_cast<unsigned*>(w + L.status), w + L.bwd, di.sms, static_cast<cudaStream_t>(stream));
+                    reinterpret_cast<unsigned*>(w + L.status), w + L.bwd, di, static_cast<cudaStream_t>(stream));
 }
 
 int lmhead_ce_fwd_bwd(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
                       const int64_t* tgt, const uint8_t* row_mask, float softcap, float grad_scale, float* nll,
                       float* lse, lmce_bf16* dh, float* dW, int accumulate_dW, void* ws, size_t ws_bytes,
                       void* stream) {
-  if (int rc = check_common(h, ldh, W, N, V, d, tgt, softcap, ws); rc) return rc;
-  if (!nll || !lse) return LMCE_EINVAL;
-  if (dh && !aligned16(dh)) return LMCE_EINVAL;
-  if (dW && !aligned16(dW)) return LMCE_EINVAL;
-  if (!std::isfinite(grad_scale)) return LMCE_EINVAL;
-  const Layout L = make_layout(N, V, d, row_mask ? LMCE_WS_MASKED : 0u);
-  if (ws_bytes < L.total) return LMCE_EINVAL;
-  DevInfo di;
-  if (int rc = dev_info(&di); rc) return rc;
-  char* w = static_cast<char*>(ws);
-  unsigned* status = reinterpret_cast<unsigned*>(w + L.status);
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dh && softcap <= kFusedSoftcapMax) {
-    // Forward and dh in one pass over the vocabulary.
-    if (int rc = fd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, status, di.sms, s);
-        rc)
-      return rc;
-  } else {
-    if (int rc = fwd_impl(h, ldh, W, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, 0u); rc)
-      return rc;
-    if (dh) {
-      if (int rc = bwd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, nullptr, 0,
-                              status, w + L.bwd, di.sms, s);
-          rc)
-        return rc;
-    }
-  }
-  if (dW) {
-    if (int rc = bwd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, nullptr, dW,
-                            accumulate_dW, status, w + L.bwd, di.sms, s);
-        rc)
-      return rc;
-  }
-  return LMCE_OK;
+  return fwd_bwd_impl(h, ldh, W, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, dW, accumulate_dW, ws,
+                      ws_bytes, stream, 0u);
 }
 
-int lmhead_ce_fwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
-                       int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
-                       float* nll, float* lse, void* ws, size_t ws_bytes, void* stream) {
-  if (int rc = check_int4(Wq, scales, group, V, d); rc) return rc;
+int lmhead_qhead_dequant(const lmce_qhead* head, int64_t V, int64_t d, lmce_bf16* out, void* stream) {
+  if (int rc = check_qhead(head, V, d); rc) return rc;
+  if (!out || !aligned16(out)) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  return qhead_dequant_impl(head, V, d, out, static_cast<cudaStream_t>(stream), di.sms);
+}
+
+int lmhead_ce_fwd_q(const lmce_bf16* h, int64_t ldh, const lmce_qhead* head, int64_t N, int64_t V, int64_t d,
+                    const int64_t* tgt, const uint8_t* row_mask, float softcap, float* nll, float* lse, void* ws,
+                    size_t ws_bytes, void* stream) {
+  if (int rc = check_qhead(head, V, d); rc) return rc;
   if (!ws || !aligned16(ws)) return LMCE_EINVAL;
-  const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_INT4 | (row_mask ? LMCE_WS_MASKED : 0u));
+  const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_QHEAD | (row_mask ? LMCE_WS_MASKED : 0u));
   if (ws_bytes < L.total) return LMCE_EINVAL;
   lmce_bf16* wdeq = reinterpret_cast<lmce_bf16*>(static_cast<char*>(ws) + L.wdeq);
   if (int rc = check_common(h, ldh, wdeq, N, V, d, tgt, softcap, ws); rc) return rc;
   if (!nll) return LMCE_EINVAL;
   DevInfo di;
   if (int rc = dev_info(&di); rc) return rc;
-  if (int rc = dequant_impl(Wq, scales, V, d, group, wdeq, static_cast<cudaStream_t>(stream), di.sms); rc)
-    return rc;
-  return fwd_impl(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, LMCE_WS_INT4);
+  if (int rc = qhead_dequant_impl(head, V, d, wdeq, static_cast<cudaStream_t>(stream), di.sms); rc) return rc;
+  return fwd_impl(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, LMCE_WS_QHEAD);
+}
+
+int lmhead_ce_bwd_q(const lmce_bf16* h, int64_t ldh, const lmce_qhead* head, int64_t N, int64_t V, int64_t d,
+                    const int64_t* tgt, const uint8_t* row_mask, float softcap, const float* lse, const float* nll,
+                    float grad_scale, lmce_bf16* dh, void* ws, size_t ws_bytes, void* stream) {
+  if (int rc = check_qhead(head, V, d); rc) return rc;
+  if (!ws || !aligned16(ws) || !dh) return LMCE_EINVAL;
+  const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_QHEAD | (row_mask ? LMCE_WS_MASKED : 0u));
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  char* w = static_cast<char*>(ws);
+  lmce_bf16* wdeq = reinterpret_cast<lmce_bf16*>(w + L.wdeq);
+  if (int rc = check_common(h, ldh, wdeq, N, V, d, tgt, softcap, ws); rc) return rc;
+  if (!lse || !aligned16(dh) || !std::isfinite(grad_scale)) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = qhead_dequant_impl(head, V, d, wdeq, s, di.sms); rc) return rc;
+  return bwd_launch(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, nullptr, 0,
+                    reinterpret_cast<unsigned*>(w + L.status), w + L.bwd, di, s);
+}
+
+int lmhead_ce_fwd_bwd_q(const lmce_bf16* h, int64_t ldh, const lmce_qhead* head, int64_t N, int64_t V, int64_t d,
+                        const int64_t* tgt, const uint8_t* row_mask, float softcap, float grad_scale, float* nll,
+                        float* lse, lmce_bf16* dh, void* ws, size_t ws_bytes, void* stream) {
+  if (int rc = check_qhead(head, V, d); rc) return rc;
+  if (!ws || !aligned16(ws)) return LMCE_EINVAL;
+  const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_QHEAD | (row_mask ? LMCE_WS_MASKED : 0u));
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  lmce_bf16* wdeq = reinterpret_cast<lmce_bf16*>(static_cast<char*>(ws) + L.wdeq);
+  if (int rc = check_common(h, ldh, wdeq, N, V, d, tgt, softcap, ws); rc) return rc;
+  if (!nll || !lse || !dh || !aligned16(dh) || !std::isfinite(grad_scale)) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  if (int rc = qhead_dequant_impl(head, V, d, wdeq, static_cast<cudaStream_t>(stream), di.sms); rc) return rc;
+  return fwd_bwd_impl(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, nullptr, 0, ws,
+                      ws_bytes, stream, LMCE_WS_QHEAD);
+}
+
+int lmhead_ce_fwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
+                       int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
+                       float* nll, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  const lmce_qhead hd = int4_head(Wq, scales, group);
+  return lmhead_ce_fwd_q(h, ldh, &hd, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream);
 }
 
 int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
                        int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
                        const float* lse, const float* nll, float grad_scale, lmce_bf16* dh, void* ws,
                        size_t ws_bytes, void* stream) {
-  if (int rc = check_int4(Wq, scales, group, V, d); rc) return rc;
-  if (!ws || !aligned16(ws) || !dh) return LMCE_EINVAL;
-  const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_INT4 | (row_mask ? LMCE_WS_MASKED : 0u));
-  if (ws_bytes < L.total) return LMCE_EINVAL;
-  lmce_bf16* wdeq = reinterpret_cast<lmce_bf16*>(static_cast<char*>(ws) + L.wdeq);
-  if (int rc = check_common(h, ldh, wdeq, N, V, d, tgt, softcap, ws); rc) return rc;
-  DevInfo di;
-  if (int rc = dev_info(&di); rc) return rc;
-  if (int rc = dequant_impl(Wq, scales, V, d, group, wdeq, static_cast<cudaStream_t>(stream), di.sms); rc)
-    return rc;
-  return lmhead_ce_bwd(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, nullptr, 0, ws,
-                       ws_bytes, stream);
+  const lmce_qhead hd = int4_head(Wq, scales, group);
+  return lmhead_ce_bwd_q(h, ldh, &hd, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, ws, ws_bytes,
+                         stream);
 }
 
 int lmhead_ce_fwd_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
                            int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask,
                            float softcap, float grad_scale, float* nll, float* lse, lmce_bf16* dh, void* ws,
                            size_t ws_bytes, void* stream) {
-  if (int rc = check_int4(Wq, scales, group, V, d); rc) return rc;
-  if (!ws || !aligned16(ws)) return LMCE_EINVAL;
-  const Layout L = make_layout(N < 1 ? 1 : N, V, d, LMCE_WS_INT4 | (row_mask ? LMCE_WS_MASKED : 0u));
+  const lmce_qhead hd = int4_head(Wq, scales, group);
+  return lmhead_ce_fwd_bwd_q(h, ldh, &hd, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, ws, ws_bytes,
+                             stream);
+}
+
+int lmhead_rmsnorm_fwd(const lmce_bf16* x, int64_t ldx, const float* g, float eps, int64_t N, int64_t d,
+                       lmce_bf16* h, int64_t ldh, float* rinv, void* stream) {
+  if (int rc = check_norm(x, ldx, g, N, d); rc) return rc;
+  if (!h || !rinv || ldh < d || ldh % 8 != 0 || !aligned16(h) || !(eps >= 0.0f) || !std::isfinite(eps))
+    return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  return rmsnorm_fwd_impl(x, ldx, g, eps, N, d, h, ldh, rinv, static_cast<cudaStream_t>(stream), di.sms);
+}
+
+int lmhead_rmsnorm_bwd(const lmce_bf16* x, int64_t ldx, const float* g, const float* rinv, const lmce_bf16* dh,
+                       int64_t lddh, int64_t N, int64_t d, lmce_bf16* dx, int64_t lddx, float* dg, int accumulate_dg,
+                       void* ws, size_t ws_bytes, void* stream) {
+  if (int rc = check_norm(x, ldx, g, N, d); rc) return rc;
+  if (!rinv || !dh || !dx || lddh < d || lddh % 8 != 0 || lddx < d || lddx % 8 != 0 || !aligned16(dh) ||
+      !aligned16(dx))
+    return LMCE_EINVAL;
+  float* dgp = nullptr;
+  if (dg) {
+    if (!ws || !aligned16(ws) || (reinterpret_cast<uintptr_t>(dg) & 3u) != 0) return LMCE_EINVAL;
+    const Layout L = make_layout(N, 1, d, LMCE_WS_RMSNORM);
+    if (ws_bytes < L.dgp + sizeof(float) * kNormBlocks * d) return LMCE_EINVAL;
+    dgp = reinterpret_cast<float*>(static_cast<char*>(ws) + L.dgp);
+  }
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  return rmsnorm_bwd_impl(x, ldx, g, rinv, dh, lddh, N, d, dx, lddx, dg, accumulate_dg, dgp,
+                          static_cast<cudaStream_t>(stream));
+}
+
+int lmhead_ce_fwd_rmsnorm(const lmce_bf16* x, int64_t ldx, const float* g, float eps, const lmce_bf16* W, int64_t N,
+                          int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
+                          float* nll, float* lse, void* ws, size_t ws_bytes, void* stream) {
+  if (int rc = check_norm(x, ldx, g, N, d); rc) return rc;
+  if (!ws || !aligned16(ws) || !(eps >= 0.0f) || !std::isfinite(eps)) return LMCE_EINVAL;
+  const Layout L = make_layout(N, V, d, LMCE_WS_RMSNORM | (row_mask ? LMCE_WS_MASKED : 0u));
   if (ws_bytes < L.total) return LMCE_EINVAL;
   char* w = static_cast<char*>(ws);
-  lmce_bf16* wdeq = reinterpret_cast<lmce_bf16*>(w + L.wdeq);
-  if (int rc = check_common(h, ldh, wdeq, N, V, d, tgt, softcap, ws); rc) return rc;
-  if (!nll || !lse || !dh || !aligned16(dh)) return LMCE_EINVAL;
-  if (!std::isfinite(grad_scale)) return LMCE_EINVAL;
+  lmce_bf16* hn = reinterpret_cast<lmce_bf16*>(w + L.hn);
+  if (int rc = check_common(hn, d, W, N, V, d, tgt, softcap, ws); rc) return rc;
+  if (!nll) return LMCE_EINVAL;
   DevInfo di;
   if (int rc = dev_info(&di); rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  unsigned* status = reinterpret_cast<unsigned*>(w + L.status);
-  if (int rc = dequant_impl(Wq, scales, V, d, group, wdeq, s, di.sms); rc) return rc;
-  if (softcap <= kFusedSoftcapMax)
-    return fd_launch(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, status, di.sms, s);
-  if (int rc = fwd_impl(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream,
-                        LMCE_WS_INT4);
+  if (int rc = rmsnorm_fwd_impl(x, ldx, g, eps, N, d, hn, d, reinterpret_cast<float*>(w + L.rinv), s, di.sms); rc)
+    return rc;
+  return fwd_impl(hn, d, W, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, LMCE_WS_RMSNORM);
+}
+
+int lmhead_ce_fwd_bwd_rmsnorm(const lmce_bf16* x, int64_t ldx, const float* g, float eps, const lmce_bf16* W,
+                              int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask,
+                              float softcap, float grad_scale, float* nll, float* lse, lmce_bf16* dx, int64_t lddx,
+                              float* dg, float* dW, int accumulate, void* ws, size_t ws_bytes, void* stream) {
+  if (int rc = check_norm(x, ldx, g, N, d); rc) return rc;
+  if (!ws || !aligned16(ws) || !(eps >= 0.0f) || !std::isfinite(eps)) return LMCE_EINVAL;
+  if (dg && !dx) return LMCE_EINVAL;  // the gain's gradient comes with dx
+  if (dx && (lddx < d || lddx % 8 != 0 || !aligned16(dx))) return LMCE_EINVAL;
+  if (dg && (reinterpret_cast<uintptr_t>(dg) & 3u) != 0) return LMCE_EINVAL;
+  if (dW && !aligned16(dW)) return LMCE_EINVAL;
+  const Layout L = make_layout(N, V, d, LMCE_WS_RMSNORM | (row_mask ? LMCE_WS_MASKED : 0u));
+  if (ws_bytes < L.total) return LMCE_EINVAL;
+  char* w = static_cast<char*>(ws);
+  lmce_bf16* hn = reinterpret_cast<lmce_bf16*>(w + L.hn);
+  lmce_bf16* dhn = reinterpret_cast<lmce_bf16*>(w + L.dhn);
+  float* rinv = reinterpret_cast<float*>(w + L.rinv);
+  if (int rc = check_common(hn, d, W, N, V, d, tgt, softcap, ws); rc) return rc;
+  if (!nll || !lse || !std::isfinite(grad_scale)) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (int rc = rmsnorm_fwd_impl(x, ldx, g, eps, N, d, hn, d, rinv, s, di.sms); rc) return rc;
+  if (int rc = fwd_bwd_impl(hn, d, W, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dx ? dhn : nullptr, dW,
+                            accumulate, ws, ws_bytes, stream, LMCE_WS_RMSNORM);
       rc)
     return rc;
-  return bwd_launch(h, ldh, wdeq, N, V, d, tgt, row_mask, softcap, lse, nll, grad_scale, dh, nullptr, 0, status,
-                    w + L.bwd, di.sms, s);
+  if (!dx) return LMCE_OK;
+  return rmsnorm_bwd_impl(x, ldx, g, rinv, dhn, d, N, d, dx, lddx, dg, accumulate,
+                          reinterpret_cast<float*>(w + L.dgp), s);
 }
 
 int bpb_reduce(const float* nll, const int32_t* bytes, const uint8_t* row_mask, int64_t N, lmce_bpb_acc* acc,
@@ -506,6 +743,36 @@ int bpb_reduce(const float* nll, const int32_t* bytes, const uint8_t* row_mask, 
   return LMCE_OK;
 }
 
+int bpb_reduce_lut(const float* nll, const int64_t* tgt, const int32_t* lut, int64_t V, const uint8_t* row_mask,
+                   int64_t N, lmce_bpb_acc* acc, void* ws, size_t ws_bytes, void* stream) {
+  if (!nll || !tgt || !lut || !acc || !ws || N < 1 || V < 1) return LMCE_EINVAL;
+  if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(acc) & 7u) != 0) return LMCE_EINVAL;
+  const Layout L = make_layout(1, 1, 64, 0u);
+  if (ws_bytes < L.bpb + sizeof(lmce::BpbPartial) * lmce::kBpbBlocks) return LMCE_EINVAL;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  char* w = static_cast<char*>(ws);
+  auto* part = reinterpret_cast<lmce::BpbPartial*>(w + L.bpb);
+  lmce::count_launches(2);
+  lmce::bpb_partial_kernel<<<lmce::kBpbBlocks, lmce::kBpbThreads, 0, s>>>(
+      nll, nullptr, row_mask, N, part, tgt, lut, V, reinterpret_cast<unsigned*>(w + L.status));
+  lmce::bpb_final_kernel<<<1, lmce::kBpbBlocks, 0, s>>>(part, reinterpret_cast<lmce::BpbPartial*>(acc));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "bpb_reduce_lut launch");
+  return LMCE_OK;
+}
+
+int lmce_wait_selftest(long long limit_cycles, int arrive, void* ws, size_t ws_bytes, void* stream) {
+  if (!ws || ws_bytes < 64 || !aligned16(ws) || limit_cycles < 0) return LMCE_EINVAL;
+  DevInfo di;
+  if (int rc = dev_info(&di); rc) return rc;
+  lmce::count_launches(1);
+  lmce::wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(limit_cycles, arrive,
+                                                                               static_cast<unsigned*>(ws));
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return cuda_fail(e, "wait_selftest launch");
+  return LMCE_OK;
+}
+
 int lmce_bpb(const lmce_bpb_acc* acc, double* bpb_out) {
   if (!acc || !bpb_out) return LMCE_EINVAL;
   if (acc->sum_bytes == 0) return LMCE_EDATA;
@@ -515,11 +782,8 @@ int lmce_bpb(const lmce_bpb_acc* acc, double* bpb_out) {
 
 int lmhead_int4_dequant(const uint8_t* Wq, const lmce_f16* scales, int64_t V, int64_t d, int group, lmce_bf16* out,
                         void* stream) {
-  if (int rc = check_int4(Wq, scales, group, V, d); rc) return rc;
-  if (!out || !aligned16(out)) return LMCE_EINVAL;
-  DevInfo di;
-  if (int rc = dev_info(&di); rc) return rc;
-  return dequant_impl(Wq, scales, V, d, group, out, static_cast<cudaStream_t>(stream), di.sms);
+  const lmce_qhead hd = int4_head(Wq, scales, group);
+  return lmhead_qhead_dequant(&hd, V, d, out, stream);
 }
 
 int lmhead_tied_embed_bwd(const int64_t* ids, const lmce_bf16* g, int64_t ldg, int64_t N, int64_t V, int64_t d,
@@ -645,13 +909,17 @@ extern "C" int lmhead_ce_fwd_noalloc(const lmce_bf16* h, int64_t ldh, const lmce
   if (d % 64 != 0 || d > 512) return LMCE_ENOTSUP;
   if (ldh < d || ldh % 8 != 0) return LMCE_EINVAL;
   if (!aligned16(h) || !aligned16(W)) return LMCE_EINVAL;
-  if (!(softcap > 0.0f) || !(softcap <= softcap_max(V))) return LMCE_ENOTSUP;
+  if (!softcap_ok(softcap) || softcap_online(softcap, V)) return LMCE_ENOTSUP;  // fixed-shift form only
   DevInfo di;
   if (int rc = dev_info(&di); rc) return rc;
   unsigned char* scratch = nullptr;
   if (int rc = noalloc_scratch(di.dev, &scratch); rc) return rc;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   unsigned* status = reinterpret_cast<unsigned*>(scratch);
+  // The status word starts every call clear, so that the finalize below sees
+  // only this call's expired waits (it writes NaN rows for them).
+  cudaError_t e0 = cudaMemsetAsync(status, 0, sizeof(unsigned), s);
+  if (e0 != cudaSuccess) return cuda_fail(e0, "lmhead_ce_fwd_noalloc status reset");
 
   CUtensorMap tm_h, tm_w;
   if (int rc = lmce::make_map_bf16_3d(&tm_h, h, d, N, ldh * 2, lmce::fwdk::BM, static_cast<uint32_t>(d / 64)); rc)
@@ -666,23 +934,20 @@ extern "C" int lmhead_ce_fwd_noalloc(const lmce_bf16* h, int64_t ldh, const lmce
   p.VT = static_cast<int>(cdiv(V, lmce::fwdk::BN));
   p.N_pad = static_cast<int>(cdiv(N, lmce::fwdk::PAIR_ROWS) * lmce::fwdk::PAIR_ROWS);
   p.tgt = tgt;
-  p.inv_c = 1.0f / softcap;
-  p.c = softcap;
-  p.zlim2 = (lmce::kTanhXmax * softcap) * (lmce::kTanhXmax * softcap);
-  lmce::scaled_tanh_coeffs(static_cast<double>(softcap) * 1.4426950408889634, 1.0 / static_cast<double>(softcap),
-                           p.k);
+  fwd_params_softcap(p, softcap);
   p.part = reinterpret_cast<float*>(scratch + kNoAllocPartOff);
+  p.partm = nullptr;
   p.st = reinterpret_cast<float*>(scratch + kNoAllocStOff);
   p.status = status;
   p.maxseg = p.VT;
   const int64_t T_max = cdiv(N, lmce::fwdk::PAIR_ROWS) * p.VT;
-  const int pairs = static_cast<int>(std::min<int64_t>(T_max, lmce::fwdk::max_clusters(di.sms)));
+  const int pairs = static_cast<int>(std::min<int64_t>(T_max, lmce::fwdk::max_clusters(di.dev, di.sms)));
   lmce::count_launches(2);
   if (int rc = lmce::fwdk::launch(tm_h, tm_w, p, pairs, s); rc) return rc;
   const int fblocks = static_cast<int>(std::min<int64_t>(cdiv(N, 256), int64_t(di.sms) * 4));
   lmce::fwd_finalize_kernel<<<fblocks, 256, 0, s>>>(p.part, p.VT, pairs, lmce::fwdk::PAIR_ROWS, p.N_pad, p.st, tgt,
                                                     nullptr, static_cast<int>(N), static_cast<int>(V), nullptr, nll,
-                                                    lse, status);
+                                                    lse, status, /*nan_on_timeout=*/1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "lmhead_ce_fwd_noalloc launch");
   return LMCE_OK;

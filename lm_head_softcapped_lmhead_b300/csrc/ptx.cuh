@@ -72,7 +72,7 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t pa
 constexpr long long kWaitLimitCycles = 4000000000ll;  // ~2 s at 2 GHz
 template <bool kClusterAcquire = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
-                                          unsigned* status) {
+                                          unsigned* status, long long limit_cycles = kWaitLimitCycles) {
   const uint32_t a = smem_u32(bar);
   long long t0 = 0;
   for (uint32_t it = 0;; ++it) {
@@ -82,7 +82,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
       const long long now = clock64();
       if (t0 == 0) {
         t0 = now;
-      } else if (now - t0 > kWaitLimitCycles) {
+      } else if (now - t0 > limit_cycles) {
         *abort_flag = 1;
         atomicOr(status, ST_ETIMEOUT);
         return false;

@@ -109,6 +109,43 @@ def quantize_int4_rtn(W_bf16_bits: np.ndarray, group: int = INT4_GROUP):
     return Wq, scale16.view(np.uint16).copy()
 
 
+def quantize_int4_asym(W_bf16_bits: np.ndarray, group: int = INT4_GROUP):
+    """Harness-side asymmetric per-group int4 quantiser (input generation
+    only): per group scale = fp16((max - min) / 15) and an integer zero point
+    z = clamp(round(-min / scale), 0, 15); q = clamp(round(w / scale) + z, 0,
+    15), unsigned nibbles (element 2m in the low nibble of byte m).  Returns
+    (Wq [V, d/2] uint8, scales [V, d/group] fp16 bits, zeros [V, d/group] uint8)."""
+    W = bf16_bits_to_f32(W_bf16_bits).astype(np.float64)
+    V, d = W.shape
+    g = W.reshape(V, d // group, group)
+    lo, hi = g.min(axis=2), g.max(axis=2)
+    scale16 = ((hi - lo) / 15.0).astype(np.float16)
+    sc = scale16.astype(np.float64)
+    safe = np.where(sc > 0, sc, 1.0)
+    zero = np.clip(np.rint(-lo / safe), 0, 15)
+    q = np.clip(np.rint(g / safe[:, :, None]) + zero[:, :, None], 0, 15)
+    q = np.where(sc[:, :, None] > 0, q, zero[:, :, None]).astype(np.int64).reshape(V, d)
+    Wq = (q[:, 0::2] | (q[:, 1::2] << 4)).astype(np.uint8)
+    return Wq, scale16.view(np.uint16).copy(), zero.astype(np.uint8)
+
+
+def quantize_int8_rows(W_bf16_bits: np.ndarray, qmax: int = 127):
+    """Harness-side per-row int8 quantiser (qmax = 63 gives int7 values in the
+    same int8 storage): scale = fp16(max|w_row| / qmax), q = clamp(round(w /
+    scale), -qmax, qmax).  Returns (q [V, d] int8, scales [V] fp16 bits)."""
+    W = bf16_bits_to_f32(W_bf16_bits).astype(np.float64)
+    amax = np.abs(W).max(axis=1)
+    scale16 = (amax / qmax).astype(np.float16)
+    sc = scale16.astype(np.float64)
+    q = np.where(sc[:, None] > 0, np.rint(W / np.where(sc > 0, sc, 1.0)[:, None]), 0.0)
+    return np.clip(q, -qmax, qmax).astype(np.int8), scale16.view(np.uint16).copy()
+
+
+def to_fp16_bits(W_bf16_bits: np.ndarray) -> np.ndarray:
+    """The table stored as fp16 (round to nearest even from the bf16 values)."""
+    return bf16_bits_to_f32(W_bf16_bits).astype(np.float16).view(np.uint16).copy()
+
+
 def make_inputs(cfg: int, seed: int | None = None, N: int | None = None,
                 V: int | None = None, d: int = D_MODEL, w_scale: float = 1.0,
                 h_scale: float = 1.0) -> dict:

@@ -63,10 +63,9 @@ def test_fwd_host_validation(L):
     assert fwd(L, ldh=500) == EINVAL
     assert fwd(L, ldh=516) == EINVAL        # row pitch not a multiple of 16 bytes
     assert fwd(L, h=A + 2) == EINVAL        # misaligned base
-    assert fwd(L, c=0.0) == ENOTSUP
-    assert fwd(L, c=-1.0) == ENOTSUP
+    assert fwd(L, c=-1.0) == ENOTSUP        # softcap 0 means no cap; negative caps do not exist
     assert fwd(L, c=float("nan")) == ENOTSUP
-    assert fwd(L, c=82.0) == ENOTSUP        # above lmce_softcap_max(200) = 86 - ln 200
+    assert fwd(L, c=float("inf")) == ENOTSUP
     assert fwd(L, ws_bytes=100) == EINVAL   # workspace too small
 
 
@@ -95,7 +94,7 @@ def test_fwd_bwd_host_validation(L):
     assert fb(dh=A + 4) == EINVAL
     assert fb(dW=A + 8) == EINVAL
     assert fb(d=96) == ENOTSUP
-    assert fb(c=82.0) == ENOTSUP
+    assert fb(c=-3.0) == ENOTSUP
     assert fb(ws_bytes=100) == EINVAL
 
 
@@ -120,7 +119,7 @@ def test_fwd_bwd_int4_host_validation(L):
     assert fb(dh=0) == EINVAL                # the int4 head is frozen: dh is the only gradient
     assert fb(dh=A + 4) == EINVAL
     assert fb(w=float("nan")) == EINVAL
-    assert fb(c=82.0) == ENOTSUP
+    assert fb(c=-1.0) == ENOTSUP
     assert fb(ws_bytes=L.lmce_workspace_bytes(100, 200, 512, 0)) == EINVAL   # no room for the dequantised head
 
 
@@ -184,3 +183,64 @@ def test_valid_call_without_gpu_fails_cleanly(L):
 def test_strerror(L):
     for code in range(6):
         assert L.lmce_strerror(code)
+
+
+def test_qhead_host_validation(L):
+    """Quantised-head descriptions that fail before any launch."""
+    import lm_head_softcapped_lmhead_b300 as lm
+    P = ctypes.c_void_p
+
+    def head(fmt=lm.LMCE_QHEAD_INT4, group=64, codes=A, scales=A, zeros=A):
+        return lm._QHead(fmt, group, codes, scales, zeros)
+
+    def deq(hd, V=10, d=512, out=A):
+        return L.lmhead_qhead_dequant(ctypes.byref(hd), V, d, P(out), None)
+    assert deq(head(fmt=7)) == EINVAL
+    assert deq(head(codes=None)) == EINVAL
+    assert deq(head(group=48)) == EINVAL
+    assert deq(head(fmt=lm.LMCE_QHEAD_INT4_ASYM, zeros=None)) == EINVAL
+    assert deq(head(fmt=lm.LMCE_QHEAD_INT8_ROW, codes=A + 8)) == EINVAL     # int8 codes: 16-byte vectors
+    assert deq(head(fmt=lm.LMCE_QHEAD_INT8_ROW, scales=None)) == EINVAL
+    assert deq(head(fmt=lm.LMCE_QHEAD_FP16, codes=A + 2)) == EINVAL
+    assert deq(head(), d=96) == EINVAL
+    assert deq(head(), out=A + 2) == EINVAL
+    hd = head()
+    assert L.lmhead_ce_fwd_q(P(A), 512, ctypes.byref(hd), 100, 200, 512, P(A), None, 30.0, P(0), None, P(A),
+                             1 << 40, None) == EINVAL                      # nll required
+    assert L.lmhead_ce_fwd_bwd_q(P(A), 512, ctypes.byref(hd), 100, 200, 512, P(A), None, 30.0, 1.0, P(A), P(A),
+                                 P(0), P(A), 1 << 40, None) == EINVAL       # dh required
+    assert L.lmhead_ce_bwd_q(P(A), 512, ctypes.byref(hd), 100, 200, 512, P(A), None, 30.0, P(A), None, 1.0, P(A),
+                             P(A), 100, None) == EINVAL                     # workspace too small
+
+
+def test_rmsnorm_host_validation(L):
+    P = ctypes.c_void_p
+    fwd_n = lambda x=A, ldx=512, d=512, h=A, rinv=A, eps=1e-6: L.lmhead_rmsnorm_fwd(  # noqa: E731
+        P(x), ldx, None, eps, 100, d, P(h), 512, P(rinv), None)
+    assert fwd_n(x=0) == EINVAL
+    assert fwd_n(rinv=0) == EINVAL
+    assert fwd_n(d=96, ldx=96) == ENOTSUP
+    assert fwd_n(ldx=500) == EINVAL
+    assert fwd_n(eps=-1.0) == EINVAL
+    bwd_n = lambda dg=None, ws=A, ws_bytes=1 << 40, dx=A: L.lmhead_rmsnorm_bwd(  # noqa: E731
+        P(A), 512, None, P(A), P(A), 512, 100, 512, P(dx), 512, P(dg), 0, P(ws), ws_bytes, None)
+    assert bwd_n(dx=0) == EINVAL
+    assert bwd_n(dg=A, ws=0) == EINVAL
+    assert bwd_n(dg=A, ws_bytes=100) == EINVAL
+    fb = lambda dx=A, dg=A, ws_bytes=1 << 40: L.lmhead_ce_fwd_bwd_rmsnorm(  # noqa: E731
+        P(A), 512, None, 1e-6, P(A), 100, 200, 512, P(A), None, 30.0, 1.0, P(A), P(A), P(dx), 512, P(dg), P(A), 0,
+        P(A), ws_bytes, None)
+    assert fb(dx=0) == EINVAL                # the gain's gradient comes with dx
+    assert fb(ws_bytes=100) == EINVAL
+
+
+def test_bpb_lut_and_selftest_host_validation(L):
+    P = ctypes.c_void_p
+    lut = lambda lut_p=A, V=100, N=10: L.bpb_reduce_lut(P(A), P(A), P(lut_p), V, None, N, P(A), P(A),  # noqa: E731
+                                                         1 << 20, None)
+    assert lut(lut_p=0) == EINVAL
+    assert lut(V=0) == EINVAL
+    assert lut(N=0) == EINVAL
+    assert L.lmce_wait_selftest(100, 0, P(0), 64, None) == EINVAL
+    assert L.lmce_wait_selftest(-1, 0, P(A), 64, None) == EINVAL
+    assert L.lmce_wait_selftest(100, 0, P(A), 8, None) == EINVAL

@@ -2,7 +2,9 @@
 device memory (a host process that owns all device memory through its own
 pool, or a path that must not pay cudaMalloc's implicit synchronisation).
 Its scratch is a static device array inside the library, so it takes no
-workspace; it must give the same nll and lse as lmhead_ce_fwd.
+workspace.  It runs the same kernels in the same launch shape as
+lmhead_ce_fwd, so it must give the same bits; and its nll must match the
+oracle on sampled rows.
 
 Called through the C ABI with ctypes.  This file is collected last so that a
 run stopping at the first failure has already run every other test; it also
@@ -29,15 +31,16 @@ def lm():
     return lm
 
 
-def noalloc_fwd(lm, d_inp, c):
+def noalloc_fwd(lm, d_inp, c, tgt=None):
     N, d = d_inp["h"].shape
     V = d_inp["W"].shape[0]
+    tgt = d_inp["tgt"] if tgt is None else tgt
     nll = torch.full((N,), float("nan"), device="cuda")
     lse = torch.full((N,), float("nan"), device="cuda")
     stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
     rc = lm.lib().lmhead_ce_fwd_noalloc(ctypes.c_void_p(d_inp["h"].data_ptr()), d_inp["h"].stride(0),
                                         ctypes.c_void_p(d_inp["W"].data_ptr()), N, V, d,
-                                        ctypes.c_void_p(d_inp["tgt"].data_ptr()), c,
+                                        ctypes.c_void_p(tgt.data_ptr()), c,
                                         ctypes.c_void_p(nll.data_ptr()), ctypes.c_void_p(lse.data_ptr()), stream)
     assert rc == lm.LMCE_OK, lm.strerror(rc)
     return nll, lse
@@ -54,8 +57,10 @@ def workspace_fwd(lm, d_inp, c):
     return nll, lse
 
 
-def test_noalloc_matches_workspace_forward_two_calls(lm):
-    # Two calls in a row with different shapes share the static scratch.
+def test_noalloc_matches_workspace_forward_two_calls(lm, oracle_mod):
+    """Two calls in a row with different shapes share the static scratch; each
+    gives bit for bit the nll and lse of lmhead_ce_fwd, and its nll matches
+    the oracle on sampled rows within the nll tolerance."""
     cases = [si.make_inputs(3, N=5000, V=6000, d=512, w_scale=20.0),
              si.make_inputs(2, N=65536, V=8192, d=512)]
     for inp in cases:
@@ -63,10 +68,28 @@ def test_noalloc_matches_workspace_forward_two_calls(lm):
         a_nll, a_lse = noalloc_fwd(lm, d_inp, 30.0)
         torch.cuda.synchronize()
         b_nll, b_lse = workspace_fwd(lm, d_inp, 30.0)
-        a, b = a_nll.cpu().numpy(), b_nll.cpu().numpy()
-        assert np.all(np.isfinite(a))
-        assert np.abs(a - b).max() <= NLL_ATOL
-        assert np.abs(a_lse.cpu().numpy() - b_lse.cpu().numpy()).max() <= NLL_ATOL
+        assert torch.all(torch.isfinite(a_nll))
+        assert torch.equal(a_nll, b_nll) and torch.equal(a_lse, b_lse)
+        rows = np.random.default_rng(inp["N"]).choice(inp["N"], 24, replace=False)
+        ref_nll, _ = oracle_mod.fwd(inp["h"], inp["W"], inp["tgt"], 30.0, rows=rows)
+        assert np.abs(a_nll.cpu().numpy()[rows] - ref_nll).max() <= NLL_ATOL
+
+
+def test_noalloc_bad_target_row_is_nan(lm):
+    """A target equal to V gives NaN in that row only; the other rows are
+    those of a call with valid targets, and the next call (status word
+    cleared at its start) is clean again."""
+    inp = si.make_inputs(2, N=700, V=900, d=256)
+    d_inp = dev_inputs(inp)
+    good_nll, good_lse = noalloc_fwd(lm, d_inp, 30.0)
+    bad = d_inp["tgt"].clone()
+    bad[123] = 900
+    nll, _ = noalloc_fwd(lm, d_inp, 30.0, tgt=bad)
+    n = nll.cpu().numpy()
+    assert np.isnan(n[123]) and np.isfinite(np.delete(n, 123)).all()
+    assert np.array_equal(np.delete(n, 123), np.delete(good_nll.cpu().numpy(), 123))
+    again, _ = noalloc_fwd(lm, d_inp, 30.0)
+    assert torch.equal(again, good_nll)
 
 
 def test_noalloc_rejects_sizes_beyond_its_scratch(lm):
@@ -78,3 +101,8 @@ def test_noalloc_rejects_sizes_beyond_its_scratch(lm):
         rc = L.lmhead_ce_fwd_noalloc(P(d_inp["h"].data_ptr()), 64, P(d_inp["W"].data_ptr()), N, V, 64,
                                      P(d_inp["tgt"].data_ptr()), 30.0, P(d_inp["h"].data_ptr()), None, None)
         assert rc == lm.LMCE_EINVAL
+    # only the fixed-shift form fits its scratch: no cap and caps above lmce_softcap_max(V) are refused
+    for c in (0.0, 90.0):
+        rc = L.lmhead_ce_fwd_noalloc(P(d_inp["h"].data_ptr()), 64, P(d_inp["W"].data_ptr()), 64, 64, 64,
+                                     P(d_inp["tgt"].data_ptr()), c, P(d_inp["h"].data_ptr()), None, None)
+        assert rc == lm.LMCE_ENOTSUP
