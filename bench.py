@@ -13,8 +13,9 @@ steps.
     python bench.py --table     # every workload's call throughput, markdown (one GPU)
 
 Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
-on its own GPU (weak scaling, no data-path collective); the time is the max
-over ranks.  --impl reference times the fp64 CPU oracle on the host cores on
+on its own GPU (weak scaling) and every step ends with the data-parallel
+exchange: a sum all-reduce of dW (16 MB, NCCL) and a gather of the 24-byte
+bpb accumulators; the time is the max over ranks.  --impl reference times the fp64 CPU oracle on the host cores on
 a bounded sample of the same workload.
 """
 from __future__ import annotations
@@ -166,10 +167,14 @@ def run_ours(args, rank, world, local_rank):
         e_g = torch.from_numpy(e["g"].view(np.int16)).view(torch.bfloat16).to(dev)
         e_ws = lm.workspace(e["N"], e["V"], e["d"], lm.LMCE_WS_EMBED, device=dev)
 
+    from lm_head_softcapped_lmhead_b300 import dist as ldist
+    gathered = []
+
     # One step: forward + dh in one pass, the bits-per-byte sums, then the dW
-    # pass (which needs the forward's lse), each call bracketed by events.
+    # pass (which needs the forward's lse), each call bracketed by events;
+    # with several ranks, then the gradient and bpb exchange.
     def step(events=None):
-        ev = events or [None] * 4
+        ev = events or [None] * 5
         if ev[0] is not None:
             ev[0].record(stream)
         if args.profile_step == "embed":
@@ -195,6 +200,14 @@ def run_ours(args, rank, world, local_rank):
                          nll=nll)
         if ev[3] is not None:
             ev[3].record(stream)
+        if world > 1:
+            # The data-parallel exchange: the tied table's gradient (a 16 MB
+            # sum all-reduce) and the 24-byte bpb accumulators (gathered on
+            # the device, combined in rank order after the run).
+            ldist.allreduce_dW(dW)
+            gathered.append(ldist.allgather_bpb_acc(acc))
+        if ev[4] is not None:
+            ev[4].record(stream)
 
     def barrier():
         if world > 1:
@@ -220,7 +233,7 @@ def run_ours(args, rank, world, local_rank):
     if lm.lmce_status(ws, stream) != lm.LMCE_OK:
         raise RuntimeError("device status after warm-up is not OK")
 
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(args.steps)]
     barrier()
     torch.cuda.synchronize()
     launches0 = lm.lmce_launch_count()
@@ -236,10 +249,13 @@ def run_ours(args, rank, world, local_rank):
     if lm.lmce_status(ws, stream) != lm.LMCE_OK:
         raise RuntimeError("device status after the timed steps is not OK")
 
-    step_ms = [e[0].elapsed_time(e[3]) for e in evs]
+    step_ms = [e[0].elapsed_time(e[4]) for e in evs]
     part_ms = {"fwd_dh": [e[0].elapsed_time(e[1]) for e in evs],
                "bpb_reduce": [e[1].elapsed_time(e[2]) for e in evs],
                "bwd_dW": [e[2].elapsed_time(e[3]) for e in evs]}
+    if world > 1:
+        part_ms["dp_exchange"] = [e[3].elapsed_time(e[4]) for e in evs]
+    bpb_all = ldist.combine_bpb_acc(gathered[-1]) if gathered else None
     total_ms = sum(step_ms)
 
     if args.profile:
@@ -316,13 +332,15 @@ def run_ours(args, rank, world, local_rank):
         "dtype": "bf16", "data": "synthetic (seeded PCG64; FineWeb-shaped: d=512, V=8192, seq 2048)",
         "config": {"workload": WORKLOAD, "N": N, "V": V, "d": d, "softcap": SOFTCAP, "loss": "mean",
                    "l2": "flushed between steps (256 MB write outside the timed events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+                   "parallelism": f"dp{world}: row shards, dW all-reduce (NCCL) + bpb gather each step"
+                   if world > 1 else "single GPU"},
         "roofline": {"bound": "tensor", "kernel": dom, "achieved": achieved, "peak": peak_burst,
                      "unit": "TFLOP/s", "frac": achieved / peak_burst, "peak_source": f"{peak_src} bf16 burst",
                      "frac_of_sustained": achieved / peak_sust, "traffic": ncu_traffic(dom),
                      "traffic_unit": "bytes/launch (ncu dram read + write)",
                      "flops_per_launch": fpt[dom] * N},
         "kernels_ms": avg,
+        "bpb_all_ranks": bpb_all,
         "mfu_6NVd": model_flops / (ms_step / 1e3) / 1e12 / peak_burst,
         "tensor_frac_exec_8NVd": exec_flops / (ms_step / 1e3) / 1e12 / peak_burst,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

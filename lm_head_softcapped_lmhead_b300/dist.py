@@ -45,6 +45,27 @@ def allreduce_bpb(local: tuple, group=None) -> tuple:
     return combine_bpb(parts)
 
 
+def allgather_bpb_acc(acc: torch.Tensor, group=None) -> torch.Tensor:
+    """Device-side exchange of the 24-byte bpb accumulators (no host sync):
+    returns a [world, 3] float64 tensor whose row r holds rank r's
+    accumulator bytes (sum_nll, then the two int64 counts bit-cast); combine
+    it with :func:`combine_bpb_acc` in rank order when the values are needed."""
+    import torch.distributed as dist
+
+    world = dist.get_world_size(group)
+    out = torch.empty((world, 3), dtype=torch.float64, device=acc.device)
+    dist.all_gather(list(out.unbind(0)), acc.reshape(3).contiguous(), group=group)
+    return out
+
+
+def combine_bpb_acc(gathered: torch.Tensor) -> tuple:
+    """(sum_nll, sum_bytes, n) from allgather_bpb_acc's [world, 3] tensor,
+    added in rank order."""
+    g = gathered.detach().cpu().contiguous()
+    ints = g.view(torch.int64)
+    return combine_bpb([(float(g[r, 0]), int(ints[r, 1]), int(ints[r, 2])) for r in range(g.shape[0])])
+
+
 def allreduce_dW(dW: torch.Tensor, group=None) -> torch.Tensor:
     """Sum the tied-table gradient over ranks in place."""
     import torch.distributed as dist

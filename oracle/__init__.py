@@ -108,6 +108,8 @@ def _load():
         lib.oracle_rmsnorm_fwd_f64.restype = ctypes.c_int
         lib.oracle_rmsnorm_bwd_f64.argtypes = [P, P, D, P, I64, I64, P, P]
         lib.oracle_rmsnorm_bwd_f64.restype = ctypes.c_int
+        lib.oracle_f64_to_bf16_rne_array.argtypes = [P, P, I64]
+        lib.oracle_f64_to_bf16_rne_array.restype = None
         lib.oracle_bf16_to_f64_array.argtypes = [P, P, I64]
         lib.oracle_bf16_to_f64_array.restype = None
         lib.oracle_f16_to_f64.argtypes = [ctypes.c_uint16]
@@ -150,6 +152,14 @@ def f16_to_f64(bits: int) -> float:
 
 def f64_to_bf16_rne(x: float) -> int:
     return int(_load().oracle_f64_to_bf16_rne(float(x)))
+
+
+def round_bf16(x) -> np.ndarray:
+    """float64 array -> bf16 bit patterns (uint16), round to nearest even."""
+    x = _c(x, np.float64)
+    out = np.empty(x.shape, dtype=np.uint16)
+    _load().oracle_f64_to_bf16_rne_array(_ptr(x), _ptr(out), x.size)
+    return out
 
 
 def _as_f64(x):

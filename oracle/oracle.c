@@ -124,6 +124,10 @@ void oracle_bf16_to_f64_array(const uint16_t* in, double* out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = oracle_bf16_to_f64(in[i]);
 }
 
+void oracle_f64_to_bf16_rne_array(const double* in, uint16_t* out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = oracle_f64_to_bf16_rne(in[i]);
+}
+
 /* ---- forward: softcapped cross-entropy of the tied head ---------------- */
 
 /* One row's forward.  s must hold V doubles of scratch. */

@@ -1,7 +1,8 @@
 """Multi-rank host logic on CPU: two gloo ranks each score a contiguous row
-shard (with the CPU oracle standing in for a GPU's forward), then combine the
-bits-per-byte sums and the dW gradient; the result equals the single-process
-answer."""
+shard (with the CPU oracle standing in for a GPU's forward), add their input
+positions' embedding gradients into the same table gradient, then combine
+the bits-per-byte sums and dW; the result equals the single-process answer
+(head dW plus every position's embedding gradient)."""
 import math
 import os
 import socket
@@ -40,10 +41,18 @@ def _worker(rank, world, port, out_path):
     _, sn, sb, n = oracle.bpb(nll, inp["nbytes"][a:b])
     tot = ld.allreduce_bpb((sn, sb, n))
     _, dW = oracle.bwd(inp["h"][a:b], inp["W"], inp["tgt"][a:b], 30.0, lse, 1.0 / inp["N"], want_dh=False)
+    # the rank's input positions' embedding gradients join the same table gradient before the exchange
+    e = si.make_embed_inputs(N=101, V=64, d=64, seed=77)
+    dW = dW + oracle.embed_bwd(e["ids"][a:b], e["g"][a:b], 64)
     dWt = torch.from_numpy(dW)
     ld.allreduce_dW(dWt)
+    # the accumulator exchange the benchmark uses (24 bytes per rank, combined in rank order)
+    acc = torch.tensor([sn, 0.0, 0.0], dtype=torch.float64)
+    acc.view(torch.int64)[1] = sb
+    acc.view(torch.int64)[2] = n
+    tot2 = ld.combine_bpb_acc(ld.allgather_bpb_acc(acc))
     if rank == 0:
-        np.savez(out_path, sn=tot[0], sb=tot[1], n=tot[2], dW=dWt.numpy())
+        np.savez(out_path, sn=tot[0], sb=tot[1], n=tot[2], dW=dWt.numpy(), sn2=tot2[0], sb2=tot2[1], n2=tot2[2])
     dist.barrier()
     dist.destroy_process_group()
 
@@ -69,5 +78,8 @@ def test_two_gloo_ranks_match_single_process(tmp_path, oracle_mod):
     b, sn, sb, n = oracle_mod.bpb(nll, inp["nbytes"])
     assert int(got["sb"]) == sb and int(got["n"]) == n
     assert float(got["sn"]) == pytest.approx(sn, rel=1e-13)
+    assert (float(got["sn2"]), int(got["sb2"]), int(got["n2"])) == (float(got["sn"]), int(got["sb"]), int(got["n"]))
     _, dW = oracle_mod.bwd(inp["h"], inp["W"], inp["tgt"], 30.0, lse, 1.0 / inp["N"], want_dh=False)
+    e = si.make_embed_inputs(N=101, V=64, d=64, seed=77)
+    dW = dW + oracle_mod.embed_bwd(e["ids"], e["g"], 64)
     assert np.allclose(got["dW"], dW, rtol=0, atol=1e-14)

@@ -272,7 +272,12 @@ def test_rmsnorm_kernels_match_oracle(lm, oracle_mod, with_gain):
 @pytest.mark.parametrize("masked", [False, True])
 def test_rmsnorm_head_training_step(lm, oracle_mod, masked):
     """lmhead_ce_fwd_bwd_rmsnorm (normalise, forward + dh, dW, then dx and dg)
-    against the oracle's RMSNorm -> forward -> backward -> RMSNorm backward."""
+    against the oracle's RMSNorm -> forward -> backward -> RMSNorm backward.
+    The normalised rows enter the head as bf16 (the model's dtype; the
+    forward + backward workload's hidden states are RMSNorm rows rounded to
+    bf16), so the oracle's head runs on its RMSNorm output rounded once to
+    bf16, and the RMSNorm backward takes the head's dh with respect to those
+    rows."""
     N, V, d, c, eps = 600, 900, 256, 30.0, 1e-6
     x, g, inp = _norm_inputs(N, V, d)
     mask = (np.arange(N) % 4 != 1).astype(np.uint8) if masked else None
@@ -290,7 +295,7 @@ def test_rmsnorm_head_training_step(lm, oracle_mod, masked):
     lm.lmhead_ce_fwd_bwd_rmsnorm(tx, tg, eps, d_inp["W"], d_inp["tgt"], c, w, nll, lse, dx=dx, dg=dg, dW=dW,
                                  row_mask=tm, ws=ws)
     assert lm.lmce_status(ws) == lm.LMCE_OK
-    hn, _ = oracle_mod.rmsnorm_fwd(x, g, eps)
+    hn = oracle_mod.round_bf16(oracle_mod.rmsnorm_fwd(x, g, eps)[0])
     ref_nll, ref_lse = oracle_mod.fwd(hn, inp["W"], inp["tgt"], c, mask=mask)
     assert np.abs(nll.cpu().numpy() - ref_nll).max() <= NLL_ATOL
     ref_dhn, ref_dW = oracle_mod.bwd(hn, inp["W"], inp["tgt"], c, ref_lse, w, mask=mask)

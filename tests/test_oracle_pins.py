@@ -60,6 +60,18 @@ def test_bf16_rounding_matches_torch(oracle_mod):
     assert np.array_equal(got, ref)
 
 
+def test_round_bf16_array_matches_scalar_and_torch(oracle_mod):
+    """The array form of the bf16 rounding equals the scalar one and torch's
+    float64 -> bfloat16 on randoms, ties and edge values."""
+    rng = np.random.default_rng(13)
+    x = np.concatenate([rng.standard_normal(2000) * 10.0 ** rng.integers(-40, 39, 2000),
+                        [0.0, -0.0, 1.0 + 2.0 ** -8, 1.0 + 3 * 2.0 ** -8, 3.4e38, -1e-45, np.inf]])
+    got = oracle_mod.round_bf16(x)
+    assert np.array_equal(got, np.array([oracle_mod.f64_to_bf16_rne(float(v)) for v in x], dtype=np.uint16))
+    ref = torch.from_numpy(x).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(got, ref)
+
+
 def test_widen_bf16_exact(oracle_mod):
     bits = np.arange(0, 65536, 7, dtype=np.uint16)
     ref = torch.from_numpy(bits.view(np.int16).copy()).view(torch.bfloat16).to(torch.float64).numpy()
