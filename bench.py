@@ -568,6 +568,25 @@ def run_table(args):
         tf = lambda k: k * M * V * d / (ms * 1e-3) / 1e12 / peak  # noqa: E731
         rows.append((cfg, what, N, V, M / ms * 1e3, ms, tf(exec_f), tf(model_f), o_rate, S))
         del inp
+    # The int4 head's forward two ways: dequantised once into a bf16 copy
+    # (lmhead_ce_fwd_int4) or inside the forward kernel
+    # (lmhead_ce_fwd_int4_inkernel), at the full batch and at small ones.
+    q5 = si.make_inputs(5)
+    Wq5 = torch.from_numpy(q5["Wq"]).to(dev)
+    sc5 = torch.from_numpy(q5["scales"].view(np.int16)).to(dev)
+    for Nq in (512, 4096, 65536):
+        hq = bf(q5["h"][:Nq])
+        tq = torch.from_numpy(q5["tgt"][:Nq]).to(dev)
+        nq = torch.empty(Nq, device=dev)
+        wsa = lm.workspace(Nq, q5["V"], q5["d"], lm.LMCE_WS_INT4, device=dev)
+        wsb = lm.workspace(Nq, q5["V"], q5["d"], device=dev)
+        ms_a = gpu_ms(lambda: lm.lmhead_ce_fwd_int4(hq, Wq5, sc5, si.INT4_GROUP, SOFTCAP, tq, nq, ws=wsa,
+                                                     stream=stream))
+        ms_b = gpu_ms(lambda: lm.lmhead_ce_fwd_int4_inkernel(hq, Wq5, sc5, si.INT4_GROUP, SOFTCAP, tq, nq, ws=wsb,
+                                                              stream=stream))
+        notes.append(f"int4 head forward, N={Nq}: dequantise once + bf16 forward {ms_a:.4f} ms, "
+                     f"dequantised in the kernel {ms_b:.4f} ms")
+    del q5
     # The tied table's gradient through the input embedding (HBM-bound):
     # the training micro-batch's input positions, Zipf token ids.
     e = si.make_embed_inputs()

@@ -203,6 +203,20 @@ LMCE_API int lmhead_ce_fwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* 
                        int64_t N, int64_t V, int64_t d, const int64_t* tgt, const uint8_t* row_mask, float softcap,
                        float* nll, float* lse, void* ws, size_t ws_bytes, void* stream);
 
+/* The same forward as lmhead_ce_fwd_int4 with the dequantisation inside the
+ * forward kernel: the packed nibbles stream through the kernel's ring (a
+ * quarter of the bf16 head's bytes) and converter warps write each stage's
+ * bf16 tile (bf16_rne(q * scale), bit-exact, so nll and lse are bit for bit
+ * those of lmhead_ce_fwd_int4).  Needs no room for a dequantised copy: the
+ * workspace is lmce_workspace_bytes(N, V, d, row_mask ? LMCE_WS_MASKED : 0).
+ * Wq must be 16-byte aligned.  lmhead_ce_fwd_int4 (dequantise once, then
+ * the bf16 forward) is faster on large batches; this call saves the 2 V d
+ * byte copy and its pass, which pays on small ones. */
+LMCE_API int lmhead_ce_fwd_int4_inkernel(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales,
+                                         int group, int64_t N, int64_t V, int64_t d, const int64_t* tgt,
+                                         const uint8_t* row_mask, float softcap, float* nll, float* lse, void* ws,
+                                         size_t ws_bytes, void* stream);
+
 /* Backward for the int4 head: dh only (the quantised head is frozen).
  * Same layout rules as lmhead_ce_fwd_int4 and lmhead_ce_bwd. */
 LMCE_API int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,

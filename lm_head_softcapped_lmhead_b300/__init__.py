@@ -37,6 +37,7 @@ EXPORTS = (
     "lmhead_ce_fwd_bwd", "lmhead_ce_fwd_bwd_int4", "lmhead_tied_embed_bwd", "lmhead_ce_fwd_q", "lmhead_ce_bwd_q",
     "lmhead_ce_fwd_bwd_q", "lmhead_qhead_dequant", "lmhead_rmsnorm_fwd", "lmhead_rmsnorm_bwd",
     "lmhead_ce_fwd_rmsnorm", "lmhead_ce_fwd_bwd_rmsnorm", "bpb_reduce_lut", "lmce_wait_selftest",
+    "lmhead_ce_fwd_int4_inkernel",
 )
 
 _lib = None
@@ -100,6 +101,7 @@ def lib():
                                            P], I),
             "bpb_reduce_lut": ([P, P, P, I64, P, I64, P, P, SZ, P], I),
             "lmce_wait_selftest": ([ctypes.c_longlong, I, P, SZ, P], I),
+            "lmhead_ce_fwd_int4_inkernel": ([P, I64, P, P, I, I64, I64, I64, P, P, F, P, P, P, SZ, P], I),
         }
         for name, (args, res) in sig.items():
             fn = getattr(L, name)
@@ -207,6 +209,18 @@ def lmhead_ce_fwd_int4(h, Wq, scales, group, softcap, tgt, nll, lse=None, row_ma
                                   _p(row_mask), float(softcap), _p(nll), _p(lse), _p(ws), ws.numel(),
                                   _stream(stream))
     _check(rc, "lmhead_ce_fwd_int4")
+
+
+def lmhead_ce_fwd_int4_inkernel(h, Wq, scales, group, softcap, tgt, nll, lse=None, row_mask=None, ws=None,
+                                stream=None):
+    """lmhead_ce_fwd_int4 with the dequantisation inside the forward kernel."""
+    _bf16_bits(h, "h")
+    N, d = h.shape
+    V = Wq.shape[0]
+    rc = lib().lmhead_ce_fwd_int4_inkernel(_p(h), h.stride(0), _p(Wq), _p(scales), int(group), N, V, d, _p(tgt),
+                                           _p(row_mask), float(softcap), _p(nll), _p(lse), _p(ws), ws.numel(),
+                                           _stream(stream))
+    _check(rc, "lmhead_ce_fwd_int4_inkernel")
 
 
 def lmhead_ce_bwd_int4(h, Wq, scales, group, softcap, tgt, lse, grad_scale, dh, row_mask=None, ws=None,

@@ -44,6 +44,9 @@
 
 #include <string>
 
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
 #include "ptx.cuh"
 #include "softcap_math.cuh"
 
@@ -57,21 +60,44 @@ constexpr int BN = 256;        // vocab per tile (pair MMA N)
 constexpr int HALF_N = BN / 2; // vocab rows of a tile loaded by each CTA
 constexpr int KB = 64;         // K elements per chunk (one 128-byte swizzle row)
 constexpr int SC = 2;          // chunks per ring stage (one 32 KB TMA load)
-constexpr int STAGES = 3;      // ring depth
 constexpr int MAX_KC = 8;      // d <= 512
 constexpr int EPI_WARPS = 8;
 constexpr int TMA_WARP = 8;
 constexpr int MMA_WARP = 9;
-constexpr int THREADS = 320;
 constexpr uint32_t X_CHUNK = BM * KB * 2;      // 16 KB: 128 rows x 64
 constexpr uint32_t W_CHUNK = HALF_N * KB * 2;  // 16 KB: 128 vocab rows x 64
 constexpr uint32_t STAGE = SC * W_CHUNK;       // 32 KB
 constexpr uint32_t SMEM_X = 0;
-constexpr uint32_t SMEM_RING = SMEM_X + MAX_KC * X_CHUNK;
-constexpr uint32_t SMEM_BAR = SMEM_RING + STAGES * STAGE;
-constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;  // + barriers + alignment slack
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_ROWS, BN, false, false);
+
+// Shared-memory plan of the bf16 form: h block (128 KB), then a ring of
+// 3 x 32 KB W stages (two 64-column chunks each), barriers (256 B) and
+// alignment slack (1 KB).
+// The int4 form (kInt4): the head arrives as packed nibbles (8 KB per CTA
+// and stage: 128 vocab rows x 64 bytes = 128 columns of d) through a 3-stage
+// ring, and CONV_WARPS converter warps write each stage's bf16 tile (the
+// 128B-swizzled layout the TMA writes in the bf16 form) into a 2 x 32 KB
+// ring.  (One-chunk stages, 4 x 16 KB, were slower: each stage hand-off
+// between the converters and the pair MMA costs about the same time
+// whatever the stage's size.)
+template <bool kInt4>
+struct FCfg {
+  static constexpr int SC = 2;                        // 64-column chunks per stage
+  static constexpr uint32_t STAGE = SC * W_CHUNK;     // bytes of one bf16 stage
+  static constexpr int STAGES = kInt4 ? 2 : 3;        // bf16 ring stages
+  static constexpr int PSTAGES = kInt4 ? 3 : 0;       // packed ring stages
+  static constexpr int CONV_WARPS = kInt4 ? 2 : 0;    // warps 10, 11
+  static constexpr int THREADS = 320 + 32 * CONV_WARPS;
+  static constexpr uint32_t PK_ROW = 32 * SC;         // packed bytes per vocab row and stage
+  static constexpr uint32_t PK_STAGE = HALF_N * PK_ROW;
+  static constexpr uint32_t SMEM_RING = SMEM_X + MAX_KC * X_CHUNK;
+  static constexpr uint32_t SMEM_PK = SMEM_RING + STAGES * STAGE;
+  static constexpr uint32_t SMEM_BAR = SMEM_PK + PSTAGES * PK_STAGE;
+  static constexpr uint32_t SMEM_BYTES = SMEM_BAR + 256 + 1024;
+  static_assert(SMEM_BYTES <= 232448, "shared memory above the 227 KB per-CTA limit");
+  static_assert(STAGES <= 4 && PSTAGES <= 6, "mbarrier slots");
+};
 
 struct Params {
   int N;                // rows addressed by the h tensor map
@@ -87,6 +113,8 @@ struct Params {
   float* partm;         // online form: [2 maxseg][N_pad] base-2 running maxima of the partials
   float* st;            // [N] e^{s_t}, the target column's term (online form: a_t = s_t log2 e)
   unsigned* status;
+  const __half* qscales;  // int4 form: [V, d / qgroup] fp16 scales
+  int qgroup;             // int4 form: elements per scale group along d
 };
 
 // Exact-form sum for chunks whose |z| may exceed the polynomial range.  Out
@@ -272,10 +300,51 @@ __device__ __forceinline__ void chunk_terms_online(const uint32_t (&r)[32], cons
   }
 }
 
-template <bool kOnline>
-__global__ void __launch_bounds__(THREADS, 1)
+// ---- int4 form: converter -------------------------------------------------------
+// Eight packed nibbles (one 32-bit word: element 2m in the low nibble of byte
+// m, two's complement) times their fp16 group scale -> eight bf16 values
+// bf16_rne(q * scale), packed as one 16-byte unit.  Exact as the
+// dequantisation kernel: 2^23 + (n ^ 8) is built from the bits, minus
+// 2^23 + 8 gives q, q * scale is exact in fp32, and the one rounding is the
+// RNE to bf16.
+__device__ __forceinline__ uint32_t pack_bf16x2_rn(float lo, float hi) {
+  __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&b);
+}
+__device__ __forceinline__ uint4 int4_word_to_bf16x8(uint32_t w, float scale) {
+  const float2 off = make_float2(-8388616.0f, -8388616.0f);  // -(2^23 + 8)
+  const float2 s2 = make_float2(scale, scale);
+  const uint32_t x = w ^ 0x88888888u;
+  uint32_t out[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 f = make_float2(__uint_as_float(0x4B000000u | ((x >> (8 * j)) & 0xFu)),
+                                 __uint_as_float(0x4B000000u | ((x >> (8 * j + 4)) & 0xFu)));
+    const float2 v = __fmul2_rn(__fadd2_rn(f, off), s2);
+    out[j] = pack_bf16x2_rn(v.x, v.y);
+  }
+  return make_uint4(out[0], out[1], out[2], out[3]);
+}
+
+// Converter lane layout: in iteration i (0..15) lane l of converter warp cw
+// handles row r = 64 cw + 4 i + l / 8 of the CTA's 128 vocab rows and the
+// 16-byte unit u = l % 8 (8 columns) of each 64-column chunk of the stage, so
+// a warp reads 4 consecutive packed rows and writes 4 whole 128-byte rows of
+// the swizzled bf16 chunk per instruction.
+constexpr int CONV_ITERS = 16;
+
+template <bool kOnline, bool kInt4 = false>
+__global__ void __launch_bounds__(FCfg<kInt4>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
                const Params p) {
+  // tm_w: the head's bf16 rows (box 64 x 128 x 2), or in the int4 form its
+  // packed bytes (2-D uint8, box 64 bytes x 128 rows).
+  using C = FCfg<kInt4>;
+  constexpr int SC = C::SC;
+  constexpr uint32_t STAGE = C::STAGE;
+  constexpr int STAGES = C::STAGES;
+  constexpr uint32_t SMEM_RING = C::SMEM_RING;
+  constexpr uint32_t SMEM_BAR = C::SMEM_BAR;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + SMEM_BAR);
@@ -286,8 +355,11 @@ __global__ void __launch_bounds__(THREADS, 1)
   uint64_t* acc_full = bars + 10;   // [2] each CTA
   uint64_t* acc_empty = bars + 12;  // [2] leader: 8 warps of each CTA
   uint64_t* mma_done = bars + 14;   // each CTA
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 192);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 196);
+  uint64_t* pk_full = bars + 15;    // [PSTAGES] int4 form, each CTA: the packed bytes have landed
+  uint64_t* pk_empty = bars + 21;   // [PSTAGES] int4 form, each CTA: the converters have read them
+  // 27 mbarriers (216 bytes), then the TMEM address and the abort flag.
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + SMEM_BAR + 248);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + SMEM_BAR + 252);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -305,8 +377,13 @@ __global__ void __launch_bounds__(THREADS, 1)
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(full + i, 1);
+      // bf16 form: the leader's expect_tx; int4 form: every converter warp of both CTAs
+      mbar_init(full + i, kInt4 ? 2 * C::CONV_WARPS : 1);
       mbar_init(empty + i, 1);
+    }
+    for (int i = 0; i < C::PSTAGES; ++i) {
+      mbar_init(pk_full + i, 1);                  // the TMA warp's expect_tx (+ the bytes)
+      mbar_init(pk_empty + i, C::CONV_WARPS);     // every converter warp has read the stage
     }
     mbar_init(x_full, 1);
     mbar_init(x_empty, 1);
@@ -341,7 +418,7 @@ __global__ void __launch_bounds__(THREADS, 1)
       uint32_t phase = 0, xph = 0;
       int prev_rbp = -1;
       uint32_t pend = 0;
-      uint32_t pend_ph[STAGES] = {0, 0, 0};
+      uint32_t pend_ph[6] = {0, 0, 0, 0, 0, 0};
       bool ok = true;
       for (long long g = g_begin; g < g_end && ok; ++g) {
         const int rbp = static_cast<int>(g / p.VT);
@@ -357,20 +434,39 @@ __global__ void __launch_bounds__(THREADS, 1)
           prev_rbp = rbp;
         }
         for (int pr = 0; pr < npair; ++pr) {
-          ok = mbar_wait(empty + stage, phase ^ 1u, abort_flag, p.status);
-          if (!ok) break;
-          if (leader) mbar_expect_tx(full + stage, 2u * STAGE);
-          tma_load_3d_pair(smem + SMEM_RING + stage * STAGE, &tm_w, mapa_shared(smem_u32(full + stage), 0), 0,
-                           vt * BN + static_cast<int>(rank) * HALF_N, SC * pr);
+          if constexpr (kInt4) {
+            // Packed bytes of the stage (this CTA's 128 vocab rows, 64 bytes
+            // = 128 columns of d each) into the packed ring; the converters
+            // fill the bf16 stage from it.
+            ok = mbar_wait(pk_empty + stage, phase ^ 1u, abort_flag, p.status);
+            if (!ok) break;
+            mbar_expect_tx(pk_full + stage, C::PK_STAGE);
+            tma_load_2d(smem + C::SMEM_PK + stage * C::PK_STAGE, &tm_w, pk_full + stage, C::PK_ROW * pr,
+                        vt * BN + static_cast<int>(rank) * HALF_N);
+          } else {
+            ok = mbar_wait(empty + stage, phase ^ 1u, abort_flag, p.status);
+            if (!ok) break;
+            if (leader) mbar_expect_tx(full + stage, 2u * STAGE);
+            tma_load_3d_pair(smem + SMEM_RING + stage * STAGE, &tm_w, mapa_shared(smem_u32(full + stage), 0), 0,
+                             vt * BN + static_cast<int>(rank) * HALF_N, SC * pr);
+          }
           pend |= 1u << stage;
           pend_ph[stage] = phase;
-          if (++stage == STAGES) {
+          if (++stage == (kInt4 ? C::PSTAGES : STAGES)) {
             stage = 0;
             phase ^= 1u;
           }
         }
       }
-      if (!ok && leader) {
+      if (!ok && kInt4) {
+        // Bounded wait for this CTA's packed loads (they complete locally).
+        const long long t0 = clock64();
+        for (int s = 0; s < C::PSTAGES; ++s)
+          if (pend & (1u << s))
+            while (!mbar_try_wait(smem_u32(pk_full + s), pend_ph[s]) && clock64() - t0 < kWaitLimitCycles) {
+            }
+      }
+      if (!ok && leader && !kInt4) {
         // Bounded wait for issued copies to land (the leader's full barriers
         // count both CTAs' bytes; the peer leaves only after the leader,
         // through the final cluster barrier).
@@ -401,7 +497,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           tc_fence_after();
           const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
           for (int pr = 0; pr < npair && ok; ++pr) {
-            ok = mbar_wait(full + stage, phase, abort_flag, p.status);
+            ok = mbar_wait<kInt4>(full + stage, phase, abort_flag, p.status);
             if (!ok) break;
             tc_fence_after();
             for (int c = 0; c < SC; ++c) {
@@ -433,6 +529,84 @@ __global__ void __launch_bounds__(THREADS, 1)
       // TMEM is released (bounded).
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(mma_done), 0) && clock64() - t0 < kWaitLimitCycles) {
+      }
+    }
+  } else if (kInt4 && warp > MMA_WARP) {
+    // ---------------- converter warps (int4 form) ----------------
+    // Each stage (128 columns of d) of this CTA's 128 vocab rows of the W
+    // tile: packed ring slot -> bf16 ring slot.  The fp16 scales of the next
+    // stage are loaded into registers while this one is converted.
+    if (g_begin < g_end) {
+      const int cw = warp - MMA_WARP - 1;
+      const int u = lane & 7;
+      const int rsub = lane >> 3;
+      const int ngr = p.d / p.qgroup;  // scales per vocab row
+      const uint32_t lead_full = mapa_shared(smem_u32(full), 0);
+      // scales of stage (g, pr) for this lane's 16 rows and both chunks
+      auto load_scales = [&](long long g, int pr, float (&sc)[CONV_ITERS][2]) {
+        const int vt = static_cast<int>(g % p.VT);
+        const int gi0 = (64 * SC * pr + 8 * u) / p.qgroup;
+        const int gi1 = (64 * SC * pr + 64 + 8 * u) / p.qgroup;
+        const bool two = SC == 2 && SC * pr + 1 < p.KC;
+#pragma unroll
+        for (int i = 0; i < CONV_ITERS; ++i) {
+          const long long v = static_cast<long long>(vt) * BN + static_cast<int>(rank) * HALF_N + 64 * cw + 4 * i + rsub;
+          const bool valid = v < p.V;
+          const __half* row = p.qscales + (valid ? v : 0) * ngr;
+          sc[i][0] = valid ? __half2float(row[gi0]) : 0.f;
+          sc[i][1] = (valid && two) ? __half2float(row[gi1]) : 0.f;
+        }
+      };
+      float sc_cur[CONV_ITERS][2], sc_nxt[CONV_ITERS][2];
+      load_scales(g_begin, 0, sc_cur);
+      int stage = 0, ps = 0;
+      uint32_t phase = 0, pph = 0;
+      bool ok = true;
+      for (long long g = g_begin; g < g_end && ok; ++g) {
+        for (int pr = 0; pr < npair; ++pr) {
+          // the following stage's scales, in flight during this stage
+          const bool more = (pr + 1 < npair) || (g + 1 < g_end);
+          if (more) load_scales(pr + 1 < npair ? g : g + 1, pr + 1 < npair ? pr + 1 : 0, sc_nxt);
+          ok = mbar_wait(pk_full + ps, pph, abort_flag, p.status);
+          if (ok) ok = mbar_wait(empty + stage, phase ^ 1u, abort_flag, p.status);
+          if (!ok) break;
+          const int nch = min(SC, p.KC - SC * pr);
+          uint8_t* dst = smem + SMEM_RING + stage * STAGE;
+          const uint8_t* pk = smem + C::SMEM_PK + ps * C::PK_STAGE;
+#pragma unroll
+          for (int i = 0; i < CONV_ITERS; ++i) {
+            const int r = 64 * cw + 4 * i + rsub;
+#pragma unroll
+            for (int c = 0; c < SC; ++c) {
+              if (c < nch) {
+                const uint32_t w = *reinterpret_cast<const uint32_t*>(pk + r * C::PK_ROW + c * 32 + u * 4);
+                *reinterpret_cast<uint4*>(dst + c * W_CHUNK + r * 128 + ((u ^ (r & 7)) << 4)) =
+                    int4_word_to_bf16x8(w, sc_cur[i][c]);
+              }
+            }
+          }
+          // The bf16 tile is visible to the tensor core (async proxy) before
+          // the leader's MMA is told that it is full.
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(pk_empty + ps);
+            mbar_arrive_cluster(lead_full + static_cast<uint32_t>(stage) * 8u);
+          }
+          if (++stage == STAGES) {
+            stage = 0;
+            phase ^= 1u;
+          }
+          if (++ps == C::PSTAGES) {
+            ps = 0;
+            pph ^= 1u;
+          }
+#pragma unroll
+          for (int i = 0; i < CONV_ITERS; ++i) {
+            sc_cur[i][0] = sc_nxt[i][0];
+            sc_cur[i][1] = sc_nxt[i][1];
+          }
+        }
       }
     }
   } else {
@@ -537,14 +711,15 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // Co-resident 2-CTA clusters of fwd_kernel on device `dev` (cached per
-// device; both forms have the same shape and shared memory).
-inline int max_clusters(int dev, int sms) {
-  static int cached[64] = {};
-  if (dev >= 0 && dev < 64 && cached[dev]) return cached[dev];
+// device and form; the online form has the shape of the fixed-shift one).
+inline int max_clusters(int dev, int sms, bool int4 = false) {
+  static int cached[2][64] = {};
+  const int f = int4 ? 1 : 0;
+  if (dev >= 0 && dev < 64 && cached[f][dev]) return cached[f][dev];
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * (sms / 2));
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.blockDim = dim3(int4 ? FCfg<true>::THREADS : FCfg<false>::THREADS);
+  cfg.dynamicSmemBytes = int4 ? FCfg<true>::SMEM_BYTES : FCfg<false>::SMEM_BYTES;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -553,20 +728,38 @@ inline int max_clusters(int dev, int sms) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, fwd_kernel<false>, &cfg) != cudaSuccess || n <= 0) {
+  const cudaError_t e = int4 ? cudaOccupancyMaxActiveClusters(&n, fwd_kernel<false, true>, &cfg)
+                             : cudaOccupancyMaxActiveClusters(&n, fwd_kernel<false, false>, &cfg);
+  if (e != cudaSuccess || n <= 0) {
     (void)cudaGetLastError();
     n = sms / 2;
   }
-  if (dev >= 0 && dev < 64) cached[dev] = n;
+  if (dev >= 0 && dev < 64) cached[f][dev] = n;
   return n;
 }
 
+// Shared-memory attribute of every form (once per device).
+inline cudaError_t set_attributes() {
+  cudaError_t e = cudaFuncSetAttribute(fwd_kernel<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       FCfg<false>::SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fwd_kernel<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             FCfg<false>::SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fwd_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             FCfg<true>::SMEM_BYTES);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(fwd_kernel<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             FCfg<true>::SMEM_BYTES);
+  return e;
+}
+
 inline int launch(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const Params& p, int pairs, cudaStream_t s,
-                  bool online = false) {
+                  bool online = false, bool int4 = false) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2 * pairs);
-  cfg.blockDim = dim3(THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.blockDim = dim3(int4 ? FCfg<true>::THREADS : FCfg<false>::THREADS);
+  cfg.dynamicSmemBytes = int4 ? FCfg<true>::SMEM_BYTES : FCfg<false>::SMEM_BYTES;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -575,8 +768,13 @@ inline int launch(const CUtensorMap& tm_h, const CUtensorMap& tm_w, const Params
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e = online ? cudaLaunchKernelEx(&cfg, fwd_kernel<true>, tm_h, tm_w, p)
-                         : cudaLaunchKernelEx(&cfg, fwd_kernel<false>, tm_h, tm_w, p);
+  cudaError_t e;
+  if (int4)
+    e = online ? cudaLaunchKernelEx(&cfg, fwd_kernel<true, true>, tm_h, tm_w, p)
+               : cudaLaunchKernelEx(&cfg, fwd_kernel<false, true>, tm_h, tm_w, p);
+  else
+    e = online ? cudaLaunchKernelEx(&cfg, fwd_kernel<true, false>, tm_h, tm_w, p)
+               : cudaLaunchKernelEx(&cfg, fwd_kernel<false, false>, tm_h, tm_w, p);
   if (e != cudaSuccess) {
     set_last_error(std::string("fwd_kernel launch: ") + cudaGetErrorString(e));
     return 3;

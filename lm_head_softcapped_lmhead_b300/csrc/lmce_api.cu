@@ -132,12 +132,7 @@ int dev_info(DevInfo* out) {
       g_last_err = "device is not sm_103 (compute capability 10.3)";
       return LMCE_ENOTSUP;
     }
-    if ((e = cudaFuncSetAttribute(lmce::fwdk::fwd_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  lmce::fwdk::SMEM_BYTES)) != cudaSuccess)
-      return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
-    if ((e = cudaFuncSetAttribute(lmce::fwdk::fwd_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  lmce::fwdk::SMEM_BYTES)) != cudaSuccess)
-      return cuda_fail(e, "cudaFuncSetAttribute(fwd, online)");
+    if ((e = lmce::fwdk::set_attributes()) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
     if (int rc = lmce::bwdk::setup_attributes(); rc != 0) return rc;
     sms[dev] = n;
     ready[dev] = true;
@@ -214,6 +209,30 @@ int make_map_bf16_3d(CUtensorMap* m, const void* base, uint64_t d, uint64_t rows
   return LMCE_OK;
 }
 
+// 2-D uint8 tensor map over a row-major [rows, inner_bytes] array (row pitch
+// pitch_bytes), box = box_inner bytes x box_rows, no swizzle, out-of-bounds
+// bytes read as zero.
+int make_map_u8_2d(CUtensorMap* m, const void* base, uint64_t inner_bytes, uint64_t rows, uint64_t pitch_bytes,
+                   uint32_t box_inner, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) {
+    g_last_err = "cuTensorMapEncodeTiled unavailable";
+    return LMCE_ECUDA;
+  }
+  cuuint64_t dims[2] = {inner_bytes, rows};
+  cuuint64_t strides[1] = {pitch_bytes};
+  cuuint32_t box[2] = {box_inner, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    g_last_err = "cuTensorMapEncodeTiled (uint8) failed with CUresult " + std::to_string(static_cast<int>(r));
+    return LMCE_ECUDA;
+  }
+  return LMCE_OK;
+}
+
 void set_last_error(const std::string& s) { g_last_err = s; }
 void count_launches(unsigned n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
@@ -284,9 +303,12 @@ void fwd_params_softcap(lmce::fwdk::Params& p, float c) {
   lmce::scaled_tanh_coeffs(static_cast<double>(ce) * 1.4426950408889634, 1.0 / static_cast<double>(ce), p.k);
 }
 
+// The forward.  With q4 (an LMCE_QHEAD_INT4 head) W is unused: the kernel's
+// converter warps dequantise the packed head stage by stage (the int4 form).
 int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
              const int64_t* tgt, const uint8_t* mask, float c, float* nll, float* lse, void* ws, size_t ws_bytes,
-             void* stream, unsigned extra_flags) {
+             void* stream, unsigned extra_flags, const lmce_qhead* q4 = nullptr) {
+  if (q4) W = static_cast<const lmce_bf16*>(q4->codes);  // only checked for alignment here
   if (int rc = check_common(h, ldh, W, N, V, d, tgt, c, ws); rc) return rc;
   if (!nll) return LMCE_EINVAL;
   const Layout L = make_layout(N, V, d, (mask ? LMCE_WS_MASKED : 0u) | extra_flags);
@@ -329,7 +351,14 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
   // h: each CTA's 128 x d rows in one load; W: 128 vocab rows x 2 chunks.
   if (int rc = lmce::make_map_bf16_3d(&tm_h, hx, d, N, ldx * 2, lmce::fwdk::BM, static_cast<uint32_t>(d / 64)); rc)
     return rc;
-  if (int rc = lmce::make_map_bf16_3d(&tm_w, W, d, V, d * 2, lmce::fwdk::HALF_N, lmce::fwdk::SC); rc) return rc;
+  if (q4) {
+    if (int rc = lmce::make_map_u8_2d(&tm_w, q4->codes, d / 2, V, d / 2, lmce::fwdk::FCfg<true>::PK_ROW,
+                                      lmce::fwdk::HALF_N);
+        rc)
+      return rc;
+  } else if (int rc = lmce::make_map_bf16_3d(&tm_w, W, d, V, d * 2, lmce::fwdk::HALF_N, lmce::fwdk::SC); rc) {
+    return rc;
+  }
 
   lmce::fwdk::Params p{};
   p.N = static_cast<int>(N);
@@ -347,11 +376,16 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
   p.status = status;
   p.maxseg = p.VT;
   const bool online = softcap_online(c, V);
+  if (q4) {
+    p.qscales = reinterpret_cast<const __half*>(q4->scales);
+    p.qgroup = q4->group;
+  }
 
   const int64_t T_max = cdiv(N, lmce::fwdk::PAIR_ROWS) * p.VT;
-  const int pairs = static_cast<int>(std::min<int64_t>(T_max, lmce::fwdk::max_clusters(di.dev, di.sms)));
+  const int pairs =
+      static_cast<int>(std::min<int64_t>(T_max, lmce::fwdk::max_clusters(di.dev, di.sms, q4 != nullptr)));
   lmce::count_launches(2);
-  if (int rc = lmce::fwdk::launch(tm_h, tm_w, p, pairs, s, online); rc) return rc;
+  if (int rc = lmce::fwdk::launch(tm_h, tm_w, p, pairs, s, online, q4 != nullptr); rc) return rc;
   cudaError_t e = cudaSuccess;
   const int fblocks = static_cast<int>(std::min<int64_t>(cdiv(N, 256), int64_t(di.sms) * 4));
   if (online)
@@ -627,6 +661,16 @@ int lmhead_ce_fwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const
                        float* nll, float* lse, void* ws, size_t ws_bytes, void* stream) {
   const lmce_qhead hd = int4_head(Wq, scales, group);
   return lmhead_ce_fwd_q(h, ldh, &hd, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream);
+}
+
+int lmhead_ce_fwd_int4_inkernel(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales,
+                                int group, int64_t N, int64_t V, int64_t d, const int64_t* tgt,
+                                const uint8_t* row_mask, float softcap, float* nll, float* lse, void* ws,
+                                size_t ws_bytes, void* stream) {
+  const lmce_qhead hd = int4_head(Wq, scales, group);
+  if (int rc = check_qhead(&hd, V, d); rc) return rc;
+  if (!aligned16(Wq)) return LMCE_EINVAL;  // the packed rows are read by TMA
+  return fwd_impl(h, ldh, nullptr, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, 0u, &hd);
 }
 
 int lmhead_ce_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8_t* Wq, const lmce_f16* scales, int group,
