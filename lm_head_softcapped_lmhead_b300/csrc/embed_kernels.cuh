@@ -9,19 +9,29 @@
 // hold it.  The ids are Zipf-distributed: one token can own 15 % of the rows.
 //
 // The result is deterministic (the same bits on every call): each token's
-// rows are summed in row order, in fp32, in pieces of at most kPieceRows rows
-// (so that a hot token's rows are summed by many warps), and the pieces of a
-// token are added in order before the one addition into dW.
-//   1. count:   per token and row chunk, the rows (integer atomics),
-//               stored token-major (hist[v][c]);
-//   2. totals:  per token (one warp), its row count and its number of pieces;
-//   3. scan:    exclusive scans of the two over the tokens (one block);
-//   4. bases:   per token (one warp, an exclusive scan over its chunks), where
-//               each chunk's rows of it start in the sorted order;
-//   5. place:   one warp per chunk walks its rows in order and writes each row
-//               index at its token's next slot (a stable counting sort);
-//   6. pieces:  one warp per piece sums its rows (bf16 -> fp32) in order;
-//   7. combine: one warp per token adds its pieces in order, then into dW.
+// rows are summed in fp32 along a fixed tree that depends only on the
+// token's row count -- pieces of kPieceRows consecutive rows (in row order),
+// groups of kGroupPieces consecutive pieces (in piece order), then the groups
+// in order -- and the total is added into dW once.  A stable counting sort
+// puts every token's rows together in row order first.
+//   1. count:   per row chunk (chunk_rows(N) rows) and token, the rows (integer
+//               atomics; chunk-major hist[c][v]);
+//   2. tokscan: per token (one thread), the exclusive prefix of its counts
+//               over the chunks (in place), its rows, pieces and groups, and
+//               their scans inside 256-token blocks;
+//   3. tokfin:  the blocks' offsets added (every block scans the blocks'
+//               totals), each piece's token recorded;
+//   4. place:   per chunk, one warp walks the chunk's rows in order with the
+//               chunk's cursors in shared memory; lanes holding the same
+//               token take consecutive slots in lane order (stable);
+//   5. pieces:  one warp per piece sums its rows (bf16 -> fp32) in row
+//               order; a token with one piece adds it into dW.  Otherwise the
+//               warp that completes the last piece of a group (an arrival
+//               counter) sums the group's pieces in order, and the warp that
+//               completes the last group of a token sums its groups in order
+//               and adds the total into dW (a token with one group adds the
+//               group's sum).  Which warp does a sum varies; its order does
+//               not.
 // Rows whose id is outside [0, V) raise ST_EDATA and are skipped.
 #pragma once
 #include <cstdint>
@@ -31,12 +41,14 @@
 namespace lmce {
 namespace embk {
 
-constexpr int kPieceRows = 64;     // rows summed by one warp
-constexpr int kMaxChunks = 1024;   // row chunks of the counting sort
+constexpr int kPieceRows = 32;     // rows summed by one warp
+constexpr int kGroupPieces = 16;   // pieces summed by one warp
+constexpr int kMaxChunks = 256;    // row chunks of the counting sort
+constexpr int kPlaceSmemV = 32768; // largest V whose chunk cursors the place kernel keeps in shared memory
 
 // Rows per chunk of the counting sort for N rows (a multiple of 32).
 inline long long chunk_rows(long long N) {
-  long long r = 256;
+  long long r = 1024;
   while ((N + r - 1) / r > kMaxChunks) r *= 2;
   return r;
 }
@@ -45,178 +57,360 @@ inline long long n_chunks(long long N) { return (N + chunk_rows(N) - 1) / chunk_
 inline long long max_pieces(long long N, long long V) {
   return (N + kPieceRows - 1) / kPieceRows + (N < V ? N : V);
 }
+// Upper bound on the groups of tokens with at least two pieces: such a token
+// has more than kPieceRows rows, so there are fewer than N / 33 of them and
+// their groups sum to less than N / 33 + (N / 32 + N / 33) / 16 < N / 16.
+inline long long max_groups(long long N) { return N / 16 + 64; }
 
 struct Layout {
-  size_t hist, offs, pbase, perm, part, total;
+  size_t hist, offs, pbase, gbase, perm, part, gpart, pcnt, gcnt, powner, btot, total;
 };
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 inline Layout layout(long long N, long long V, long long d) {
   Layout L{};
   size_t o = 0;
-  L.hist = o;   // [V][chunks] int: counts, then bases, then cursors
+  L.hist = o;   // [chunks][V] int: counts, then within-token prefixes (cursors)
   o = up256(o + sizeof(int) * static_cast<size_t>(n_chunks(N)) * static_cast<size_t>(V));
   L.offs = o;   // [V + 1] int: first sorted position of each token
   o = up256(o + sizeof(int) * static_cast<size_t>(V + 1));
   L.pbase = o;  // [V + 1] int: first piece of each token
   o = up256(o + sizeof(int) * static_cast<size_t>(V + 1));
+  L.gbase = o;  // [V + 1] int: first group of each token (tokens with >= 2 pieces)
+  o = up256(o + sizeof(int) * static_cast<size_t>(V + 1));
   L.perm = o;   // [N] int: row indices sorted by token, stable
   o = up256(o + sizeof(int) * static_cast<size_t>(N));
-  L.part = o;   // [max_pieces][d] float: piece sums
+  L.part = o;   // [max_pieces][d] float: piece sums of tokens with several pieces
   o = up256(o + sizeof(float) * static_cast<size_t>(max_pieces(N, V)) * static_cast<size_t>(d));
+  L.gpart = o;  // [max_groups][d] float: group sums of tokens with several groups
+  o = up256(o + sizeof(float) * static_cast<size_t>(max_groups(N)) * static_cast<size_t>(d));
+  L.pcnt = o;   // [max_groups] int: pieces of each group completed
+  o = up256(o + sizeof(int) * static_cast<size_t>(max_groups(N)));
+  L.gcnt = o;   // [V] int: groups of each token completed
+  o = up256(o + sizeof(int) * static_cast<size_t>(V));
+  L.powner = o; // [max_pieces] int: the token of each piece
+  o = up256(o + sizeof(int) * static_cast<size_t>(max_pieces(N, V)));
+  L.btot = o;   // [3][blocks of 256 tokens] int: the blocks' totals
+  o = up256(o + sizeof(int) * 3 * static_cast<size_t>((V + 255) / 256));
   L.total = o;
   return L;
 }
 
 __device__ __forceinline__ bool id_ok(long long v, int V) { return v >= 0 && v < V; }
 
-// 1. hist[v][c] = rows of chunk c with id v.
-__global__ void count_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int C, int* __restrict__ hist,
-                             unsigned* status) {
+// The kernels after the first are launched with programmatic stream
+// serialization: their launch overlaps the previous kernel's tail, and each
+// waits here (griddepcontrol.wait) until the previous kernel has completed
+// and its memory operations are visible before reading what it wrote.
+__device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// 1. hist[c][v] = rows of chunk c with id v.  With use_smem (V <=
+//    kPlaceSmemV; dynamic shared memory of V ints) block c counts in shared
+//    memory and writes its row out whole; otherwise it zeroes its row and
+//    counts with global atomics.
+__global__ void count_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int* __restrict__ hist,
+                             unsigned* status, int use_smem) {
+  extern __shared__ int s_hist[];
   const int c = blockIdx.x;
   const int i0 = c * R, i1 = min(N, i0 + R);
+  int* h = hist + static_cast<size_t>(c) * V;
+  int* cnt = use_smem ? s_hist : h;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) cnt[v] = 0;
+  __syncthreads();
   for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
     const long long v = ids[i];
     if (!id_ok(v, V)) {
       atomicOr(status, ST_EDATA);
       continue;
     }
-    atomicAdd(hist + static_cast<size_t>(v) * C + c, 1);
+    atomicAdd(cnt + v, 1);
   }
+  if (!use_smem) return;
+  __syncthreads();
+  for (int v = threadIdx.x; v < V; v += blockDim.x) h[v] = s_hist[v];
 }
 
-// 2. offs[v] = rows of token v, pbase[v] = its pieces (scanned in place next);
-//    one warp per token.
-__global__ void totals_kernel(const int* __restrict__ hist, int C, int V, int* __restrict__ offs,
-                              int* __restrict__ pbase) {
-  const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
-  for (int v = blockIdx.x * warps + (threadIdx.x >> 5); v < V; v += gridDim.x * warps) {
-    const int* h = hist + static_cast<size_t>(v) * C;
-    int t = 0;
-    for (int c = lane; c < C; c += 32) t += h[c];
+// Block-wide exclusive scan (blockDim.x == 256) of one value per thread;
+// returns the thread's prefix, *total the block's sum.
+__device__ __forceinline__ int block_scan_256(int x, int* s_warp, int* total) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc = x;
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-    if (lane == 0) {
-      offs[v] = t;
-      pbase[v] = (t + kPieceRows - 1) / kPieceRows;
-    }
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, inc, o);
+    if (lane >= o) inc += y;
   }
-}
-
-// 3. Exclusive scans of offs and pbase over v (one block), the totals in
-//    entry V.
-__global__ void scan_kernel(int* __restrict__ offs, int* __restrict__ pbase, int V) {
-  __shared__ int s_a[1024], s_b[1024];
-  __shared__ int carry_a, carry_b;
-  if (threadIdx.x == 0) {
-    carry_a = 0;
-    carry_b = 0;
+  if (lane == 31) s_warp[warp] = inc;
+  __syncthreads();
+  if (warp == 0) {
+    int w = lane < 8 ? s_warp[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < 8) s_warp[lane] = w;  // inclusive over the warps
   }
   __syncthreads();
-  for (int base = 0; base < V; base += blockDim.x) {
-    const int v = base + threadIdx.x;
-    const int a = v < V ? offs[v] : 0, b = v < V ? pbase[v] : 0;
-    s_a[threadIdx.x] = a;
-    s_b[threadIdx.x] = b;
-    __syncthreads();
-    // Hillis-Steele inclusive scan of the tile.
-    for (int off = 1; off < static_cast<int>(blockDim.x); off <<= 1) {
-      const int xa = threadIdx.x >= static_cast<unsigned>(off) ? s_a[threadIdx.x - off] : 0;
-      const int xb = threadIdx.x >= static_cast<unsigned>(off) ? s_b[threadIdx.x - off] : 0;
-      __syncthreads();
-      s_a[threadIdx.x] += xa;
-      s_b[threadIdx.x] += xb;
-      __syncthreads();
-    }
-    if (v < V) {
-      offs[v] = carry_a + s_a[threadIdx.x] - a;
-      pbase[v] = carry_b + s_b[threadIdx.x] - b;
-    }
-    __syncthreads();
-    if (threadIdx.x == blockDim.x - 1) {
-      carry_a += s_a[threadIdx.x];
-      carry_b += s_b[threadIdx.x];
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) {
-    offs[V] = carry_a;
-    pbase[V] = carry_b;
-  }
+  const int before = (warp > 0 ? s_warp[warp - 1] : 0) + inc - x;
+  *total = s_warp[7];
+  __syncthreads();
+  return before;
 }
 
-// 4. hist[v][c] <- offs[v] + rows of token v in chunks before c; one warp
-//    per token, 32 chunks at a time (warp exclusive scan plus a carry).
-__global__ void bases_kernel(int* __restrict__ hist, int C, int V, const int* __restrict__ offs) {
-  const int warps = blockDim.x >> 5, lane = threadIdx.x & 31;
-  for (int v = blockIdx.x * warps + (threadIdx.x >> 5); v < V; v += gridDim.x * warps) {
-    int* h = hist + static_cast<size_t>(v) * C;
-    int run = offs[v];
-    for (int c0 = 0; c0 < C; c0 += 32) {
-      const int c = c0 + lane;
-      const int n = c < C ? h[c] : 0;
-      int x = n;  // inclusive scan over the lanes
+// 2. Per token v (one thread of 256-thread blocks): hist[c][v] <- rows of v
+//    in chunks before c (in place); the rows, pieces and groups of v (only
+//    tokens with >= 2 pieces have groups), scanned inside the block, with
+//    the block's totals in btot.
+__global__ void __launch_bounds__(256) tokscan_kernel(int* __restrict__ hist, int C, int V, int* __restrict__ offs,
+                                                      int* __restrict__ pbase, int* __restrict__ gbase,
+                                                      int* __restrict__ gcnt, int* __restrict__ btot) {
+  wait_prior_grid();
+  __shared__ int s_warp[8];
+  const int v = blockIdx.x * 256 + threadIdx.x;
+  int run = 0;
+  if (v < V) {
+    for (int c0 = 0; c0 < C; c0 += 16) {
+      int x[16];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
+      for (int k = 0; k < 16; ++k) x[k] = c0 + k < C ? hist[static_cast<size_t>(c0 + k) * V + v] : 0;
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        if (c0 + k < C) hist[static_cast<size_t>(c0 + k) * V + v] = run;
+        run += x[k];
       }
-      if (c < C) h[c] = run + x - n;
-      run += __shfl_sync(0xffffffffu, x, 31);
     }
+  }
+  const int np = (run + kPieceRows - 1) / kPieceRows;
+  const int ng = np >= 2 ? (np + kGroupPieces - 1) / kGroupPieces : 0;
+  int ta, tb, tc;
+  const int la = block_scan_256(run, s_warp, &ta);
+  const int lb = block_scan_256(np, s_warp, &tb);
+  const int lc = block_scan_256(ng, s_warp, &tc);
+  if (v < V) {
+    offs[v] = la;
+    pbase[v] = lb;
+    gbase[v] = lc;
+    gcnt[v] = np;  // read (and zeroed) by tokfin_kernel
+  }
+  const int nb = gridDim.x;
+  if (threadIdx.x == 0) {
+    btot[blockIdx.x] = ta;
+    btot[nb + blockIdx.x] = tb;
+    btot[2 * nb + blockIdx.x] = tc;
   }
 }
 
-// 5. One warp per chunk, rows in order, 32 at a time: lanes with equal ids
+// 3. Per token u (one thread, the same 256-token blocks): its block's
+//    offsets (each block scans the blocks' totals itself) are added to the
+//    block-local prefixes, so that offs / pbase / gbase hold the exclusive
+//    scans over all tokens (totals at V); each piece records its token (the
+//    token's piece count was left in gcnt, which then becomes the token's
+//    arrival counter, zeroed), and the groups' arrival counters are zeroed.
+__global__ void __launch_bounds__(256) tokfin_kernel(int V, int* __restrict__ offs, int* __restrict__ pbase,
+                                                     int* __restrict__ gbase, const int* __restrict__ btot,
+                                                     int* __restrict__ gcnt, int* __restrict__ pcnt,
+                                                     int* __restrict__ powner) {
+  wait_prior_grid();
+  __shared__ int s_warp[8];
+  __shared__ int s_off[3], s_tot[3];
+  const int nb = gridDim.x;
+  for (int q = 0; q < 3; ++q) {
+    int carry = 0, mine = 0;
+    for (int b0 = 0; b0 < nb; b0 += 256) {
+      const int bi = b0 + threadIdx.x;
+      const int x = bi < nb ? btot[q * nb + bi] : 0;
+      int t;
+      const int ex = block_scan_256(x, s_warp, &t);
+      if (bi == static_cast<int>(blockIdx.x)) mine = carry + ex;
+      carry += t;
+    }
+    if (threadIdx.x == (blockIdx.x & 255u)) s_off[q] = mine;
+    if (threadIdx.x == 0) s_tot[q] = carry;
+  }
+  __syncthreads();
+  const int u = blockIdx.x * 256 + threadIdx.x;
+  if (u < V) {
+    offs[u] += s_off[0];
+    const int pb = pbase[u] + s_off[1];
+    pbase[u] = pb;
+    gbase[u] += s_off[2];
+    const int np = gcnt[u];
+    gcnt[u] = 0;
+    for (int p = pb; p < pb + np; ++p) powner[p] = u;
+  }
+  if (blockIdx.x == static_cast<unsigned>(nb - 1) && threadIdx.x == 0) {
+    offs[V] = s_tot[0];
+    pbase[V] = s_tot[1];
+    gbase[V] = s_tot[2];
+  }
+  for (int q = u; q < s_tot[2]; q += nb * 256) pcnt[q] = 0;
+}
+
+// 4. Block c: warp 0 walks the chunk's rows in order, 32 at a time, and
+//    writes each row index at its token's next slot; lanes with equal ids
 //    take consecutive slots in lane order, so each token's rows keep their
-//    row order (stable).
-__global__ void place_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int C, int* __restrict__ hist,
-                             int* __restrict__ perm) {
-  const int warps = blockDim.x >> 5;
-  const int c = blockIdx.x * warps + (threadIdx.x >> 5);
-  const int lane = threadIdx.x & 31;
-  if (c >= C) return;
-  const int i0 = c * R, i1 = min(N, i0 + R);
-  int* hc = hist + c;  // hc[v * C]: this chunk's cursor of token v
-  for (int b = i0; b < i1; b += 32) {
-    const int i = b + lane;
-    const long long v = i < i1 ? ids[i] : -1;
-    const bool ok = i < i1 && id_ok(v, V);
-    const unsigned active = __ballot_sync(0xffffffffu, ok);
-    const unsigned peers = __match_any_sync(0xffffffffu, ok ? v : -1ll) & active;
-    int slot = 0;
-    if (ok) {
-      const unsigned below = peers & ((1u << lane) - 1u);
-      slot = hc[static_cast<size_t>(v) * C] + __popc(below);
-      perm[slot] = i;
+//    row order (stable).  The chunk's cursors (offs[v] + hist[c][v]) are
+//    staged in shared memory when V <= kPlaceSmemV (dynamic shared memory of
+//    V ints), else updated in place in hist.
+__global__ void place_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int* __restrict__ hist,
+                             const int* __restrict__ offs, int* __restrict__ perm, int use_smem) {
+  extern __shared__ int s_cur[];
+  wait_prior_grid();
+  const int c = blockIdx.x;
+  int* hc = hist + static_cast<size_t>(c) * V;
+  if (use_smem) {
+    // 8 independent loads of each array in flight per thread.
+    for (int v0 = threadIdx.x; v0 < V; v0 += 8 * blockDim.x) {
+      int a[8], b[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int v = v0 + k * blockDim.x;
+        a[k] = v < V ? offs[v] : 0;
+        b[k] = v < V ? hc[v] : 0;
+      }
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        const int v = v0 + k * blockDim.x;
+        if (v < V) s_cur[v] = a[k] + b[k];
+      }
     }
-    __syncwarp();
-    if (ok && (peers & ((1u << lane) - 1u)) == 0u)  // the group's lowest lane
-      hc[static_cast<size_t>(v) * C] += __popc(peers);
-    __syncwarp();
+    __syncthreads();
+  }
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
+  const int i0 = c * R, i1 = min(N, i0 + R);
+  // The walk is serial, so the chunk's ids are loaded ahead, 32 steps (1024
+  // rows) at a time, lane l holding row b + 32 s + l of step s (-1 for rows
+  // that do not count).
+  constexpr int kSteps = 32;
+  for (int b0 = i0; b0 < i1; b0 += 32 * kSteps) {
+    int tok[kSteps];
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st) {
+      const int i = b0 + 32 * st + lane;
+      const long long v = i < i1 ? ids[i] : -1;
+      tok[st] = id_ok(v, V) ? static_cast<int>(v) : -1;
+    }
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st) {
+      const int i = b0 + 32 * st + lane;
+      const int v = tok[st];
+      const bool ok = v >= 0;
+      const unsigned active = __ballot_sync(0xffffffffu, ok);
+      const unsigned peers = __match_any_sync(0xffffffffu, v) & active;
+      const unsigned below = peers & ((1u << lane) - 1u);
+      int base = 0;
+      if (ok) base = use_smem ? s_cur[v] : offs[v] + hc[v];
+      if (ok) perm[base + __popc(below)] = i;
+      __syncwarp();
+      if (ok && below == 0u) {  // the group's lowest lane advances the cursor
+        if (use_smem)
+          s_cur[v] = base + __popc(peers);
+        else
+          hc[v] += __popc(peers);
+      }
+      __syncwarp();
+    }
   }
 }
 
-// Token owning piece p: the last v with pbase[v] <= p (pbase is sorted).
-__device__ __forceinline__ int piece_owner(const int* __restrict__ pbase, int V, int p) {
+// Token owning entry p of a sorted exclusive-prefix array base[0..V]: the
+// last v with base[v] <= p.
+__device__ __forceinline__ int owner_of(const int* __restrict__ base, int V, int p) {
   int lo = 0, hi = V - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
-    if (pbase[mid] <= p) lo = mid; else hi = mid - 1;
+    if (base[mid] <= p) lo = mid; else hi = mid - 1;
   }
   return lo;
 }
 
-// 6. part[p][:] = sum, in row order, of the rows of piece p (one warp; lane l
-//    holds dims 8 l .. 8 l + 7 and 256 + 8 l .. + 7).
-__global__ void pieces_kernel(const uint16_t* __restrict__ g, long long ldg, int d, int V,
+// dW[v][:] += s (lane l holds the float4 groups l, l + 32, l + 64, l + 96).
+__device__ __forceinline__ void add_row_f4(float* __restrict__ dW, int v, int ng4, const float4 (&s)[4], int lane) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const int j = lane + 32 * q;
+    if (j < ng4) {
+      float4* o = reinterpret_cast<float4*>(dW + static_cast<size_t>(v) * (4 * ng4)) + j;
+      float4 a = *o;
+      a.x += s[q].x;
+      a.y += s[q].y;
+      a.z += s[q].z;
+      a.w += s[q].w;
+      *o = a;
+    }
+  }
+}
+
+// Sum, in order, of n rows of d floats starting at src (row stride d) into s
+// (lane l: float4 groups l + 32 q); up to kSumBatch rows' loads in flight.
+// The rows were written by other warps of the same kernel (see
+// pieces_kernel), so the loads bypass L1 (ld.global.cg).
+constexpr int kSumBatch = 4;
+__device__ __forceinline__ void sum_rows_f4(const float* __restrict__ src, int n, int ng4, float4 (&s)[4], int lane) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) s[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int r0 = 0; r0 < n; r0 += kSumBatch) {
+    float4 buf[kSumBatch][4];
+#pragma unroll
+    for (int b = 0; b < kSumBatch; ++b)
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int j = lane + 32 * q;
+        buf[b][q] = (r0 + b < n && j < ng4)
+                        ? __ldcg(reinterpret_cast<const float4*>(src + static_cast<size_t>(r0 + b) * (4 * ng4)) + j)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+    for (int b = 0; b < kSumBatch; ++b) {
+      if (r0 + b >= n) break;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        s[q].x += buf[b][q].x;
+        s[q].y += buf[b][q].y;
+        s[q].z += buf[b][q].z;
+        s[q].w += buf[b][q].w;
+      }
+    }
+  }
+}
+
+// Lane 0 adds 1 to *counter after this warp's stores are visible GPU-wide;
+// returns (to every lane) whether this warp brought it to `last_value`.
+__device__ __forceinline__ bool arrive_last(int* counter, int last_value, int lane) {
+  __threadfence();
+  __syncwarp();
+  int old = 0;
+  if (lane == 0) old = atomicAdd(counter, 1);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  const bool last = old == last_value;
+  if (last) __threadfence();  // the other warps' sums are read after this
+  return last;
+}
+
+// 5. Piece p (one warp): the sum, in row order, of its rows of g (bf16 ->
+//    fp32).  Lane l holds dims 8 l .. 8 l + 7 and 256 + 8 l .. + 7; eight
+//    rows' loads are in flight at once, the additions stay in row order.  A
+//    token with a single piece adds it into dW.  Otherwise part[p] = sum, and
+//    the warp completing the last piece of group q (pcnt[q]) sums the
+//    group's pieces in order; a token with one group adds that into dW, else
+//    gpart[q] = sum and the warp completing the token's last group (gcnt[v])
+//    sums its groups in order and adds the total into dW.
+constexpr int kRowBatch = 8;
+__global__ void __launch_bounds__(256, 2) pieces_kernel(const uint16_t* __restrict__ g, long long ldg, int d, int V,
                               const int* __restrict__ offs, const int* __restrict__ pbase,
-                              const int* __restrict__ perm, float* __restrict__ part) {
+                              const int* __restrict__ gbase, const int* __restrict__ powner,
+                              const int* __restrict__ perm, float* __restrict__ part,
+                              float* __restrict__ gpart, int* __restrict__ pcnt, int* __restrict__ gcnt,
+                              float* __restrict__ dW) {
+  wait_prior_grid();
   const int warps = blockDim.x >> 5;
   const int lane = threadIdx.x & 31;
   const int np = pbase[V];
   const int ng = d / 8;  // 8-dim groups of a row
+  const int ng4 = d / 4;
   for (int p = blockIdx.x * warps + (threadIdx.x >> 5); p < np; p += gridDim.x * warps) {
-    const int v = piece_owner(pbase, V, p);
+    const int v = powner[p];
     const int start = offs[v] + (p - pbase[v]) * kPieceRows;
     const int len = min(kPieceRows, offs[v + 1] - start);
     float acc[2][8];
@@ -224,16 +418,24 @@ __global__ void pieces_kernel(const uint16_t* __restrict__ g, long long ldg, int
     for (int q = 0; q < 2; ++q)
 #pragma unroll
       for (int k = 0; k < 8; ++k) acc[q][k] = 0.f;
-    // Loads of several rows are in flight; the additions stay in row order.
-#pragma unroll 4
-    for (int r = 0; r < len; ++r) {
-      const uint16_t* row = g + static_cast<long long>(perm[start + r]) * ldg;
+    for (int r0 = 0; r0 < len; r0 += kRowBatch) {
+      uint4 buf[kRowBatch][2];
 #pragma unroll
-      for (int q = 0; q < 2; ++q) {
-        const int j = lane + 32 * q;
-        if (j < ng) {
-          const uint4 u = __ldg(reinterpret_cast<const uint4*>(row) + j);
-          const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+      for (int b = 0; b < kRowBatch; ++b) {
+        const bool live = r0 + b < len;
+        const uint16_t* row = g + static_cast<long long>(live ? perm[start + r0 + b] : 0) * ldg;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int j = lane + 32 * q;
+          buf[b][q] = (live && j < ng) ? __ldg(reinterpret_cast<const uint4*>(row) + j) : make_uint4(0u, 0u, 0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int b = 0; b < kRowBatch; ++b) {
+        if (r0 + b >= len) break;
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const uint32_t w[4] = {buf[b][q].x, buf[b][q].y, buf[b][q].z, buf[b][q].w};
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
             acc[q][2 * k] += __uint_as_float(w[k] << 16);
@@ -242,66 +444,49 @@ __global__ void pieces_kernel(const uint16_t* __restrict__ g, long long ldg, int
         }
       }
     }
-    float* out = part + static_cast<size_t>(p) * d;
+    const int npc = pbase[v + 1] - pbase[v];
+    const bool single = npc == 1;
 #pragma unroll
     for (int q = 0; q < 2; ++q) {
       const int j = lane + 32 * q;
-      if (j < ng) {
-        float4* o = reinterpret_cast<float4*>(out + 8 * j);
-        o[0] = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
-        o[1] = make_float4(acc[q][4], acc[q][5], acc[q][6], acc[q][7]);
+      if (j >= ng) continue;
+      const float4 lo = make_float4(acc[q][0], acc[q][1], acc[q][2], acc[q][3]);
+      const float4 hi = make_float4(acc[q][4], acc[q][5], acc[q][6], acc[q][7]);
+      float4* o = reinterpret_cast<float4*>((single ? dW + static_cast<size_t>(v) * d : part + static_cast<size_t>(p) * d) +
+                                            8 * j);
+      if (single) {
+        float4 a = o[0], b = o[1];
+        o[0] = make_float4(a.x + lo.x, a.y + lo.y, a.z + lo.z, a.w + lo.w);
+        o[1] = make_float4(b.x + hi.x, b.y + hi.y, b.z + hi.z, b.w + hi.w);
+      } else {
+        o[0] = lo;
+        o[1] = hi;
       }
     }
-  }
-}
-
-// 7. dW[v][:] += sum of token v's pieces, in piece order (one warp per token;
-//    lane l holds the float4 groups l, l + 32, l + 64, l + 96 of a row).  The
-//    loads of several pieces are in flight at once; each element's additions
-//    stay in piece order.
-__global__ void combine_kernel(const float* __restrict__ part, const int* __restrict__ pbase, int V, int d,
-                               float* __restrict__ dW) {
-  const int warps = blockDim.x >> 5;
-  const int lane = threadIdx.x & 31;
-  const int ng = d / 4;  // float4 groups of a row (at most 128)
-  for (int v = blockIdx.x * warps + (threadIdx.x >> 5); v < V; v += gridDim.x * warps) {
-    const int p0 = pbase[v], p1 = pbase[v + 1];
-    if (p0 == p1) continue;
-    float4 s[4];
-    const float4* b0 = reinterpret_cast<const float4*>(part + static_cast<size_t>(p0) * d);
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int j = lane + 32 * q;
-      s[q] = j < ng ? b0[j] : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
-#pragma unroll 4
-    for (int p = p0 + 1; p < p1; ++p) {
-      const float4* b = reinterpret_cast<const float4*>(part + static_cast<size_t>(p) * d);
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int j = lane + 32 * q;
-        if (j < ng) {
-          const float4 x = b[j];
-          s[q].x += x.x;
-          s[q].y += x.y;
-          s[q].z += x.z;
-          s[q].w += x.w;
-        }
-      }
+    if (single) continue;
+    // ---- the group of this piece ----
+    const int gl = (p - pbase[v]) / kGroupPieces;  // group index within the token
+    const int q = gbase[v] + gl;
+    const int p0 = pbase[v] + gl * kGroupPieces;
+    const int n_in = min(kGroupPieces, pbase[v + 1] - p0);
+    if (!arrive_last(pcnt + q, n_in - 1, lane)) continue;
+    float4 sg[4];
+    sum_rows_f4(part + static_cast<size_t>(p0) * d, n_in, ng4, sg, lane);
+    const int ngr = gbase[v + 1] - gbase[v];
+    if (ngr == 1) {
+      add_row_f4(dW, v, ng4, sg, lane);
+      continue;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int j = lane + 32 * q;
-      if (j < ng) {
-        float4* o = reinterpret_cast<float4*>(dW + static_cast<size_t>(v) * d) + j;
-        float4 a = *o;
-        a.x += s[q].x;
-        a.y += s[q].y;
-        a.z += s[q].z;
-        a.w += s[q].w;
-        *o = a;
-      }
+    for (int k = 0; k < 4; ++k) {
+      const int j = lane + 32 * k;
+      if (j < ng4) reinterpret_cast<float4*>(gpart + static_cast<size_t>(q) * d)[j] = sg[k];
     }
+    // ---- the token's groups ----
+    if (!arrive_last(gcnt + v, ngr - 1, lane)) continue;
+    float4 st[4];
+    sum_rows_f4(gpart + static_cast<size_t>(gbase[v]) * d, ngr, ng4, st, lane);
+    add_row_f4(dW, v, ng4, st, lane);
   }
 }
 

@@ -133,6 +133,12 @@ int dev_info(DevInfo* out) {
       return LMCE_ENOTSUP;
     }
     if ((e = lmce::fwdk::set_attributes()) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
+    if ((e = cudaFuncSetAttribute(lmce::embk::place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sizeof(int) * lmce::embk::kPlaceSmemV))) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(place)");
+    if ((e = cudaFuncSetAttribute(lmce::embk::count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sizeof(int) * lmce::embk::kPlaceSmemV))) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(count)");
     if (int rc = lmce::bwdk::setup_attributes(); rc != 0) return rc;
     sms[dev] = n;
     ready[dev] = true;
@@ -286,6 +292,24 @@ int fd_launch(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, in
               const int64_t* tgt, const uint8_t* mask, float c, float grad_scale, float* nll, float* lse,
               lmce_bf16* dh, unsigned* status, const DevInfo& di, cudaStream_t s) {
   return lmce::bwdk::launch_fd(h, ldh, W, N, V, d, tgt, mask, c, grad_scale, nll, lse, dh, status, di.dev, di.sms, s);
+}
+
+// Launch with programmatic stream serialization: the kernel's launch may
+// overlap the previous kernel on the stream; the kernel itself waits
+// (griddepcontrol.wait) before reading what that kernel wrote.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem, cudaStream_t s, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 // The one-pass forward + dh (FD) accumulates unnormalised terms: only for
@@ -850,23 +874,37 @@ int lmhead_tied_embed_bwd(const int64_t* ids, const lmce_bf16* g, int64_t ldg, i
   int* hist = reinterpret_cast<int*>(e + E.hist);
   int* offs = reinterpret_cast<int*>(e + E.offs);
   int* pbase = reinterpret_cast<int*>(e + E.pbase);
+  int* gbase = reinterpret_cast<int*>(e + E.gbase);
   int* perm = reinterpret_cast<int*>(e + E.perm);
   float* part = reinterpret_cast<float*>(e + E.part);
+  float* gpart = reinterpret_cast<float*>(e + E.gpart);
+  int* pcnt = reinterpret_cast<int*>(e + E.pcnt);
+  int* gcnt = reinterpret_cast<int*>(e + E.gcnt);
+  int* powner = reinterpret_cast<int*>(e + E.powner);
   const int R = static_cast<int>(ek::chunk_rows(N)), C = static_cast<int>(ek::n_chunks(N));
   const int n = static_cast<int>(N), v = static_cast<int>(V), dd = static_cast<int>(d);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  cudaError_t err = cudaMemsetAsync(hist, 0, sizeof(int) * static_cast<size_t>(C) * V, s);
-  if (err != cudaSuccess) return cuda_fail(err, "tied_embed memset");
-  const int wblocks = static_cast<int>(std::min<int64_t>(cdiv(V, 8), int64_t(di.sms) * 8));  // a warp per token
-  lmce::count_launches(7);
-  ek::count_kernel<<<C, 256, 0, s>>>(ids, n, v, R, C, hist, status);
-  ek::totals_kernel<<<wblocks, 256, 0, s>>>(hist, C, v, offs, pbase);
-  ek::scan_kernel<<<1, 1024, 0, s>>>(offs, pbase, v);
-  ek::bases_kernel<<<wblocks, 256, 0, s>>>(hist, C, v, offs);
-  ek::place_kernel<<<static_cast<int>(cdiv(C, 8)), 256, 0, s>>>(ids, n, v, R, C, hist, perm);
-  ek::pieces_kernel<<<di.sms * 8, 256, 0, s>>>(g, ldg, dd, v, offs, pbase, perm, part);
-  ek::combine_kernel<<<static_cast<int>(std::min<int64_t>(cdiv(V, 8), int64_t(di.sms) * 8)), 256, 0, s>>>(
-      part, pbase, v, dd, dW);
+  const int use_smem = V <= ek::kPlaceSmemV ? 1 : 0;
+  const size_t place_smem = use_smem ? sizeof(int) * static_cast<size_t>(V) : 0;
+  int* btot = reinterpret_cast<int*>(e + E.btot);
+  const int nb = static_cast<int>(cdiv(V, 256));
+  lmce::count_launches(5);
+  ek::count_kernel<<<C, 256, place_smem, s>>>(ids, n, v, R, hist, status, use_smem);
+  cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess)
+    err = launch_pdl(ek::tokscan_kernel, nb, 256, 0, s, hist, C, v, offs, pbase, gbase, gcnt, btot);
+  if (err == cudaSuccess)
+    err = launch_pdl(ek::tokfin_kernel, nb, 256, 0, s, v, offs, pbase, gbase, static_cast<const int*>(btot), gcnt,
+                     pcnt, powner);
+  if (err == cudaSuccess)
+    err = launch_pdl(ek::place_kernel, C, 256, place_smem, s, ids, n, v, R, hist, static_cast<const int*>(offs), perm,
+                     use_smem);
+  if (err == cudaSuccess)
+    err = launch_pdl(ek::pieces_kernel, di.sms * 8, 256, 0, s, reinterpret_cast<const uint16_t*>(g),
+                     static_cast<long long>(ldg), dd, v, static_cast<const int*>(offs), static_cast<const int*>(pbase),
+                     static_cast<const int*>(gbase), static_cast<const int*>(powner), static_cast<const int*>(perm), part,
+                     gpart, pcnt, gcnt, dW);
+  if (err != cudaSuccess) return cuda_fail(err, "tied_embed launch");
   err = cudaGetLastError();
   if (err != cudaSuccess) return cuda_fail(err, "tied_embed launch");
   return LMCE_OK;
