@@ -4,7 +4,7 @@ Method: minimax (Remez exchange) fit, in relative error, of
     g(u) = tanh(sqrt(u)) / sqrt(u)      on u in [0, XMAX^2],
 by a degree-DEG polynomial P, so that tanh(x) ~= x * P(x^2) for |x| <= XMAX.
 Outside that range the kernels use tanh(x) = 1 - 2 / (exp(2x) + 1).
-Run:  python fit_tanh.py   (prints the coefficients pasted into tanh_poly.cuh
+Run:  python fit_tanh.py   (prints the coefficients written into softcap_math.cuh
 and the worst relative error, in exact arithmetic and evaluated in fp32).
 """
 import numpy as np
