@@ -16,11 +16,10 @@
 //    z = X Y^T (tcgen05, A from TMEM, M=128 N=128, double-buffered in TMEM),
 //    and its 16 epilogue warps (one 32-column chunk each per tile) turn each
 //    z tile into the bf16 tile P = -G (DH) or -G^T (DW) in the 128B-swizzled
-//    K-major layout the A CTA's MMA reads.  P reaches the peer CTA's shared
-//    memory (DSMEM) by st.async from the epilogue warps (FD, DH), or (DW)
-//    through a local staging copy that a forwarder warp sends in two bulk
-//    copies per tile.
-//  * rank 1, the A CTA: loads the same Y tile in 32-row slabs (as the
+//    K-major layout the A CTA's MMA reads, into a local staging copy; a
+//    forwarder warp sends each staged tile to the peer CTA's shared memory
+//    (DSMEM) in two bulk copies.
+//  * rank 1, the A CTA: loads the same Y tile in 64-row slabs (as the
 //    MN-major B operand) and accumulates acc (128 x d fp32, all 512 TMEM
 //    columns) += P Y with tcgen05 M=128 N=d/2; after the last tile its 16
 //    drain warps scale by w and write dh (bf16) or dW (fp32, added or
@@ -73,12 +72,12 @@ constexpr int FWD_WARP = 18;   // Z: forwards P tiles to the A CTA; A: acknowled
 constexpr int THREADS = 608;
 constexpr uint32_t CHUNK = 128 * KB * 2;  // 16 KB: 128 rows x 64 bf16
 constexpr uint32_t ZSTAGE = ZSC * CHUNK;   // 64 KB
-// The A CTA loads its Y tile in 4 slabs of 32 rows x d (one TMA load per
-// slab, up to 32 KB); inside a slab the d / 64 chunks of 32 x 64 follow each
-// other (4 KB apart).
-constexpr int SLAB_ROWS = 32;
+// The A CTA loads its Y tile in 2 slabs of 64 rows x d (one TMA load per
+// slab, up to 64 KB); inside a slab the d / 64 chunks of 64 x 64 follow each
+// other (8 KB apart).
+constexpr int SLAB_ROWS = 64;
 constexpr int NSLAB = BT / SLAB_ROWS;
-constexpr uint32_t SLAB_CHUNK = SLAB_ROWS * KB * 2;  // 4 KB
+constexpr uint32_t SLAB_CHUNK = SLAB_ROWS * KB * 2;  // 8 KB
 constexpr uint32_t P_SLOT = 2 * CHUNK;                // 32 KB: one 128 x 128 bf16 P tile
 constexpr uint32_t Z_TMEM_X = 256;  // Z: the stationary block X in TMEM columns 256-511
 // FD: per-row records of the Z epilogue, [column group][row] x 32 bytes:
@@ -87,29 +86,27 @@ constexpr uint32_t Z_TMEM_X = 256;  // Z: the stationary block X in TMEM columns
 constexpr uint32_t REC_BYTES = 32;
 constexpr int FL_LIVE = 1, FL_TVALID = 2, FL_HIT = 4;
 
-// Shared-memory plan of a mode.  The Z CTA holds the ring of Y stages (X is
-// in TMEM); the A CTA holds a ring of Y slabs and the P slots.  P tiles reach
-// the A CTA in one of two ways:
-//  * FD, DH: each epilogue thread stores its 64 bytes straight into the P
-//    slot with st.async (these epilogues hold the row's data in registers and
-//    are light, so the stores overlap them);
-//  * DW: the epilogue writes the tile into a local staging copy and the
-//    forwarder warp sends each 16 KB column chunk with one bulk DSMEM copy
-//    (its epilogue, which broadcasts per-column data, is heavier, and 2048
-//    DSMEM stores per tile slow it).
-// Deep P buffering decouples the Z epilogue from the A CTA's MMAs; half a
-// tile of Y slabs in flight is enough.  Measured at N=65536, V=8192, d=512
-// (ms per pass): FD, st.async, 3 x 64 KB ring, 5 P slots: 1.044 (bulk copies
-// with 2 staging copies: 1.101); DW, bulk, 2 x 64 KB ring, 2 staging copies,
-// 4 P slots: 1.078 (st.async with 5 P slots: 1.273); DH (dh only): st.async
-// 0.983, bulk 1.025.
+// Shared-memory plan of a mode.  The Z CTA holds a ring of Y stages (X is in
+// TMEM) and the P staging copies; the A CTA holds a ring of Y slabs and the P
+// slots.  The Z epilogue writes each P tile into a local staging copy, and
+// the forwarder warp sends each 16 KB column chunk of it with one bulk DSMEM
+// copy into an A CTA P slot.
+// What the measurements favoured (N=65536, V=8192, d=512, ms per pass): few
+// large transfers between the CTAs' rings over many small ones.  Y slabs of
+// 64 rows (two 64 KB slots) against 32 rows (two 32 KB slots, 5 P slots):
+// DW 0.983 against 1.078, FD 1.018 against 1.044 (FD then stored P with
+// st.async), DH 0.936 against 0.954; four 16-row slots in the same 64 KB
+// made every pass 40 % slower, and four 32-row slots in 128 KB were slower
+// than two 64-row ones (DW 1.135 against 1.004).  One 32 KB bulk copy per
+// tile instead of two 16 KB copies: FD 1.021, DW 0.991.  Three staging
+// copies against two: DW 0.983 against 1.004 (FD has room for two beside its
+// row records).
 template <int MODE>
 struct Cfg {
-  static constexpr bool kBulk = MODE == DW;
-  static constexpr int YSTAGES = kBulk ? 2 : 3;  // Z ring stages (64 KB)
-  static constexpr int NSTG = kBulk ? 2 : 0;     // Z: P staging copies
-  static constexpr int ASLOTS = 2;               // A: Y slab slots (32 KB)
-  static constexpr int NPS = kBulk ? 4 : 5;      // A: P slots (32 KB)
+  static constexpr int YSTAGES = 2;               // Z ring stages (64 KB)
+  static constexpr int NSTG = MODE == FD ? 2 : 3; // Z: P staging copies (32 KB)
+  static constexpr int ASLOTS = 2;                // A: Y slab slots (64 KB)
+  static constexpr int NPS = 3;                   // A: P slots (32 KB)
   // Z CTA layout
   static constexpr uint32_t Z_Y = 0;
   static constexpr uint32_t Z_STG = Z_Y + YSTAGES * ZSTAGE;          // NSTG x 2 x 16 KB
@@ -430,7 +427,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     bwd_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_y,
                const __grid_constant__ CUtensorMap tm_ys, const Params p) {
   // tm_x: X blocks and tm_y: Y tiles, box 64 x 128 x 4 (four chunks, 64 KB);
-  // tm_ys: Y slabs, box 64 x 32 x KC.
+  // tm_ys: Y slabs, box 64 x 64 x KC.
   using C = Cfg<MODE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -634,8 +631,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     } else if (warp == FWD_WARP) {
-      if constexpr (C::kBulk) {
-       if (lane == 0) {
+      if (lane == 0) {
         // ---- P forwarder: staging copy -> the A CTA's P slot ----
         // Per tile, each 16 KB column chunk goes in one bulk DSMEM copy that
         // completes the slot's mbarrier in the A CTA (which expects the whole
@@ -683,14 +679,13 @@ __global__ void __launch_bounds__(THREADS, 1)
           while (clock64() - c0 < 200000) {
           }
         }
-       }
       }
     } else {
-      // ---- Z epilogue: z tile -> P tile in the peer's shared memory ----
+      // ---- Z epilogue: z tile -> P tile in a staging copy ----
       // Warp w reads TMEM lanes 32 (w % 4) .. +31 (its 32 rows) and columns
       // 32 (w / 4) .. +31 of each tile: one 32-column chunk per warp and tile,
-      // four warps per scheduler so that TMEM loads, math and the DSMEM stores
-      // of different warps overlap.
+      // four warps per scheduler so that TMEM loads, math and the stores of
+      // different warps overlap.
       const int q = warp & 3;
       const int cq = warp >> 2;     // 32-column group of the tile
       const int m = q * 32 + lane;  // row of the P tile (= TMEM lane)
@@ -710,13 +705,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       int cur_hit = -1, pf_hit = -1;
       float cur_pm1 = 0.f, pf_pm1 = 0.f;
       const int use_pm1 = p.nll_in != nullptr;
-      const uint32_t stg = smem_u32(smem + C::Z_STG);                 // bulk modes
-      const uint32_t peer_p = mapa_shared(smem_u32(smem + C::A_P), 1);  // FD
-      const uint32_t peer_pfull = mapa_shared(smem_u32(p_full), 1);     // FD
+      const uint32_t stg = smem_u32(smem + C::Z_STG);
       const uint32_t peer_rd_full = mapa_shared(smem_u32(rd_full), 1);
-      int acc = 0, slot = 0;
-      uint32_t aph = 0, sph = 0;
-      int staged = 0;  // bulk modes: tiles staged; tile n uses staging copy n % NSTG
+      int acc = 0;
+      uint32_t aph = 0;
+      int staged = 0;  // tiles staged; tile n uses staging copy n % NSTG
       bool ok = true;
       int fd_units = 0;
       for (int u = cluster; u < p.n_units && ok; u += n_clusters) {
@@ -833,46 +826,26 @@ __global__ void __launch_bounds__(THREADS, 1)
             else
               g_chunk_dw<false>(r, kc, cur_nl, cur_hit, m, use_pm1, cur_pm1, packed);
           }
-          if constexpr (C::kBulk) {
-            // Four swizzled 16-byte stores into the staging copy (the P slot
-            // layout), once that copy's previous tile has reached the A CTA;
-            // the forwarder warp then sends each 64-column chunk in one bulk
-            // copy.
-            const int set = staged % C::NSTG;
-            ok = mbar_wait<true>(stg_empty + set, (static_cast<uint32_t>(staged / C::NSTG) & 1u) ^ 1u, abort_flag,
-                                 p.status);
-            if (!ok) break;
-            const uint32_t dst_row =
-                stg + static_cast<uint32_t>(2 * set + (cq >> 1)) * CHUNK + static_cast<uint32_t>(m) * 128u;
+          // Four swizzled 16-byte stores into the staging copy (the P slot
+          // layout), once that copy's previous tile has reached the A CTA;
+          // the forwarder warp then sends each 64-column chunk in one bulk
+          // copy.
+          const int set = staged % C::NSTG;
+          ok = mbar_wait<true>(stg_empty + set, (static_cast<uint32_t>(staged / C::NSTG) & 1u) ^ 1u, abort_flag,
+                               p.status);
+          if (!ok) break;
+          const uint32_t dst_row =
+              stg + static_cast<uint32_t>(2 * set + (cq >> 1)) * CHUNK + static_cast<uint32_t>(m) * 128u;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint32_t unit = static_cast<uint32_t>((cq & 1) * 4 + v);
-              const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
-              st_shared_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
-            }
-            fence_proxy_async_smem();  // visible to the bulk copy (async proxy)
-            __syncwarp();
-            if (lane == 0) mbar_arrive(stg_full + 2 * set + (cq >> 1));
-            ++staged;
-          } else {
-            // Four swizzled 16-byte DSMEM stores into the P slot, once the A
-            // CTA's MMA no longer reads it.
-            ok = mbar_wait<true>(p_empty + slot, sph ^ 1u, abort_flag, p.status);
-            if (!ok) break;
-            const uint32_t dst_row = peer_p + static_cast<uint32_t>(slot) * P_SLOT +
-                                     static_cast<uint32_t>(cq >> 1) * CHUNK + static_cast<uint32_t>(m) * 128u;
-            const uint32_t pfull_slot = peer_pfull + static_cast<uint32_t>(slot) * 8u;
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              const uint32_t unit = static_cast<uint32_t>((cq & 1) * 4 + v);
-              const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
-              st_async_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3], pfull_slot);
-            }
-            if (++slot == C::NPS) {
-              slot = 0;
-              sph ^= 1u;
-            }
+          for (int v = 0; v < 4; ++v) {
+            const uint32_t unit = static_cast<uint32_t>((cq & 1) * 4 + v);
+            const uint32_t addr = dst_row + ((unit ^ static_cast<uint32_t>(m & 7)) << 4);
+            st_shared_v4(addr, packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
           }
+          fence_proxy_async_smem();  // visible to the bulk copy (async proxy)
+          __syncwarp();
+          if (lane == 0) mbar_arrive(stg_full + 2 * set + (cq >> 1));
+          ++staged;
         }
         if (MODE == FD) {
           // Row record for the A drain, once it has read the previous one.
@@ -895,7 +868,7 @@ __global__ void __launch_bounds__(THREADS, 1)
     // =========================== A CTA ===========================
     if (warp == TMA_WARP) {
       if (lane == 0) {
-        // The Y tiles arrive in slabs of 32 rows x d (one load each) through
+        // The Y tiles arrive in slabs of 64 rows x d (one load each) through
         // a ring of ASLOTS slab slots.
         int rs = 0;
         uint32_t rph = 0;
@@ -962,11 +935,13 @@ __global__ void __launch_bounds__(THREADS, 1)
               ok = mbar_wait(ay_full + rs, rph, abort_flag, p.status);
               if (!ok) break;
               tc_fence_after();
-              // The slab's two K steps of 16 rows (2 KB apart); P: chunk sl / 2,
-              // K columns 32 (sl % 2) + 16 kk (32 bytes per step).  MN-major B:
-              // N = 64 nh columns of d in chunks 4 KB apart inside the slab.
+              // The slab's four K steps of 16 rows (2 KB apart); P: the chunk
+              // of K columns 64 sl .. +63, 16 kk + .. (32 bytes per step).
+              // MN-major B: N = 64 nh columns of d in chunks 8 KB apart inside
+              // the slab.
               const uint64_t bd0 = sdesc_sw128(smem_u32(smem + C::A_Y + rs * p.KC * SLAB_CHUNK), SLAB_CHUNK, 1024);
-              const uint64_t ad0 = pdesc + static_cast<uint64_t>(((sl >> 1) * CHUNK + (sl & 1) * 64) >> 4);
+              const int pc0 = sl * SLAB_ROWS;  // first P column (K row) of the slab
+              const uint64_t ad0 = pdesc + static_cast<uint64_t>(((pc0 / KB) * CHUNK + (pc0 % KB) * 2) >> 4);
 #pragma unroll
               for (int kk = 0; kk < SLAB_ROWS / 16; ++kk) {
                 const uint32_t accf = (i != 0 || sl != 0 || kk != 0) ? 1u : 0u;
@@ -998,8 +973,7 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
       }
     } else if (warp == FWD_WARP) {
-      if constexpr (C::kBulk) {
-       if (lane == 0) {
+      if (lane == 0) {
         // ---- P acknowledgements: each tile's bytes have landed ----
         // The Z CTA's staging copy is free once the bulk copies into the P
         // slot have completed; the slots are visited in the MMA warp's order.
@@ -1021,7 +995,6 @@ __global__ void __launch_bounds__(THREADS, 1)
             }
           }
         }
-       }
       }
     } else {
       // ---- A drain: accumulator -> dh / dW ----
