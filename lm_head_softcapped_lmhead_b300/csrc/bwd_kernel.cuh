@@ -82,8 +82,13 @@ constexpr uint32_t P_SLOT = 2 * CHUNK;                // 32 KB: one 128 x 128 bf
 constexpr uint32_t Z_TMEM_X = 256;  // Z: the stationary block X in TMEM columns 256-511
 // FD: per-row records of the Z epilogue, [column group][row] x 32 bytes:
 // {double sum of e^s over the non-target columns, float e^{s_t},
-//  1 - tanh_t^2, int target, int flags}.
+//  1 - tanh_t^2, int target, int flags}.  They go through global memory
+// (L2): [cluster][column group][row], so the Z CTA's shared memory holds a
+// third P staging copy instead.
 constexpr uint32_t REC_BYTES = 32;
+constexpr int NREC_GROUPS = EPI_WARPS / 4;
+constexpr int kFdRecClusters = 128;  // clusters with a record area (launches use at most this many)
+constexpr size_t kFdRecClusterBytes = static_cast<size_t>(NREC_GROUPS) * BM * REC_BYTES;  // 16 KB
 constexpr int FL_LIVE = 1, FL_TVALID = 2, FL_HIT = 4;
 
 // Shared-memory plan of a mode.  The Z CTA holds a ring of Y stages (X is in
@@ -99,19 +104,17 @@ constexpr int FL_LIVE = 1, FL_TVALID = 2, FL_HIT = 4;
 // made every pass 40 % slower, and four 32-row slots in 128 KB were slower
 // than two 64-row ones (DW 1.135 against 1.004).  One 32 KB bulk copy per
 // tile instead of two 16 KB copies: FD 1.021, DW 0.991.  Three staging
-// copies against two: DW 0.983 against 1.004 (FD has room for two beside its
-// row records).
+// copies against two: DW 0.983 against 1.004.
 template <int MODE>
 struct Cfg {
   static constexpr int YSTAGES = 2;               // Z ring stages (64 KB)
-  static constexpr int NSTG = MODE == FD ? 2 : 3; // Z: P staging copies (32 KB)
+  static constexpr int NSTG = 3;                  // Z: P staging copies (32 KB)
   static constexpr int ASLOTS = 2;                // A: Y slab slots (64 KB)
   static constexpr int NPS = 3;                   // A: P slots (32 KB)
   // Z CTA layout
   static constexpr uint32_t Z_Y = 0;
   static constexpr uint32_t Z_STG = Z_Y + YSTAGES * ZSTAGE;          // NSTG x 2 x 16 KB
-  static constexpr uint32_t Z_REC = Z_STG + NSTG * 2 * CHUNK;        // FD row records
-  static constexpr uint32_t Z_END = Z_REC + (MODE == FD ? (EPI_WARPS / 4) * BM * REC_BYTES : 0u);
+  static constexpr uint32_t Z_END = Z_STG + NSTG * 2 * CHUNK;
   // A CTA layout
   static constexpr uint32_t A_Y = 0;
   static constexpr uint32_t A_P = A_Y + ASLOTS * MAX_KC * SLAB_CHUNK;
@@ -166,6 +169,7 @@ struct Params {
   int accumulate;
   float* dw_part;       // DW split partials [split][V_pad][d]
   int V_pad;
+  uint4* fd_rec;        // FD row records [cluster][NREC_GROUPS][BM] x 2 uint4 (global memory)
   unsigned* status;
 };
 
@@ -854,7 +858,8 @@ __global__ void __launch_bounds__(THREADS, 1)
             ok = mbar_wait<true>(rd_empty, static_cast<uint32_t>(fd_units - 1) & 1u, abort_flag, p.status);
             if (!ok) break;
           }
-          uint4* rec = reinterpret_cast<uint4*>(smem + C::Z_REC + (static_cast<uint32_t>(cq) * BM + m) * REC_BYTES);
+          // Global stores, ordered before the cluster-scope release arrival.
+          uint4* rec = p.fd_rec + (static_cast<size_t>(cluster * NREC_GROUPS + cq) * BM + m) * 2;
           const unsigned long long sb = static_cast<unsigned long long>(__double_as_longlong(s_acc));
           rec[0] = make_uint4(static_cast<uint32_t>(sb), static_cast<uint32_t>(sb >> 32), __float_as_uint(rec_tg.e),
                               __float_as_uint(rec_tg.om));
@@ -1005,7 +1010,6 @@ __global__ void __launch_bounds__(THREADS, 1)
       const int m = q * 32 + lane;
       constexpr int NPART = EPI_WARPS / 4;
       uint32_t fph = 0, rph = 0;
-      const uint32_t z_rec = mapa_shared(smem_u32(smem + C::Z_REC), 0);
       const uint32_t z_rd_empty = mapa_shared(smem_u32(rd_empty), 0);
       for (int u = cluster; u < p.n_units; u += n_clusters) {
         int blk, t0, t1;
@@ -1026,9 +1030,10 @@ __global__ void __launch_bounds__(THREADS, 1)
           uint32_t tsel = 0;
           double et = 0.0, om = 0.0;
 #pragma unroll
-          for (int g = 0; g < NPART; ++g) {
-            const uint32_t ra = z_rec + static_cast<uint32_t>(g * BM + m) * REC_BYTES;
-            const uint4 a0 = ld_cluster_v4(ra), a1 = ld_cluster_v4(ra + 16);
+          for (int g = 0; g < NREC_GROUPS; ++g) {
+            // After the cluster-scope acquire of rd_full; read at L2.
+            const uint4* ra = p.fd_rec + (static_cast<size_t>(cluster * NREC_GROUPS + g) * BM + m) * 2;
+            const uint4 a0 = __ldcg(ra), a1 = __ldcg(ra + 1);
             S_other += __hiloint2double(static_cast<int>(a0.y), static_cast<int>(a0.x));
             flags |= static_cast<int>(a1.y);
             tsel = a1.x;
@@ -1201,6 +1206,12 @@ inline int choose_split(long long N, long long V, int clusters) {
   return best;
 }
 
+// FD row-record area for N rows: one 16 KB area per cluster of the launch.
+inline size_t fd_rec_bytes(long long N) {
+  const long long blocks = cdivll(N, BM);
+  return static_cast<size_t>(blocks < kFdRecClusters ? blocks : kFdRecClusters) * kFdRecClusterBytes;
+}
+
 inline size_t scratch_bytes(long long N, long long V, long long d) {
   const long long nt = cdivll(N, BT);
   const long long s = nt < MAX_SPLIT ? nt : MAX_SPLIT;
@@ -1356,7 +1367,7 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
 // [N, ldh] bf16, for L = grad_scale * sum of nll over the scored rows.
 inline int launch_fd(const uint16_t* h, long long ldh, const uint16_t* W, long long N, long long V, long long d,
                      const int64_t* tgt, const uint8_t* mask, float c, float grad_scale, float* nll, float* lse,
-                     uint16_t* dh, unsigned* status, int dev, int sms, cudaStream_t s) {
+                     uint16_t* dh, unsigned* status, void* rec, int dev, int sms, cudaStream_t s) {
   CUtensorMap tm_hx, tm_wy, tm_ws;
   if (int rc = make_map_bf16_3d(&tm_hx, h, d, N, ldh * 2, BM, ZSC); rc) return rc;
   if (int rc = make_map_bf16_3d(&tm_wy, W, d, V, d * 2, BT, ZSC); rc) return rc;
@@ -1385,7 +1396,9 @@ inline int launch_fd(const uint16_t* h, long long ldh, const uint16_t* W, long l
   p.n_tiles = static_cast<int>(cdivll(V, BT));
   p.split = 1;
   p.n_units = p.n_blocks;
-  const int cl = static_cast<int>(p.n_units < clusters_max ? p.n_units : clusters_max);
+  p.fd_rec = static_cast<uint4*>(rec);
+  int cl = static_cast<int>(p.n_units < clusters_max ? p.n_units : clusters_max);
+  if (cl > kFdRecClusters) cl = kFdRecClusters;
   return launch_mode<FD>(tm_hx, tm_wy, tm_ws, p, cl, s);
 }
 

@@ -52,6 +52,7 @@ struct Layout {
   size_t rinv = 0;      // RMSNorm: [N] fp32 reciprocal RMS
   size_t dgp = 0;       // RMSNorm: [kNormBlocks][d] fp32 partials of the gain's gradient
   size_t bwd = 0;       // backward scratch
+  size_t fdrec = 0;     // forward + dh pass: per-cluster row records
   size_t total = 0;
 };
 
@@ -100,6 +101,8 @@ Layout make_layout(int64_t N, int64_t V, int64_t d, unsigned flags) {
   }
   L.bwd = o;
   o = up(o + lmce::bwdk::scratch_bytes(N, V, d));
+  L.fdrec = o;
+  o = up(o + lmce::bwdk::fd_rec_bytes(N));
   L.total = o;
   return L;
 }
@@ -290,8 +293,9 @@ int bwd_launch(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, i
 }
 int fd_launch(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int64_t V, int64_t d,
               const int64_t* tgt, const uint8_t* mask, float c, float grad_scale, float* nll, float* lse,
-              lmce_bf16* dh, unsigned* status, const DevInfo& di, cudaStream_t s) {
-  return lmce::bwdk::launch_fd(h, ldh, W, N, V, d, tgt, mask, c, grad_scale, nll, lse, dh, status, di.dev, di.sms, s);
+              lmce_bf16* dh, unsigned* status, void* rec, const DevInfo& di, cudaStream_t s) {
+  return lmce::bwdk::launch_fd(h, ldh, W, N, V, d, tgt, mask, c, grad_scale, nll, lse, dh, status, rec, di.dev,
+                               di.sms, s);
 }
 
 // Launch with programmatic stream serialization: the kernel's launch may
@@ -513,7 +517,9 @@ int fwd_bwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N,
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dh && use_fd(softcap)) {
     // Forward and dh in one pass over the vocabulary.
-    if (int rc = fd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, status, di, s); rc)
+    if (int rc = fd_launch(h, ldh, W, N, V, d, tgt, row_mask, softcap, grad_scale, nll, lse, dh, status,
+                           w + L.fdrec, di, s);
+        rc)
       return rc;
   } else {
     if (int rc = fwd_impl(h, ldh, W, N, V, d, tgt, row_mask, softcap, nll, lse, ws, ws_bytes, stream, extra_flags);
