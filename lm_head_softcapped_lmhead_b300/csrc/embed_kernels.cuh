@@ -18,13 +18,15 @@
 //               atomics; chunk-major hist[c][v]);
 //   2. tokscan: per token (one thread), the exclusive prefix of its counts
 //               over the chunks (in place), its rows, pieces and groups, and
-//               their scans inside 256-token blocks;
-//   3. tokfin:  the blocks' offsets added (every block scans the blocks'
-//               totals), each piece's token recorded;
-//   4. place:   per chunk, one warp walks the chunk's rows in order with the
-//               chunk's cursors in shared memory; lanes holding the same
-//               token take consecutive slots in lane order (stable);
-//   5. pieces:  one warp per piece sums its rows (bf16 -> fp32) in row
+//               their exclusive scans over all tokens in one pass (256-token
+//               blocks taken in ticket order publish their totals and add
+//               their predecessors': decoupled look-back); each piece's
+//               token recorded, the arrival counters zeroed;
+//   3. place:   per chunk, the cursors of the chunk's tokens are staged in
+//               shared memory, then one warp walks the chunk's rows in order;
+//               lanes holding the same token take consecutive slots in lane
+//               order (stable);
+//   4. pieces:  one warp per piece sums its rows (bf16 -> fp32) in row
 //               order; a token with one piece adds it into dW.  Otherwise the
 //               warp that completes the last piece of a group (an arrival
 //               counter) sums the group's pieces in order, and the warp that
@@ -63,8 +65,11 @@ inline long long max_pieces(long long N, long long V) {
 inline long long max_groups(long long N) { return N / 16 + 64; }
 
 struct Layout {
-  size_t hist, offs, pbase, gbase, perm, part, gpart, pcnt, gcnt, powner, btot, total;
+  size_t hist, offs, pbase, gbase, perm, part, gpart, pcnt, gcnt, powner, lb, total;
 };
+// Look-back records of the token scan: per 256-token block 8 ints {flag,
+// 3 block totals, 3 inclusive prefixes, unused}, then the block ticket.
+inline long long lb_ints(long long V) { return 8 * ((V + 255) / 256) + 8; }
 inline size_t up256(size_t x) { return (x + 255) & ~size_t(255); }
 inline Layout layout(long long N, long long V, long long d) {
   Layout L{};
@@ -89,8 +94,8 @@ inline Layout layout(long long N, long long V, long long d) {
   o = up256(o + sizeof(int) * static_cast<size_t>(V));
   L.powner = o; // [max_pieces] int: the token of each piece
   o = up256(o + sizeof(int) * static_cast<size_t>(max_pieces(N, V)));
-  L.btot = o;   // [3][blocks of 256 tokens] int: the blocks' totals
-  o = up256(o + sizeof(int) * 3 * static_cast<size_t>((V + 255) / 256));
+  L.lb = o;     // look-back records and ticket of the token scan
+  o = up256(o + sizeof(int) * static_cast<size_t>(lb_ints(V)));
   L.total = o;
   return L;
 }
@@ -106,10 +111,13 @@ __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol
 // 1. hist[c][v] = rows of chunk c with id v.  With use_smem (V <=
 //    kPlaceSmemV; dynamic shared memory of V ints) block c counts in shared
 //    memory and writes its row out whole; otherwise it zeroes its row and
-//    counts with global atomics.
+//    counts with global atomics.  Also zeroes the token scan's look-back
+//    records.
 __global__ void count_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int* __restrict__ hist,
-                             unsigned* status, int use_smem) {
+                             unsigned* status, int use_smem, int* __restrict__ lb, int lb_n) {
   extern __shared__ int s_hist[];
+  // The token scan's look-back records and ticket start at zero.
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < lb_n; k += gridDim.x * blockDim.x) lb[k] = 0;
   const int c = blockIdx.x;
   const int i0 = c * R, i1 = min(N, i0 + R);
   int* h = hist + static_cast<size_t>(c) * V;
@@ -159,14 +167,27 @@ __device__ __forceinline__ int block_scan_256(int x, int* s_warp, int* total) {
 
 // 2. Per token v (one thread of 256-thread blocks): hist[c][v] <- rows of v
 //    in chunks before c (in place); the rows, pieces and groups of v (only
-//    tokens with >= 2 pieces have groups), scanned inside the block, with
-//    the block's totals in btot.
+//    tokens with >= 2 pieces have groups) and their exclusive scans over all
+//    tokens into offs / pbase / gbase (totals at V).  The scan is one pass:
+//    blocks take tickets in start order, scan their 256 tokens, publish
+//    their totals (flag 1), then add the totals of the blocks before them
+//    (one warp reads 32 of them at a time), back to the nearest one that has
+//    published its inclusive prefix (flag 2), and publish their own.  A block only waits for blocks with lower
+//    tickets, which have started, so every wait ends; each is bounded all
+//    the same (ST_ETIMEOUT).  Then each piece records its token and the
+//    arrival counters of the token and its groups are zeroed.
 __global__ void __launch_bounds__(256) tokscan_kernel(int* __restrict__ hist, int C, int V, int* __restrict__ offs,
                                                       int* __restrict__ pbase, int* __restrict__ gbase,
-                                                      int* __restrict__ gcnt, int* __restrict__ btot) {
+                                                      int* __restrict__ gcnt, int* __restrict__ pcnt,
+                                                      int* __restrict__ powner, int* lb, unsigned* status) {
   wait_prior_grid();
   __shared__ int s_warp[8];
-  const int v = blockIdx.x * 256 + threadIdx.x;
+  __shared__ int s_b, s_ex[3];
+  const int nb = gridDim.x;
+  if (threadIdx.x == 0) s_b = atomicAdd(lb + 8 * nb, 1);
+  __syncthreads();
+  const int b = s_b;
+  const int v = b * 256 + threadIdx.x;
   int run = 0;
   if (v < V) {
     for (int c0 = 0; c0 < C; c0 += 16) {
@@ -182,76 +203,90 @@ __global__ void __launch_bounds__(256) tokscan_kernel(int* __restrict__ hist, in
   }
   const int np = (run + kPieceRows - 1) / kPieceRows;
   const int ng = np >= 2 ? (np + kGroupPieces - 1) / kGroupPieces : 0;
-  int ta, tb, tc;
-  const int la = block_scan_256(run, s_warp, &ta);
-  const int lb = block_scan_256(np, s_warp, &tb);
-  const int lc = block_scan_256(ng, s_warp, &tc);
-  if (v < V) {
-    offs[v] = la;
-    pbase[v] = lb;
-    gbase[v] = lc;
-    gcnt[v] = np;  // read (and zeroed) by tokfin_kernel
-  }
-  const int nb = gridDim.x;
-  if (threadIdx.x == 0) {
-    btot[blockIdx.x] = ta;
-    btot[nb + blockIdx.x] = tb;
-    btot[2 * nb + blockIdx.x] = tc;
-  }
-}
-
-// 3. Per token u (one thread, the same 256-token blocks): its block's
-//    offsets (each block scans the blocks' totals itself) are added to the
-//    block-local prefixes, so that offs / pbase / gbase hold the exclusive
-//    scans over all tokens (totals at V); each piece records its token (the
-//    token's piece count was left in gcnt, which then becomes the token's
-//    arrival counter, zeroed), and the groups' arrival counters are zeroed.
-__global__ void __launch_bounds__(256) tokfin_kernel(int V, int* __restrict__ offs, int* __restrict__ pbase,
-                                                     int* __restrict__ gbase, const int* __restrict__ btot,
-                                                     int* __restrict__ gcnt, int* __restrict__ pcnt,
-                                                     int* __restrict__ powner) {
-  wait_prior_grid();
-  __shared__ int s_warp[8];
-  __shared__ int s_off[3], s_tot[3];
-  const int nb = gridDim.x;
-  for (int q = 0; q < 3; ++q) {
-    int carry = 0, mine = 0;
-    for (int b0 = 0; b0 < nb; b0 += 256) {
-      const int bi = b0 + threadIdx.x;
-      const int x = bi < nb ? btot[q * nb + bi] : 0;
-      int t;
-      const int ex = block_scan_256(x, s_warp, &t);
-      if (bi == static_cast<int>(blockIdx.x)) mine = carry + ex;
-      carry += t;
+  int t[3];
+  const int la = block_scan_256(run, s_warp, &t[0]);
+  const int lpb = block_scan_256(np, s_warp, &t[1]);
+  const int lgb = block_scan_256(ng, s_warp, &t[2]);
+  if (threadIdx.x < 32) {
+    // Warp 0: publish this block's totals, then read up to 32 predecessors'
+    // records at once (lane k: block b - 1 - k - 32 r), adding their totals
+    // down to the nearest one that holds its inclusive prefix.
+    const int lane = threadIdx.x;
+    volatile int* rec = lb + 8 * b;
+    int ex[3] = {0, 0, 0};
+    if (b > 0) {
+      if (lane == 0) {
+        for (int k = 0; k < 3; ++k) rec[1 + k] = t[k];
+        __threadfence();
+        atomicExch(lb + 8 * b, 1);
+      }
+      __syncwarp();
+      const long long c0 = clock64();
+      int j_hi = b - 1;
+      for (;;) {
+        const int j = j_hi - lane;
+        const volatile int* pr = lb + 8 * (j >= 0 ? j : 0);
+        const int f = j >= 0 ? pr[0] : 2;  // before block 0: an inclusive prefix of 0
+        const unsigned inc_mask = __ballot_sync(0xffffffffu, f == 2);
+        const unsigned zero_mask = __ballot_sync(0xffffffffu, f == 0);
+        const int first_inc = inc_mask ? __ffs(inc_mask) - 1 : 32;
+        const unsigned need = first_inc >= 31 ? 0xffffffffu : ((2u << first_inc) - 1u);
+        if (zero_mask & need) {
+          if (clock64() - c0 > kWaitLimitCycles) {
+            if (lane == 0) atomicOr(status, ST_ETIMEOUT);
+            break;
+          }
+          continue;
+        }
+        __threadfence();
+        int x[3] = {0, 0, 0};
+        if (j >= 0 && lane <= first_inc) {
+          const int off = lane == first_inc ? 4 : 1;
+          for (int k = 0; k < 3; ++k) x[k] = pr[off + k];
+        }
+#pragma unroll
+        for (int k = 0; k < 3; ++k) {
+#pragma unroll
+          for (int o = 16; o > 0; o >>= 1) x[k] += __shfl_xor_sync(0xffffffffu, x[k], o);
+          ex[k] += x[k];
+        }
+        if (first_inc < 32) break;
+        j_hi -= 32;
+      }
     }
-    if (threadIdx.x == (blockIdx.x & 255u)) s_off[q] = mine;
-    if (threadIdx.x == 0) s_tot[q] = carry;
+    if (lane == 0) {
+      for (int k = 0; k < 3; ++k) rec[4 + k] = ex[k] + t[k];
+      __threadfence();
+      atomicExch(lb + 8 * b, 2);
+      for (int k = 0; k < 3; ++k) s_ex[k] = ex[k];
+      if (b == nb - 1) {
+        offs[V] = ex[0] + t[0];
+        pbase[V] = ex[1] + t[1];
+        gbase[V] = ex[2] + t[2];
+      }
+    }
   }
   __syncthreads();
-  const int u = blockIdx.x * 256 + threadIdx.x;
-  if (u < V) {
-    offs[u] += s_off[0];
-    const int pb = pbase[u] + s_off[1];
-    pbase[u] = pb;
-    gbase[u] += s_off[2];
-    const int np = gcnt[u];
-    gcnt[u] = 0;
-    for (int p = pb; p < pb + np; ++p) powner[p] = u;
+  if (v < V) {
+    offs[v] = s_ex[0] + la;
+    const int pb = s_ex[1] + lpb;
+    const int gb = s_ex[2] + lgb;
+    pbase[v] = pb;
+    gbase[v] = gb;
+    gcnt[v] = 0;
+    for (int p = pb; p < pb + np; ++p) powner[p] = v;
+    for (int q = gb; q < gb + ng; ++q) pcnt[q] = 0;
   }
-  if (blockIdx.x == static_cast<unsigned>(nb - 1) && threadIdx.x == 0) {
-    offs[V] = s_tot[0];
-    pbase[V] = s_tot[1];
-    gbase[V] = s_tot[2];
-  }
-  for (int q = u; q < s_tot[2]; q += nb * 256) pcnt[q] = 0;
 }
 
-// 4. Block c: warp 0 walks the chunk's rows in order, 32 at a time, and
+// 3. Block c: warp 0 walks the chunk's rows in order, 32 at a time, and
 //    writes each row index at its token's next slot; lanes with equal ids
 //    take consecutive slots in lane order, so each token's rows keep their
-//    row order (stable).  The chunk's cursors (offs[v] + hist[c][v]) are
-//    staged in shared memory when V <= kPlaceSmemV (dynamic shared memory of
-//    V ints), else updated in place in hist.
+//    row order (stable).  The cursors of the chunk's tokens (offs[v] +
+//    hist[c][v]) are staged in shared memory when V <= kPlaceSmemV (dynamic
+//    shared memory of V ints, of which only the chunk's tokens are written;
+//    threads holding the same token write the same value), else updated in
+//    place in hist.
 __global__ void place_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int* __restrict__ hist,
                              const int* __restrict__ offs, int* __restrict__ perm, int use_smem) {
   extern __shared__ int s_cur[];
@@ -259,20 +294,20 @@ __global__ void place_kernel(const int64_t* __restrict__ ids, int N, int V, int 
   const int c = blockIdx.x;
   int* hc = hist + static_cast<size_t>(c) * V;
   if (use_smem) {
-    // 8 independent loads of each array in flight per thread.
-    for (int v0 = threadIdx.x; v0 < V; v0 += 8 * blockDim.x) {
-      int a[8], b[8];
+    const int i0 = c * R, i1 = min(N, i0 + R);
+    for (int b0 = i0; b0 < i1; b0 += 4 * static_cast<int>(blockDim.x)) {
+      int tv[4], cur[4];
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int v = v0 + k * blockDim.x;
-        a[k] = v < V ? offs[v] : 0;
-        b[k] = v < V ? hc[v] : 0;
+      for (int k = 0; k < 4; ++k) {
+        const int i = b0 + k * blockDim.x + threadIdx.x;
+        const long long id = i < i1 ? ids[i] : -1;
+        tv[k] = id_ok(id, V) ? static_cast<int>(id) : -1;
       }
 #pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        const int v = v0 + k * blockDim.x;
-        if (v < V) s_cur[v] = a[k] + b[k];
-      }
+      for (int k = 0; k < 4; ++k) cur[k] = tv[k] >= 0 ? offs[tv[k]] + hc[tv[k]] : 0;
+#pragma unroll
+      for (int k = 0; k < 4; ++k)
+        if (tv[k] >= 0) s_cur[tv[k]] = cur[k];
     }
     __syncthreads();
   }
@@ -388,7 +423,7 @@ __device__ __forceinline__ bool arrive_last(int* counter, int last_value, int la
   return last;
 }
 
-// 5. Piece p (one warp): the sum, in row order, of its rows of g (bf16 ->
+// 4. Piece p (one warp): the sum, in row order, of its rows of g (bf16 ->
 //    fp32).  Lane l holds dims 8 l .. 8 l + 7 and 256 + 8 l .. + 7; eight
 //    rows' loads are in flight at once, the additions stay in row order.  A
 //    token with a single piece adds it into dW.  Otherwise part[p] = sum, and

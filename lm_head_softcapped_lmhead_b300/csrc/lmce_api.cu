@@ -892,16 +892,15 @@ int lmhead_tied_embed_bwd(const int64_t* ids, const lmce_bf16* g, int64_t ldg, i
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int use_smem = V <= ek::kPlaceSmemV ? 1 : 0;
   const size_t place_smem = use_smem ? sizeof(int) * static_cast<size_t>(V) : 0;
-  int* btot = reinterpret_cast<int*>(e + E.btot);
+  int* lb = reinterpret_cast<int*>(e + E.lb);
   const int nb = static_cast<int>(cdiv(V, 256));
-  lmce::count_launches(5);
-  ek::count_kernel<<<C, 256, place_smem, s>>>(ids, n, v, R, hist, status, use_smem);
+  lmce::count_launches(4);
+  ek::count_kernel<<<C, 256, place_smem, s>>>(ids, n, v, R, hist, status, use_smem, lb,
+                                              static_cast<int>(ek::lb_ints(V)));
   cudaError_t err = cudaGetLastError();
   if (err == cudaSuccess)
-    err = launch_pdl(ek::tokscan_kernel, nb, 256, 0, s, hist, C, v, offs, pbase, gbase, gcnt, btot);
-  if (err == cudaSuccess)
-    err = launch_pdl(ek::tokfin_kernel, nb, 256, 0, s, v, offs, pbase, gbase, static_cast<const int*>(btot), gcnt,
-                     pcnt, powner);
+    err = launch_pdl(ek::tokscan_kernel, nb, 256, 0, s, hist, C, v, offs, pbase, gbase, gcnt, pcnt, powner, lb,
+                     status);
   if (err == cudaSuccess)
     err = launch_pdl(ek::place_kernel, C, 256, place_smem, s, ids, n, v, R, hist, static_cast<const int*>(offs), perm,
                      use_smem);
