@@ -78,16 +78,19 @@ constexpr uint32_t IDESC = idesc_bf16_f32(PAIR_ROWS, BN, false, false);
 // and stage: 128 vocab rows x 64 bytes = 128 columns of d) through a 3-stage
 // ring, and CONV_WARPS converter warps write each stage's bf16 tile (the
 // 128B-swizzled layout the TMA writes in the bf16 form) into a 2 x 32 KB
-// ring.  (One-chunk stages, 4 x 16 KB, were slower: each stage hand-off
-// between the converters and the pair MMA costs about the same time
-// whatever the stage's size.)
+// ring.  A stage's conversion sits between the packed load and the pair
+// MMA, so the converters' speed sets the form's pace: at N=65536, 2 / 4 / 8 /
+// 16 converter warps took 2.00 / 1.33 / 1.04 / 1.10 ms (16 leaves 72
+// registers a thread and spills).  One-chunk stages, 4 x 16 KB, were slower.
 template <bool kInt4>
 struct FCfg {
   static constexpr int SC = 2;                        // 64-column chunks per stage
   static constexpr uint32_t STAGE = SC * W_CHUNK;     // bytes of one bf16 stage
   static constexpr int STAGES = kInt4 ? 2 : 3;        // bf16 ring stages
   static constexpr int PSTAGES = kInt4 ? 3 : 0;       // packed ring stages
-  static constexpr int CONV_WARPS = kInt4 ? 2 : 0;    // warps 10, 11
+  static constexpr int CONV_WARPS = kInt4 ? 8 : 0;    // warps 10 .. 17
+  static constexpr int CONV_ROWS = kInt4 ? HALF_N / CONV_WARPS : 0;  // vocab rows per converter warp
+  static constexpr int CONV_IT = kInt4 ? CONV_ROWS / 4 : 1;         // rows per lane (4 per iteration)
   static constexpr int THREADS = 320 + 32 * CONV_WARPS;
   static constexpr uint32_t PK_ROW = 32 * SC;         // packed bytes per vocab row and stage
   static constexpr uint32_t PK_STAGE = HALF_N * PK_ROW;
@@ -326,13 +329,11 @@ __device__ __forceinline__ uint4 int4_word_to_bf16x8(uint32_t w, float scale) {
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-// Converter lane layout: in iteration i (0..15) lane l of converter warp cw
-// handles row r = 64 cw + 4 i + l / 8 of the CTA's 128 vocab rows and the
-// 16-byte unit u = l % 8 (8 columns) of each 64-column chunk of the stage, so
-// a warp reads 4 consecutive packed rows and writes 4 whole 128-byte rows of
-// the swizzled bf16 chunk per instruction.
-constexpr int CONV_ITERS = 16;
-
+// Converter lane layout: in iteration i (0 .. CONV_IT - 1) lane l of
+// converter warp cw handles row r = CONV_ROWS cw + 4 i + l / 8 of the CTA's
+// 128 vocab rows and the 16-byte unit u = l % 8 (8 columns) of each 64-column
+// chunk of the stage, so a warp reads 4 consecutive packed rows and writes 4
+// whole 128-byte rows of the swizzled bf16 chunk per instruction.
 template <bool kOnline, bool kInt4 = false>
 __global__ void __launch_bounds__(FCfg<kInt4>::THREADS, 1)
     fwd_kernel(const __grid_constant__ CUtensorMap tm_h, const __grid_constant__ CUtensorMap tm_w,
@@ -543,21 +544,22 @@ __global__ void __launch_bounds__(FCfg<kInt4>::THREADS, 1)
       const int ngr = p.d / p.qgroup;  // scales per vocab row
       const uint32_t lead_full = mapa_shared(smem_u32(full), 0);
       // scales of stage (g, pr) for this lane's 16 rows and both chunks
-      auto load_scales = [&](long long g, int pr, float (&sc)[CONV_ITERS][2]) {
+      auto load_scales = [&](long long g, int pr, float (&sc)[C::CONV_IT][2]) {
         const int vt = static_cast<int>(g % p.VT);
         const int gi0 = (64 * SC * pr + 8 * u) / p.qgroup;
         const int gi1 = (64 * SC * pr + 64 + 8 * u) / p.qgroup;
         const bool two = SC == 2 && SC * pr + 1 < p.KC;
 #pragma unroll
-        for (int i = 0; i < CONV_ITERS; ++i) {
-          const long long v = static_cast<long long>(vt) * BN + static_cast<int>(rank) * HALF_N + 64 * cw + 4 * i + rsub;
+        for (int i = 0; i < C::CONV_IT; ++i) {
+          const long long v =
+              static_cast<long long>(vt) * BN + static_cast<int>(rank) * HALF_N + C::CONV_ROWS * cw + 4 * i + rsub;
           const bool valid = v < p.V;
           const __half* row = p.qscales + (valid ? v : 0) * ngr;
           sc[i][0] = valid ? __half2float(row[gi0]) : 0.f;
           sc[i][1] = (valid && two) ? __half2float(row[gi1]) : 0.f;
         }
       };
-      float sc_cur[CONV_ITERS][2], sc_nxt[CONV_ITERS][2];
+      float sc_cur[C::CONV_IT][2], sc_nxt[C::CONV_IT][2];
       load_scales(g_begin, 0, sc_cur);
       int stage = 0, ps = 0;
       uint32_t phase = 0, pph = 0;
@@ -574,8 +576,8 @@ __global__ void __launch_bounds__(FCfg<kInt4>::THREADS, 1)
           uint8_t* dst = smem + SMEM_RING + stage * STAGE;
           const uint8_t* pk = smem + C::SMEM_PK + ps * C::PK_STAGE;
 #pragma unroll
-          for (int i = 0; i < CONV_ITERS; ++i) {
-            const int r = 64 * cw + 4 * i + rsub;
+          for (int i = 0; i < C::CONV_IT; ++i) {
+            const int r = C::CONV_ROWS * cw + 4 * i + rsub;
 #pragma unroll
             for (int c = 0; c < SC; ++c) {
               if (c < nch) {
@@ -602,7 +604,7 @@ __global__ void __launch_bounds__(FCfg<kInt4>::THREADS, 1)
             pph ^= 1u;
           }
 #pragma unroll
-          for (int i = 0; i < CONV_ITERS; ++i) {
+          for (int i = 0; i < C::CONV_IT; ++i) {
             sc_cur[i][0] = sc_nxt[i][0];
             sc_cur[i][1] = sc_nxt[i][1];
           }
