@@ -543,7 +543,7 @@ def run_table(args):
                         fwd_step(side)
                 stream.wait_stream(side)
                 g_ms = gpu_ms(graph.replay)
-                notes.append(f"workload 1 as a CUDA graph replay (4 kernels): {g_ms:.4f} ms per step, "
+                notes.append(f"workload 1 as a CUDA graph replay (3 kernels): {g_ms:.4f} ms per step, "
                              f"{N / g_ms / 1e3:.2f} M tokens/s (eager: {ms:.4f} ms)")
             else:
                 # The whole stream (8,388,608 scored tokens) does not fit in HBM

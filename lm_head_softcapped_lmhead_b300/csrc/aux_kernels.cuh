@@ -80,16 +80,23 @@ constexpr int kBpbThreads = 256;
 // Bytes per row: nbytes[i], or with a per-id table lut[tgt[i]] (the
 // tokenizer's byte length of the scored token); a scored row whose target is
 // outside [0, V) then counts nothing and raises ST_EDATA.
-__global__ void __launch_bounds__(kBpbThreads) bpb_partial_kernel(const float* __restrict__ nll,
-                                                                  const int32_t* __restrict__ nbytes,
-                                                                  const uint8_t* __restrict__ mask, long long N,
-                                                                  BpbPartial* __restrict__ out,
-                                                                  const int64_t* __restrict__ tgt = nullptr,
-                                                                  const int32_t* __restrict__ lut = nullptr,
-                                                                  long long V = 0, unsigned* status = nullptr) {
+// Each block adds its rows in a fixed tree and stores its partial; the block
+// that stores the last partial (an arrival counter in the workspace, zero
+// between calls) adds the kBpbBlocks partials in a fixed tree and makes one
+// ordered, non-atomic update of the caller's accumulator.  Which block does
+// that varies; the order of every sum does not.
+__global__ void __launch_bounds__(kBpbThreads) bpb_kernel(const float* __restrict__ nll,
+                                                          const int32_t* __restrict__ nbytes,
+                                                          const uint8_t* __restrict__ mask, long long N,
+                                                          BpbPartial* part, BpbPartial* acc, unsigned* cnt,
+                                                          const int64_t* __restrict__ tgt = nullptr,
+                                                          const int32_t* __restrict__ lut = nullptr,
+                                                          long long V = 0, unsigned* status = nullptr) {
+  static_assert(kBpbThreads == kBpbBlocks, "the last block adds one partial per thread");
   __shared__ double s_nll[kBpbThreads];
   __shared__ long long s_b[kBpbThreads];
   __shared__ long long s_n[kBpbThreads];
+  __shared__ int s_last;
   double a = 0.0;
   long long b = 0, c = 0;
   const long long stride = static_cast<long long>(kBpbBlocks) * kBpbThreads;
@@ -110,44 +117,39 @@ __global__ void __launch_bounds__(kBpbThreads) bpb_partial_kernel(const float* _
     b += nb;
     c += 1;
   }
+  auto tree = [&]() {
+    __syncthreads();
+    for (int w = kBpbThreads / 2; w > 0; w >>= 1) {
+      if (threadIdx.x < w) {
+        s_nll[threadIdx.x] += s_nll[threadIdx.x + w];
+        s_b[threadIdx.x] += s_b[threadIdx.x + w];
+        s_n[threadIdx.x] += s_n[threadIdx.x + w];
+      }
+      __syncthreads();
+    }
+  };
   s_nll[threadIdx.x] = a;
   s_b[threadIdx.x] = b;
   s_n[threadIdx.x] = c;
-  __syncthreads();
-  for (int w = kBpbThreads / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) {
-      s_nll[threadIdx.x] += s_nll[threadIdx.x + w];
-      s_b[threadIdx.x] += s_b[threadIdx.x + w];
-      s_n[threadIdx.x] += s_n[threadIdx.x + w];
-    }
-    __syncthreads();
+  tree();
+  if (threadIdx.x == 0) {
+    part[blockIdx.x] = BpbPartial{s_nll[0], s_b[0], s_n[0]};
+    __threadfence();
+    s_last = atomicAdd(cnt, 1u) == static_cast<unsigned>(kBpbBlocks - 1);
   }
-  if (threadIdx.x == 0) out[blockIdx.x] = BpbPartial{s_nll[0], s_b[0], s_n[0]};
-}
-
-// One block: adds the kBpbBlocks partials in a fixed tree, then adds the
-// result to the caller's accumulator (one ordered, non-atomic update).
-__global__ void __launch_bounds__(kBpbBlocks) bpb_final_kernel(const BpbPartial* __restrict__ part,
-                                                               BpbPartial* acc) {
-  __shared__ double s_nll[kBpbBlocks];
-  __shared__ long long s_b[kBpbBlocks];
-  __shared__ long long s_n[kBpbBlocks];
-  s_nll[threadIdx.x] = part[threadIdx.x].sum_nll;
-  s_b[threadIdx.x] = part[threadIdx.x].sum_bytes;
-  s_n[threadIdx.x] = part[threadIdx.x].n;
   __syncthreads();
-  for (int w = kBpbBlocks / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) {
-      s_nll[threadIdx.x] += s_nll[threadIdx.x + w];
-      s_b[threadIdx.x] += s_b[threadIdx.x + w];
-      s_n[threadIdx.x] += s_n[threadIdx.x + w];
-    }
-    __syncthreads();
-  }
+  if (!s_last) return;
+  __threadfence();  // the other blocks' partials are read after this
+  const BpbPartial* pt = part + threadIdx.x;
+  s_nll[threadIdx.x] = __ldcg(&pt->sum_nll);
+  s_b[threadIdx.x] = __ldcg(&pt->sum_bytes);
+  s_n[threadIdx.x] = __ldcg(&pt->n);
+  tree();
   if (threadIdx.x == 0) {
     acc->sum_nll += s_nll[0];
     acc->sum_bytes += s_b[0];
     acc->n += s_n[0];
+    *cnt = 0u;
   }
 }
 

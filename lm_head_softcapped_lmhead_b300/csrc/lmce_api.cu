@@ -801,6 +801,11 @@ int lmhead_ce_fwd_bwd_rmsnorm(const lmce_bf16* x, int64_t ldx, const float* g, f
                           reinterpret_cast<float*>(w + L.dgp), s);
 }
 
+// The bpb reduction's arrival counter: bytes 8..11 of the workspace's 64-byte
+// header (after the status word), zero from the caller's zero-fill and
+// reset by every reduction.
+unsigned* bpb_counter(void* ws) { return reinterpret_cast<unsigned*>(static_cast<char*>(ws) + 8); }
+
 int bpb_reduce(const float* nll, const int32_t* bytes, const uint8_t* row_mask, int64_t N, lmce_bpb_acc* acc,
                void* ws, size_t ws_bytes, void* stream) {
   if (!nll || !bytes || !acc || !ws || N < 1) return LMCE_EINVAL;
@@ -809,9 +814,9 @@ int bpb_reduce(const float* nll, const int32_t* bytes, const uint8_t* row_mask, 
   if (ws_bytes < L.bpb + sizeof(lmce::BpbPartial) * lmce::kBpbBlocks) return LMCE_EINVAL;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   auto* part = reinterpret_cast<lmce::BpbPartial*>(static_cast<char*>(ws) + L.bpb);
-  lmce::count_launches(2);
-  lmce::bpb_partial_kernel<<<lmce::kBpbBlocks, lmce::kBpbThreads, 0, s>>>(nll, bytes, row_mask, N, part);
-  lmce::bpb_final_kernel<<<1, lmce::kBpbBlocks, 0, s>>>(part, reinterpret_cast<lmce::BpbPartial*>(acc));
+  lmce::count_launches(1);
+  lmce::bpb_kernel<<<lmce::kBpbBlocks, lmce::kBpbThreads, 0, s>>>(
+      nll, bytes, row_mask, N, part, reinterpret_cast<lmce::BpbPartial*>(acc), bpb_counter(ws));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bpb_reduce launch");
   return LMCE_OK;
@@ -826,10 +831,10 @@ int bpb_reduce_lut(const float* nll, const int64_t* tgt, const int32_t* lut, int
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   char* w = static_cast<char*>(ws);
   auto* part = reinterpret_cast<lmce::BpbPartial*>(w + L.bpb);
-  lmce::count_launches(2);
-  lmce::bpb_partial_kernel<<<lmce::kBpbBlocks, lmce::kBpbThreads, 0, s>>>(
-      nll, nullptr, row_mask, N, part, tgt, lut, V, reinterpret_cast<unsigned*>(w + L.status));
-  lmce::bpb_final_kernel<<<1, lmce::kBpbBlocks, 0, s>>>(part, reinterpret_cast<lmce::BpbPartial*>(acc));
+  lmce::count_launches(1);
+  lmce::bpb_kernel<<<lmce::kBpbBlocks, lmce::kBpbThreads, 0, s>>>(
+      nll, nullptr, row_mask, N, part, reinterpret_cast<lmce::BpbPartial*>(acc), bpb_counter(ws), tgt, lut, V,
+      reinterpret_cast<unsigned*>(w + L.status));
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return cuda_fail(e, "bpb_reduce_lut launch");
   return LMCE_OK;
