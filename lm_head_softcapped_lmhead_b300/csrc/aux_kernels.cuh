@@ -46,7 +46,9 @@ __global__ void fwd_finalize_kernel(const float* __restrict__ part, int VT, int 
     }
     // S holds the non-target terms and st[r] the target's e^{s_t}:
     // nll = -ln p_t = log1p(S / e^{s_t}) keeps its relative precision as
-    // p_t -> 1.
+    // p_t -> 1.  The partials are added in fp64; the logarithms are taken in
+    // fp32 (a few ulp, far below the forward's tolerance, and without the
+    // slow fp64 pipe).
     const int64_t t = tgt[r];
     float v, l;
     if (timed_out) {
@@ -54,11 +56,12 @@ __global__ void fwd_finalize_kernel(const float* __restrict__ part, int VT, int 
     } else if (t < 0 || t >= V) {
       atomicOr(status, ST_EDATA);
       v = __int_as_float(0x7fc00000);
-      l = static_cast<float>(log(S));
+      l = logf(static_cast<float>(S));
     } else {
-      const double et = static_cast<double>(st[r]);
-      v = static_cast<float>(log1p(S / et));
-      l = static_cast<float>(log(S + et));
+      const float et = st[r];
+      const float Sf = static_cast<float>(S);
+      v = log1pf(Sf / et);
+      l = logf(static_cast<float>(S + static_cast<double>(et)));
     }
     const int o = idx ? idx[r] : r;
     nll[o] = v;
@@ -100,22 +103,44 @@ __global__ void __launch_bounds__(kBpbThreads) bpb_kernel(const float* __restric
   double a = 0.0;
   long long b = 0, c = 0;
   const long long stride = static_cast<long long>(kBpbBlocks) * kBpbThreads;
-  for (long long i = static_cast<long long>(blockIdx.x) * kBpbThreads + threadIdx.x; i < N; i += stride) {
-    if (mask && !mask[i]) continue;
-    int32_t nb;
-    if (lut) {
-      const int64_t t = tgt[i];
-      if (t < 0 || t >= V) {
-        atomicOr(status, ST_EDATA);
-        continue;
-      }
-      nb = lut[t];
-    } else {
-      nb = nbytes[i];
+  // A thread's rows i0, i0 + stride, ... in that order, four at a time with
+  // their loads issued together.
+  constexpr int kB = 4;
+  for (long long i0 = static_cast<long long>(blockIdx.x) * kBpbThreads + threadIdx.x; i0 < N; i0 += kB * stride) {
+    bool live[kB];
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const long long i = i0 + k * stride;
+      live[k] = i < N && (!mask || mask[i]);
     }
-    a += static_cast<double>(nll[i]);
-    b += nb;
-    c += 1;
+    float nv[kB];
+    int32_t nb[kB];
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      const long long i = i0 + k * stride;
+      nv[k] = 0.f;
+      nb[k] = 0;
+      if (!live[k]) continue;
+      if (lut) {
+        const int64_t t = tgt[i];
+        if (t < 0 || t >= V) {
+          atomicOr(status, ST_EDATA);
+          live[k] = false;
+          continue;
+        }
+        nb[k] = lut[t];
+      } else {
+        nb[k] = nbytes[i];
+      }
+      nv[k] = nll[i];
+    }
+#pragma unroll
+    for (int k = 0; k < kB; ++k) {
+      if (!live[k]) continue;
+      a += static_cast<double>(nv[k]);
+      b += nb[k];
+      c += 1;
+    }
   }
   auto tree = [&]() {
     __syncthreads();
@@ -183,14 +208,16 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return before;
 }
 
-// pass 1: scored-row count per block of kCompactRows rows.
+// pass 1: scored-row count per block of kCompactRows rows (thread t reads
+// rows base + 256 k + t: coalesced).
 __global__ void __launch_bounds__(kCompactThreads) compact_count_kernel(const uint8_t* __restrict__ mask, int N,
                                                                         int* __restrict__ block_count) {
   __shared__ int s_warp[kCompactThreads / 32];
-  const int base = blockIdx.x * kCompactRows + threadIdx.x * (kCompactRows / kCompactThreads);
+  const int base = blockIdx.x * kCompactRows + threadIdx.x;
   int c = 0;
+#pragma unroll
   for (int k = 0; k < kCompactRows / kCompactThreads; ++k) {
-    const int i = base + k;
+    const int i = base + k * kCompactThreads;
     if (i < N && mask[i]) ++c;
   }
   int total;
@@ -216,30 +243,35 @@ __global__ void __launch_bounds__(kCompactThreads) compact_scan_kernel(int* __re
 }
 
 // pass 3: scored rows get their compacted index (idx[pos] = i, targets
-// gathered); masked rows get nll = 0 (and lse = 0).
+// gathered) in row order; masked rows get nll = 0 (and lse = 0).  The block
+// takes its rows in 256-row slices (thread t: row base + 256 k + t), each
+// slice's positions from a block-wide scan, so loads and stores coalesce.
 __global__ void __launch_bounds__(kCompactThreads) compact_write_kernel(
     const uint8_t* __restrict__ mask, int N, const int* __restrict__ block_offset, const int64_t* __restrict__ tgt,
     int* __restrict__ idx, int64_t* __restrict__ tgt_c, float* __restrict__ nll, float* __restrict__ lse) {
   __shared__ int s_warp[kCompactThreads / 32];
   constexpr int R = kCompactRows / kCompactThreads;
-  const int base = blockIdx.x * kCompactRows + threadIdx.x * R;
-  int c = 0;
+  const int base = blockIdx.x * kCompactRows + threadIdx.x;
+  bool m[R];
+#pragma unroll
   for (int k = 0; k < R; ++k) {
-    const int i = base + k;
-    if (i < N && mask[i]) ++c;
+    const int i = base + k * kCompactThreads;
+    m[k] = i < N && mask[i];
   }
-  int pos = block_offset[blockIdx.x] + block_exclusive_scan(c, s_warp, nullptr);
+  int pos = block_offset[blockIdx.x];
+#pragma unroll
   for (int k = 0; k < R; ++k) {
-    const int i = base + k;
-    if (i >= N) break;
-    if (mask[i]) {
-      idx[pos] = i;
-      tgt_c[pos] = tgt[i];
-      ++pos;
-    } else {
+    const int i = base + k * kCompactThreads;
+    int tot;
+    const int ex = block_exclusive_scan(m[k] ? 1 : 0, s_warp, &tot);
+    if (m[k]) {
+      idx[pos + ex] = i;
+      tgt_c[pos + ex] = tgt[i];
+    } else if (i < N) {
       if (nll) nll[i] = 0.f;
       if (lse) lse[i] = 0.f;
     }
+    pos += tot;
   }
 }
 
