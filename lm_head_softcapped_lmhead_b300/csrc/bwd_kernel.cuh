@@ -98,13 +98,15 @@ constexpr int FL_LIVE = 1, FL_TVALID = 2, FL_HIT = 4;
 // copy into an A CTA P slot.
 // What the measurements favoured (N=65536, V=8192, d=512, ms per pass): few
 // large transfers between the CTAs' rings over many small ones.  Y slabs of
-// 64 rows (two 64 KB slots) against 32 rows (two 32 KB slots, 5 P slots):
-// DW 0.983 against 1.078, FD 1.018 against 1.044 (FD then stored P with
-// st.async), DH 0.936 against 0.954; four 16-row slots in the same 64 KB
-// made every pass 40 % slower, and four 32-row slots in 128 KB were slower
-// than two 64-row ones (DW 1.135 against 1.004).  One 32 KB bulk copy per
-// tile instead of two 16 KB copies: FD 1.021, DW 0.991.  Three staging
-// copies against two: DW 0.983 against 1.004.
+// 64 rows (two 64 KB slots) against 32 rows (two 32 KB slots, 4-5 P slots):
+// DW 0.983 against 1.078, DH 0.936 against 0.954, FD 1.018 against 1.044
+// (the 32-row FD form stored P into the peer with st.async, which was the
+// faster hand-off there); four 16-row slots in the same 64 KB made every pass
+// 40 % slower, and four 32-row slots in 128 KB were slower than two 64-row
+// ones (DW 1.135 against 1.004).  One 32 KB bulk copy per tile instead of
+// two 16 KB copies: FD 1.021, DW 0.991.  Three staging copies against two:
+// DW 0.983 against 1.004, FD 0.973 against 1.016 (FD's row records moved to
+// global memory to make room).
 template <int MODE>
 struct Cfg {
   static constexpr int YSTAGES = 2;               // Z ring stages (64 KB)
