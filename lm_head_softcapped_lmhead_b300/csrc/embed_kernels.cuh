@@ -172,10 +172,11 @@ __device__ __forceinline__ int block_scan_256(int x, int* s_warp, int* total) {
 //    blocks take tickets in start order, scan their 256 tokens, publish
 //    their totals (flag 1), then add the totals of the blocks before them
 //    (one warp reads 32 of them at a time), back to the nearest one that has
-//    published its inclusive prefix (flag 2), and publish their own.  A block only waits for blocks with lower
-//    tickets, which have started, so every wait ends; each is bounded all
-//    the same (ST_ETIMEOUT).  Then each piece records its token and the
-//    arrival counters of the token and its groups are zeroed.
+//    published its inclusive prefix (flag 2), and publish their own.  A
+//    block only waits for blocks with lower tickets, which have started, so
+//    every wait ends; each is bounded all the same (ST_ETIMEOUT).  Then
+//    each piece records its token and the arrival counters of the token and
+//    its groups are zeroed.
 __global__ void __launch_bounds__(256) tokscan_kernel(int* __restrict__ hist, int C, int V, int* __restrict__ offs,
                                                       int* __restrict__ pbase, int* __restrict__ gbase,
                                                       int* __restrict__ gcnt, int* __restrict__ pcnt,
