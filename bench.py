@@ -474,16 +474,18 @@ def run_table(args):
     peak = measured_peaks()[0]
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    reps = max(args.steps, 3)
+    # At least 10 warm-up calls, then the median of at least 50 timed calls.
+    reps = max(args.steps, 50)
+    warm = max(args.warmup, 10)
 
     def bf(bits):
         return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(dev)
 
     def gpu_ms(fn):
-        for _ in range(max(args.warmup, 3)):
+        for _ in range(warm):
             fn()
         torch.cuda.synchronize()
-        total = 0.0
+        times = []
         for _ in range(reps):
             flush.zero_()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -491,8 +493,8 @@ def run_table(args):
             fn()
             e1.record(stream)
             e1.synchronize()
-            total += e0.elapsed_time(e1)
-        return total / reps
+            times.append(e0.elapsed_time(e1))
+        return statistics.median(times)
 
     def oracle_rate(h_bits, W_bits, tgt, nbytes, kind, target_s=4.0):
         W = oracle.widen_bf16(W_bits)
