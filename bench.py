@@ -223,10 +223,18 @@ def run_ours(args, rank, world, local_rank):
     n_warm = 0
     t_w0 = time.perf_counter()
     min_warm_s = 0.0 if args.profile else 1.0
-    while n_warm < max(args.warmup, 3) or time.perf_counter() - t_w0 < min_warm_s:
-        step()
-        flush.zero_()
-        n_warm += 1
+
+    def warm_more():
+        more = n_warm < max(args.warmup, 3) or time.perf_counter() - t_w0 < min_warm_s
+        # Each step holds collectives, so every rank must run the same
+        # number of warm-up steps: the ranks decide together.
+        return ldist.any_rank(more) if world > 1 else more
+
+    while warm_more():
+        for _ in range(8 if world > 1 else 1):
+            step()
+            flush.zero_()
+            n_warm += 1
         if n_warm % 16 == 0:
             torch.cuda.synchronize()
     torch.cuda.synchronize()

@@ -66,6 +66,19 @@ def combine_bpb_acc(gathered: torch.Tensor) -> tuple:
     return combine_bpb([(float(g[r, 0]), int(ints[r, 1]), int(ints[r, 2])) for r in range(g.shape[0])])
 
 
+def any_rank(flag: bool, group=None) -> bool:
+    """True on every rank if `flag` is true on any rank.  Loops whose steps
+    hold collectives (the benchmark's warm-up runs until a time has passed)
+    decide with it, so that every rank runs the same number of steps."""
+    import torch.distributed as dist
+
+    backend = dist.get_backend(group)
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([1 if flag else 0], dtype=torch.int32, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX, group=group)
+    return bool(t.item())
+
+
 def allreduce_dW(dW: torch.Tensor, group=None) -> torch.Tensor:
     """Sum the tied-table gradient over ranks in place."""
     import torch.distributed as dist

@@ -2,7 +2,9 @@
 shard (with the CPU oracle standing in for a GPU's forward), add their input
 positions' embedding gradients into the same table gradient, then combine
 the bits-per-byte sums and dW; the result equals the single-process answer
-(head dW plus every position's embedding gradient)."""
+(head dW plus every position's embedding gradient).  Also: a loop whose stop
+condition differs per rank runs the same number of collective steps on every
+rank when the ranks decide with dist.any_rank (the benchmark's warm-up)."""
 import math
 import os
 import socket
@@ -51,8 +53,19 @@ def _worker(rank, world, port, out_path):
     acc.view(torch.int64)[1] = sb
     acc.view(torch.int64)[2] = n
     tot2 = ld.combine_bpb_acc(ld.allgather_bpb_acc(acc))
+    # A loop whose stop condition differs per rank (the benchmark's timed
+    # warm-up) runs the same number of steps everywhere when the ranks decide
+    # together: here rank 1 would stop after 3 steps and rank 0 after 11.
+    steps = 0
+    while ld.any_rank(steps < (11 if rank == 0 else 3)):
+        dist.all_reduce(torch.ones(1))  # a step's collective
+        steps += 1
+    agree = [ld.any_rank(rank == 0), ld.any_rank(False)]
+    counts = [torch.zeros(1, dtype=torch.int64) for _ in range(world)]
+    dist.all_gather(counts, torch.tensor([steps]))
     if rank == 0:
-        np.savez(out_path, sn=tot[0], sb=tot[1], n=tot[2], dW=dWt.numpy(), sn2=tot2[0], sb2=tot2[1], n2=tot2[2])
+        np.savez(out_path, sn=tot[0], sb=tot[1], n=tot[2], dW=dWt.numpy(), sn2=tot2[0], sb2=tot2[1], n2=tot2[2],
+                 steps=np.array([int(c) for c in counts]), agree=np.array(agree))
     dist.barrier()
     dist.destroy_process_group()
 
@@ -83,3 +96,5 @@ def test_two_gloo_ranks_match_single_process(tmp_path, oracle_mod):
     e = si.make_embed_inputs(N=101, V=64, d=64, seed=77)
     dW = dW + oracle_mod.embed_bwd(e["ids"], e["g"], 64)
     assert np.allclose(got["dW"], dW, rtol=0, atol=1e-14)
+    assert list(got["steps"]) == [11, 11]
+    assert list(got["agree"]) == [True, False]
