@@ -362,8 +362,8 @@ def run_ours(args, rank, world, local_rank):
     return line
 
 
-KERNEL_SOURCES = {"fwd": "fwd_kernel.cuh", "fwd_dh": "bwd_kernel.cuh", "bwd_dh": "bwd_kernel.cuh",
-                  "bwd_dW": "bwd_kernel.cuh"}
+KERNEL_SOURCES = {"fwd": ("fwd_kernel.cuh",), "fwd_dh": ("bwd_kernel.cuh", "ce_math.cuh"),
+                  "bwd_dh": ("bwd_kernel.cuh", "ce_math.cuh"), "bwd_dW": ("bwd_kernel.cuh", "ce_math.cuh")}
 
 
 def code_only(src: str) -> str:
@@ -385,7 +385,7 @@ def kernel_sources_sha(kernel: str, read=None) -> str:
             with open(os.path.join(csrc, name)) as fh:
                 return fh.read()
     h = hashlib.sha256()
-    for f in (KERNEL_SOURCES[kernel], "ptx.cuh", "softcap_math.cuh"):
+    for f in (*KERNEL_SOURCES[kernel], "ptx.cuh", "softcap_math.cuh"):
         h.update(code_only(read(f)).encode())
     return h.hexdigest()[:16]
 

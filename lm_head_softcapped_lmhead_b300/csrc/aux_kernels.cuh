@@ -5,6 +5,7 @@
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include "ce_math.cuh"
 #include "ptx.cuh"
 
 namespace lmce {
@@ -60,7 +61,7 @@ __global__ void fwd_finalize_kernel(const float* __restrict__ part, int VT, int 
     } else {
       const float et = st[r];
       const float Sf = static_cast<float>(S);
-      v = log1pf(Sf / et);
+      v = nll_from_sums(Sf, et);
       l = logf(static_cast<float>(S + static_cast<double>(et)));
     }
     const int o = idx ? idx[r] : r;

@@ -47,6 +47,7 @@
 #include <cmath>
 #include <string>
 
+#include "ce_math.cuh"
 #include "ptx.cuh"
 #include "softcap_math.cuh"
 
@@ -81,8 +82,8 @@ constexpr uint32_t SLAB_CHUNK = SLAB_ROWS * KB * 2;  // 8 KB
 constexpr uint32_t P_SLOT = 2 * CHUNK;                // 32 KB: one 128 x 128 bf16 P tile
 constexpr uint32_t Z_TMEM_X = 256;  // Z: the stationary block X in TMEM columns 256-511
 // FD: per-row records of the Z epilogue, [column group][row] x 32 bytes:
-// {double sum of e^s over the non-target columns, float e^{s_t},
-//  1 - tanh_t^2, int target, int flags}.  They go through global memory
+// {float sum of e^s over the non-target columns, unused, float e^{s_t},
+//  1 - tanh_t^2, int target, int flags, 2 x unused}.  They go through global memory
 // (L2): [cluster][column group][row], so the Z CTA's shared memory holds a
 // third P staging copy instead.
 constexpr uint32_t REC_BYTES = 32;
@@ -738,7 +739,10 @@ __global__ void __launch_bounds__(THREADS, 1)
         }
         // FD: this thread's row data and its running sums over the unit.
         int fd_flags = 0;
-        double s_acc = 0.0;
+        // The row's sum of e^s over its non-target columns, compensated in
+        // fp32 (Neumaier: s_hi + s_lo carries about twice fp32's precision);
+        // B300's fp64 pipe is too narrow for an add per chunk and thread.
+        float s_hi = 0.f, s_lo = 0.f;
         FdTarget rec_tg{0.f, 0.f};
         if (MODE == FD) {
           const int row = blk * BM + m;
@@ -821,7 +825,9 @@ __global__ void __launch_bounds__(THREADS, 1)
               cs = g_chunk_fd<true>(r, kc, nl_row, rel, lim, packed, tg);
             else
               cs = g_chunk_fd<false>(r, kc, nl_row, -1, lim, packed, tg);
-            s_acc += static_cast<double>(cs);
+            const float sn = s_hi + cs;
+            s_lo += (fabsf(s_hi) >= fabsf(cs)) ? ((s_hi - sn) + cs) : ((cs - sn) + s_hi);
+            s_hi = sn;
             if (rel >= 0) {
               rec_tg = tg;
               fd_flags |= FL_HIT;
@@ -862,9 +868,7 @@ __global__ void __launch_bounds__(THREADS, 1)
           }
           // Global stores, ordered before the cluster-scope release arrival.
           uint4* rec = p.fd_rec + (static_cast<size_t>(cluster * NREC_GROUPS + cq) * BM + m) * 2;
-          const unsigned long long sb = static_cast<unsigned long long>(__double_as_longlong(s_acc));
-          rec[0] = make_uint4(static_cast<uint32_t>(sb), static_cast<uint32_t>(sb >> 32), __float_as_uint(rec_tg.e),
-                              __float_as_uint(rec_tg.om));
+          rec[0] = make_uint4(__float_as_uint(s_hi + s_lo), 0u, __float_as_uint(rec_tg.e), __float_as_uint(rec_tg.om));
           rec[1] = make_uint4(static_cast<uint32_t>(trow), static_cast<uint32_t>(fd_flags), 0u, 0u);
           mbar_arrive_cluster(peer_rd_full);
           ++fd_units;
@@ -1027,39 +1031,43 @@ __global__ void __launch_bounds__(THREADS, 1)
         if (MODE == FD) {
           if (!mbar_wait<true>(rd_full, rph, abort_flag, p.status)) break;
           rph ^= 1u;
-          double S_other = 0.0;  // the row's sum of e^s over its non-target columns
+          // The row's sum of e^s over its non-target columns (the column
+          // groups' sums added in group order), the target's e^{s_t} and
+          // 1 - tanh_t^2; the scales and the logarithms in fp32 (a few ulp,
+          // and none of B300's slow fp64 arithmetic in front of the drain).
+          float S_other = 0.f;
           int flags = 0;
           uint32_t tsel = 0;
-          double et = 0.0, om = 0.0;
+          float et = 0.f, om = 0.f;
 #pragma unroll
           for (int g = 0; g < NREC_GROUPS; ++g) {
             // After the cluster-scope acquire of rd_full; read at L2.
             const uint4* ra = p.fd_rec + (static_cast<size_t>(cluster * NREC_GROUPS + g) * BM + m) * 2;
             const uint4 a0 = __ldcg(ra), a1 = __ldcg(ra + 1);
-            S_other += __hiloint2double(static_cast<int>(a0.y), static_cast<int>(a0.x));
+            S_other += __uint_as_float(a0.x);
             flags |= static_cast<int>(a1.y);
             tsel = a1.x;
             if (a1.y & FL_HIT) {
-              et = static_cast<double>(__uint_as_float(a0.z));
-              om = static_cast<double>(__uint_as_float(a0.w));
+              et = __uint_as_float(a0.z);
+              om = __uint_as_float(a0.w);
             }
           }
           mbar_arrive_cluster(z_rd_empty);
           const bool tv = (flags & FL_TVALID) != 0;
-          const double S = tv ? S_other + et : S_other;
+          const float S = tv ? S_other + et : S_other;
           if (flags & FL_LIVE) {
-            alpha = static_cast<float>(-static_cast<double>(p.w) / S);
+            alpha = -p.w / S;
             if (tv) {
               // w (p_t - 1)(1 - tanh_t^2), p_t - 1 = -S_other / S (no cancellation).
-              beta = static_cast<float>(-static_cast<double>(p.w) * (S_other / S) * om);
+              beta = -p.w * (S_other / S) * om;
               trow = static_cast<long long>(static_cast<int>(tsel));
             }
           }
           if (part == 0 && row < p.N) {
             float nll = 0.f, lse = 0.f;
             if (flags & FL_LIVE) {
-              lse = static_cast<float>(log(S));
-              nll = tv ? static_cast<float>(log1p(S_other / et)) : __int_as_float(0x7fc00000);
+              lse = logf(S);
+              nll = tv ? nll_from_sums(S_other, et) : __int_as_float(0x7fc00000);
             }
             p.nll[row] = nll;
             if (p.lse_out) p.lse_out[row] = lse;

@@ -40,6 +40,7 @@ def run_fwd(lm, d_inp, softcap, mask=None, want_lse=True):
     (2, 300, 1024, 512, 100.0, 30.0),    # W x 100: cap saturates
     (2, 257, 513, 256, 20.0, 1.0),       # c = 1: mostly the exact-tanh path
     (2, 129, 300, 128, 30.0, 50.0),      # c = 50
+    (2, 300, 1024, 512, 100.0, 70.0),    # W x 100 at c = 70: S_other / e^{s_t} up to 5e58, past fp32
 ])
 def test_fwd_matches_oracle(lm, oracle_mod, cfg, N, V, d, w_scale, c):
     inp = si.make_inputs(cfg, N=N, V=V, d=d, w_scale=w_scale)

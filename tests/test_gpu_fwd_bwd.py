@@ -57,6 +57,8 @@ def check_against_oracle(oracle_mod, inp, c, w, nll, lse, dh, dW, mask=None):
     (2, 130, 100, 128, 1.0, 30.0),     # V below one 128-column tile
     (1, 4096, 1024, 512, 1.0, 30.0),   # tiny-forward config shape
     (2, 300, 700, 256, 1.0, 70.0),     # softcap above 60: forward and dh as two passes
+    (2, 300, 1000, 512, 100.0, 60.0),  # W x 100 at c = 60 (the one-pass form's largest cap):
+                                       # S_other / e^{s_t} up to 4e51, past fp32
 ])
 def test_fwd_bwd_matches_oracle(lm, oracle_mod, cfg, N, V, d, w_scale, c):
     inp = si.make_inputs(cfg, N=N, V=V, d=d, w_scale=w_scale)
