@@ -174,21 +174,42 @@ struct Params {
   int V_pad;
   uint4* fd_rec;        // FD row records [cluster][NREC_GROUPS][BM] x 2 uint4 (global memory)
   unsigned* status;
+  float xlim;           // DH, DW: kTanhXmax, or +inf with no cap (the SFU tanh's range)
 };
 
 // The epilogue forms the NEGATED gradient tile, P = -G (or -G^T), because
-// with nth = -tanh(z/c) both exponent and derivative are one FFMA2 each:
-//   a = cl2e * tanh - lse2 = fma(nth, -cl2e, -lse2),  p = 2^a,
-//   w = tanh^2 - 1 = fma(nth, nth, -1) = -(1 - tanh^2),
+// then exponent and derivative are one FFMA2 each:
+//   a = cl2e * tanh - lse2,  p = 2^a,
+//   w = tanh^2 - 1 = -(1 - tanh^2),
 //   -G = (p - [j == t]) * w.
 // The drain multiplies the accumulator by -grad_scale.
+// DH and DW take tanh(z/c) from the SFU (tanh.approx.f32, relative error
+// about 2^-11): they only form the bf16 gradient tile, where that puts at
+// most c * 2^-11 * 0.3 ~ 5e-3 on s at |z| / c = 0.3 and about 2e-4 at the
+// logits of a 0.02-scale head, comparable to or below the tile's bf16
+// rounding; the FMA pipe, which slows the Z CTA's tensor pipe when busy,
+// then carries 4 instead of 7 packed operations per logit pair (dW pass
+// 0.983 -> 0.944 ms, dh pass 0.936 -> 0.877 ms at N = 65536).  FD keeps the
+// degree-2 polynomial (nth = -tanh: a = fma(nth, -cl2e, 0), w = fma(nth, nth,
+// -1)): its row sums give the forward's nll and lse, whose bits-per-byte sum
+// must hold 1e-5.
 struct EpiConst {
   float2 q[kTanhTerms2];  // -C_i / c^(2i+1): z * Q(z^2) = -tanh(z/c) (degree-2 fit)
   float2 ncl2e;   // -c log2(e)
+  float2 cl2e2;   // c log2(e)
+  float2 invc2;   // 1 / c
   float2 m1;      // -1
   float zlim2;    // (kTanhXmax c)^2
+  float xlim;     // kTanhXmax (|z| / c above it takes the exact slow path)
   float inv_c, cl2e;
 };
+
+// tanh on the SFU (PTX tanh.approx.f32; relative error about 2^-11).
+__device__ __forceinline__ float tanh_sfu(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 b = __floats2bfloat162_rn(lo, hi);
@@ -256,27 +277,27 @@ template <bool kHit>
 __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiConst& k, float lse2, int rel, int lim,
                                            int use_pm1, float pm1, uint32_t (&out)[16]) {
   const float2 nl = make_float2(-lse2, -lse2);
-  float mu = 0.f;  // max z^2 of the chunk (range check of the polynomial)
+  float mu = 0.f;  // max |z| / c of the chunk (range of the fast path)
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-    const float2 u = __fmul2_rn(z, z);
-    mu = fmax3(mu, u.x, u.y);
-    const float2 nth = poly2_z2(z, u, k.q);
-    const float2 a = __ffma2_rn(nth, k.ncl2e, nl);
+    const float2 x = __fmul2_rn(z, k.invc2);
+    mu = fmax3(mu, fabsf(x.x), fabsf(x.y));
+    const float2 th = make_float2(tanh_sfu(x.x), tanh_sfu(x.y));
+    const float2 a = __ffma2_rn(th, k.cl2e2, nl);
     float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
     if (kHit) {
       if (2 * j == rel) pp.x = use_pm1 ? pm1 : pp.x - 1.0f;
       if (2 * j + 1 == rel) pp.y = use_pm1 ? pm1 : pp.y - 1.0f;
     }
-    float2 g = __fmul2_rn(pp, __ffma2_rn(nth, nth, k.m1));
+    float2 g = __fmul2_rn(pp, __ffma2_rn(th, th, k.m1));
     if (lim < 32) {
       g.x = (2 * j < lim) ? g.x : 0.f;
       g.y = (2 * j + 1 < lim) ? g.y : 0.f;
     }
     out[j] = pack_bf16x2(g.x, g.y);
   }
-  if (__any_sync(0xffffffffu, !(mu <= k.zlim2))) {
+  if (__any_sync(0xffffffffu, !(mu <= k.xlim))) {
     Chunk32 c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) c.v[j] = r[j];
@@ -293,15 +314,15 @@ __device__ __forceinline__ void g_chunk_dh(const uint32_t (&r)[32], const EpiCon
 template <bool kHit>
 __device__ __forceinline__ void g_chunk_dw(const uint32_t (&r)[32], const EpiConst& k, float nl_col, int hit_col,
                                            int my_lane, int use_pm1, float pm1_col, uint32_t (&out)[16]) {
-  float mu = 0.f;  // max z^2 of the chunk (range check of the polynomial)
+  float mu = 0.f;  // max |z| / c of the chunk (range of the fast path)
 #pragma unroll
   for (int j = 0; j < 16; ++j) {
     const float2 z = make_float2(__uint_as_float(r[2 * j]), __uint_as_float(r[2 * j + 1]));
-    const float2 u = __fmul2_rn(z, z);
-    mu = fmax3(mu, u.x, u.y);
-    const float2 nth = poly2_z2(z, u, k.q);
+    const float2 x = __fmul2_rn(z, k.invc2);
+    mu = fmax3(mu, fabsf(x.x), fabsf(x.y));
+    const float2 th = make_float2(tanh_sfu(x.x), tanh_sfu(x.y));
     const float2 nl = make_float2(__shfl_sync(0xffffffffu, nl_col, 2 * j), __shfl_sync(0xffffffffu, nl_col, 2 * j + 1));
-    const float2 a = __ffma2_rn(nth, k.ncl2e, nl);
+    const float2 a = __ffma2_rn(th, k.cl2e2, nl);
     float2 pp = make_float2(ex2_approx(a.x), ex2_approx(a.y));
     if (kHit) {
       const float qx = __shfl_sync(0xffffffffu, pm1_col, 2 * j);
@@ -309,10 +330,10 @@ __device__ __forceinline__ void g_chunk_dw(const uint32_t (&r)[32], const EpiCon
       if (__shfl_sync(0xffffffffu, hit_col, 2 * j) == my_lane) pp.x = use_pm1 ? qx : pp.x - 1.0f;
       if (__shfl_sync(0xffffffffu, hit_col, 2 * j + 1) == my_lane) pp.y = use_pm1 ? qy : pp.y - 1.0f;
     }
-    const float2 g = __fmul2_rn(pp, __ffma2_rn(nth, nth, k.m1));
+    const float2 g = __fmul2_rn(pp, __ffma2_rn(th, th, k.m1));
     out[j] = pack_bf16x2(g.x, g.y);
   }
-  if (__any_sync(0xffffffffu, !(mu <= k.zlim2))) {
+  if (__any_sync(0xffffffffu, !(mu <= k.xlim))) {
     Chunk32 c;
 #pragma unroll
     for (int j = 0; j < 32; ++j) c.v[j] = r[j];
@@ -702,6 +723,11 @@ __global__ void __launch_bounds__(THREADS, 1)
       kc.ncl2e = make_float2(-p.cl2e, -p.cl2e);
       kc.m1 = make_float2(-1.0f, -1.0f);
       kc.zlim2 = p.zlim2;
+      if (MODE != FD) {
+        kc.cl2e2 = make_float2(p.cl2e, p.cl2e);
+        kc.invc2 = make_float2(p.inv_c, p.inv_c);
+        kc.xlim = p.xlim;
+      }
       kc.inv_c = p.inv_c;
       kc.cl2e = p.cl2e;
       const float kNegInf = __int_as_float(0xff800000);
@@ -1319,6 +1345,7 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
     p.inv_c = 1.0f / c;
     p.cl2e = c * kLog2e;
     p.zlim2 = (kTanhXmax * c) * (kTanhXmax * c);
+    p.xlim = kTanhXmax;
     scaled_tanh2_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
   } else {
     // No cap (softcap 0): the epilogue runs with c = 1e30, where in fp32
@@ -1329,6 +1356,7 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
     p.inv_c = 1.0f / ce;
     p.cl2e = ce * kLog2e;
     p.zlim2 = HUGE_VALF;
+    p.xlim = HUGE_VALF;
     p.q[0] = -p.inv_c;
     for (int i = 1; i < kTanhTerms2; ++i) p.q[i] = 0.0f;
   }
@@ -1395,6 +1423,7 @@ inline int launch_fd(const uint16_t* h, long long ldh, const uint16_t* W, long l
   p.cl2e = c * kLog2e;
   p.w = grad_scale;
   p.zlim2 = (kTanhXmax * c) * (kTanhXmax * c);
+  p.xlim = kTanhXmax;
   scaled_tanh2_coeffs(-1.0, 1.0 / static_cast<double>(c), p.q);
   p.status = status;
   p.W = reinterpret_cast<const __nv_bfloat16*>(W);

@@ -21,7 +21,7 @@ constexpr float kTanhC1 = -0.33332961797714233f;
 constexpr float kTanhC2 = 0.13312597572803497f;
 constexpr float kTanhC3 = -0.05022243782877922f;
 
-// The backward epilogues use a degree-2 fit on the same range (fit_tanh.py,
+// The forward + dh pass's epilogue uses a degree-2 fit on the same range (fit_tanh.py,
 // DEG = 2: worst relative error 1.2e-6 in exact arithmetic, 1.3e-6 in fp32):
 // there s = c tanh(z/c) only enters p = e^{s - lse} and 1 - tanh^2, and an
 // error of at most c * 1.3e-6 * 0.3 ~ 1e-5 in s is far below the bf16
