@@ -21,16 +21,6 @@ constexpr float kTanhC1 = -0.33332961797714233f;
 constexpr float kTanhC2 = 0.13312597572803497f;
 constexpr float kTanhC3 = -0.05022243782877922f;
 
-// The forward + dh pass's epilogue uses a degree-2 fit on the same range (fit_tanh.py,
-// DEG = 2: worst relative error 1.2e-6 in exact arithmetic, 1.3e-6 in fp32):
-// there s = c tanh(z/c) only enters p = e^{s - lse} and 1 - tanh^2, and an
-// error of at most c * 1.3e-6 * 0.3 ~ 1e-5 in s is far below the bf16
-// rounding of the gradient tile.  It saves one FFMA2 per logit pair.
-constexpr int kTanhTerms2 = 3;
-constexpr float kTanh2C0 = 0.9999988675117493f;
-constexpr float kTanh2C1 = -0.33310022950172424f;
-constexpr float kTanh2C2 = 0.12633946537971497f;
-
 __device__ __forceinline__ float tanh_poly(float x) {
   const float u = x * x;
   float p = fmaf(kTanhC3, u, kTanhC2);
@@ -50,13 +40,6 @@ __device__ __forceinline__ float2 poly_z2(float2 z, float2 u, const float2 (&k)[
   return __fmul2_rn(z, p);
 }
 
-// Degree-2 form of poly_z2: z * (k0 + k1 u + k2 u^2).
-__device__ __forceinline__ float2 poly2_z2(float2 z, float2 u, const float2 (&k)[kTanhTerms2]) {
-  float2 p = __ffma2_rn(k[2], u, k[1]);
-  p = __ffma2_rn(p, u, k[0]);
-  return __fmul2_rn(z, p);
-}
-
 // Coefficients k_i = scale * C_i * inv_c^(2i+1) (host side, in double).
 inline void scaled_tanh_coeffs(double scale, double inv_c, float (&k)[kTanhTerms]) {
   const double C[kTanhTerms] = {kTanhC0, kTanhC1, kTanhC2, kTanhC3};
@@ -66,13 +49,20 @@ inline void scaled_tanh_coeffs(double scale, double inv_c, float (&k)[kTanhTerms
     f *= inv_c * inv_c;
   }
 }
-inline void scaled_tanh2_coeffs(double scale, double inv_c, float (&k)[kTanhTerms2]) {
-  const double C[kTanhTerms2] = {kTanh2C0, kTanh2C1, kTanh2C2};
-  double f = inv_c;
-  for (int i = 0; i < kTanhTerms2; ++i) {
-    k[i] = static_cast<float>(scale * C[i] * f);
-    f *= inv_c * inv_c;
-  }
+
+// tanh on the SFU (PTX tanh.approx.f32).  Its specified relative error is
+// about 2^-11; over |x| <= kTanhXmax it measured at most 9.9e-6 (every float
+// in [1e-6, 0.3] on a B300, mean signed error at most 2.2e-6 in any decade
+// of x), against 1.1e-7 for tanh_poly.  The backward epilogues use it there,
+// with tanh_any for chunks beyond: it keeps their arithmetic off the FMA
+// pipe, whose load slows the tensor pipe of the same SM.  The forward
+// keeps tanh_poly: with 8 epilogue warps for a 128 x 256 tile per CTA, the
+// second SFU operation per logit made it SFU-bound (0.393 -> 0.435 ms at
+// N = 65536).
+__device__ __forceinline__ float tanh_sfu(float x) {
+  float y;
+  asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 // max(a, b, c) in one instruction (sm_100 three-input max).
