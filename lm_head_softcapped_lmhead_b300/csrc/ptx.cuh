@@ -43,12 +43,18 @@ __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
 }
+// try_wait with a suspend-time hint: a thread whose phase is not complete
+// sleeps in hardware until the phase completes or kWaitSuspendNs pass,
+// instead of returning at once.  Waiting warps then issue almost nothing:
+// polling loops (counters, compares, branches; integer adds go partly to the
+// FMA pipe) running beside the tensor core's MMAs slow them down.
+constexpr uint32_t kWaitSuspendNs = 100000;  // 100 us
 __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(addr), "r"(parity)
+      : "r"(addr), "r"(parity), "r"(kWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
@@ -56,19 +62,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t addr, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, "
+      "1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(addr), "r"(parity)
+      : "r"(addr), "r"(parity), "r"(kWaitSuspendNs)
       : "memory");
   return ok != 0;
 }
 
 // Bounded wait for the phase with parity `parity` of `bar`.  Returns false
 // (after raising the CTA's abort flag and the global status) if the wait
-// exceeds about kWaitLimitNs or another role of the CTA has already aborted.
-// The limit is counted in SM clock cycles (clock64 is cheap; %globaltimer is
-// not) and only checked every 1024 polls, so a healthy wait costs nothing
-// beyond its try_wait polls.
+// exceeds about limit_cycles SM clock cycles or another role of the CTA has
+// already aborted.  Each poll sleeps up to kWaitSuspendNs; the abort flag
+// and the clock (clock64 is cheap; %globaltimer is not) are checked every
+// 8 polls.
 constexpr long long kWaitLimitCycles = 4000000000ll;  // ~2 s at 2 GHz
 template <bool kClusterAcquire = false>
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag,
@@ -77,7 +84,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   long long t0 = 0;
   for (uint32_t it = 0;; ++it) {
     if (kClusterAcquire ? mbar_try_wait_cluster(a, parity) : mbar_try_wait(a, parity)) return true;
-    if ((it & 1023u) == 1023u) {
+    if ((it & 7u) == 7u) {
       if (*abort_flag) return false;
       const long long now = clock64();
       if (t0 == 0) {
