@@ -431,6 +431,15 @@ __device__ __forceinline__ int rot_tile(int t0, int n, int i, int rot) {
   return t0 + j;
 }
 
+// DW row-split partials, in the layout the drain writes: float4 index of
+// [split s][vocab block blk][32-column chunk ch][lane quarter q][float4 v of
+// the chunk][lane]: rows blk*128 + 32q + lane, columns 32ch + 4v .. +3.
+// Each of a drain warp's stores then covers 512 contiguous bytes.
+__host__ __device__ __forceinline__ long long dw_part_index(int s, int blk, int ch, int q, int v, int lane,
+                                                           int n_blocks, int nch) {
+  return ((((static_cast<long long>(s) * n_blocks + blk) * nch + ch) * 4 + q) * 8 + v) * 32 + lane;
+}
+
 // Split-major order: clusters running at the same time share a row range
 // of the streamed operand, which then stays in L2.
 __device__ __forceinline__ void unit_range(const Params& p, int u, int& blk, int& t0, int& t1) {
@@ -1151,13 +1160,14 @@ __global__ void __launch_bounds__(THREADS, 1)
                   dst[v] = a;
                 }
               } else {
+                // The partial in the drain's own layout (dw_part_index): each
+                // store instruction writes 512 contiguous bytes.
                 const int s = u / p.n_blocks;
-                float4* dst = reinterpret_cast<float4*>(
-                    p.dw_part + (static_cast<long long>(s) * p.V_pad + row) * p.d + col);
+                float4* dst = reinterpret_cast<float4*>(p.dw_part) + dw_part_index(s, blk, ch, q, 0, lane, p.n_blocks, nch);
 #pragma unroll
                 for (int v = 0; v < 8; ++v)
-                  dst[v] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
-                                       __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
+                  dst[v * 32] = make_float4(__uint_as_float(r[4 * v]), __uint_as_float(r[4 * v + 1]),
+                                            __uint_as_float(r[4 * v + 2]), __uint_as_float(r[4 * v + 3]));
               }
             }
           }
@@ -1180,28 +1190,52 @@ __global__ void __launch_bounds__(THREADS, 1)
   }
 }
 
-// dW = (accumulate ? dW : 0) + w * sum_{s < split} part[s], in split order.
-__global__ void dw_split_reduce_kernel(const float4* __restrict__ part, int split, long long V_pad_d4, long long n4,
-                                       float w, int accumulate, float4* __restrict__ dW) {
-  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < n4;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    float4 s = part[e];
-    for (int k = 1; k < split; ++k) {
-      const float4 v = part[static_cast<long long>(k) * V_pad_d4 + e];
-      s.x += v.x;
-      s.y += v.y;
-      s.z += v.z;
-      s.w += v.w;
+// dW = (accumulate ? dW : 0) + w * sum_{s < split} part[s], in split order,
+// from the drain's partial layout (dw_part_index).  One thread per (block,
+// chunk, quarter, lane): it reads each float4 plane of the splits (coalesced
+// across the lanes) and writes its row's 32 columns of the chunk.
+__global__ void dw_split_reduce_kernel(const float4* __restrict__ part, int split, int n_blocks, int nch, int V,
+                                       int d, float w, int accumulate, float* __restrict__ dW) {
+  const long long n = static_cast<long long>(n_blocks) * nch * 4 * 32;
+  const long long sstride = static_cast<long long>(n_blocks) * nch * 4 * 256;
+  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
+       t += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int lane = static_cast<int>(t & 31);
+    const long long g = t >> 5;  // (blk, ch, q)
+    const int q = static_cast<int>(g & 3);
+    const long long bc = g >> 2;
+    const int ch = static_cast<int>(bc % nch);
+    const int blk = static_cast<int>(bc / nch);
+    const int row = blk * BM + q * 32 + lane;
+    if (row >= V) continue;
+    const float4* src = part + g * 256 + lane;
+    float4* dst = reinterpret_cast<float4*>(dW + static_cast<long long>(row) * d + ch * 32);
+#pragma unroll 2
+    for (int v = 0; v < 8; ++v) {
+      float4 b[MAX_SPLIT];
+#pragma unroll
+      for (int k = 0; k < MAX_SPLIT; ++k)
+        if (k < split) b[k] = src[k * sstride + v * 32];
+      float4 s = b[0];
+#pragma unroll
+      for (int k = 1; k < MAX_SPLIT; ++k) {
+        if (k < split) {
+          s.x += b[k].x;
+          s.y += b[k].y;
+          s.z += b[k].z;
+          s.w += b[k].w;
+        }
+      }
+      float4 o = make_float4(w * s.x, w * s.y, w * s.z, w * s.w);
+      if (accumulate) {
+        const float4 a = dst[v];
+        o.x += a.x;
+        o.y += a.y;
+        o.z += a.z;
+        o.w += a.w;
+      }
+      dst[v] = o;
     }
-    float4 o = make_float4(w * s.x, w * s.y, w * s.z, w * s.w);
-    if (accumulate) {
-      const float4 b = dW[e];
-      o.x += b.x;
-      o.y += b.y;
-      o.z += b.z;
-      o.w += b.w;
-    }
-    dW[e] = o;
   }
 }
 
@@ -1365,12 +1399,12 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
     const int cl = static_cast<int>(q.n_units < clusters_max ? q.n_units : clusters_max);
     if (int rc = launch_mode<DW>(tm_wx, tm_hy, tm_hs, q, cl, s); rc) return rc;
     if (q.split > 1) {
-      const long long n4 = V * d / 4;
-      const int blocks = static_cast<int>(cdivll(n4, 256) < sms * 8 ? cdivll(n4, 256) : sms * 8);
+      const long long nt = static_cast<long long>(q.n_blocks) * (d / 32) * 4 * 32;
+      const int blocks = static_cast<int>(cdivll(nt, 256) < sms * 8 ? cdivll(nt, 256) : sms * 8);
       count_launches(1);
-      dw_split_reduce_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(scratch), q.split,
-                                                    static_cast<long long>(q.V_pad) * d / 4, n4, p.w, accumulate,
-                                                    reinterpret_cast<float4*>(dW));
+      dw_split_reduce_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(scratch), q.split, q.n_blocks,
+                                                    static_cast<int>(d / 32), static_cast<int>(V), static_cast<int>(d),
+                                                    p.w, accumulate, dW);
       cudaError_t e = cudaGetLastError();
       if (e != cudaSuccess) {
         set_last_error(std::string("dw_split_reduce launch: ") + cudaGetErrorString(e));
