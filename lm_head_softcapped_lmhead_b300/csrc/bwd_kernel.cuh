@@ -1191,51 +1191,54 @@ __global__ void __launch_bounds__(THREADS, 1)
 }
 
 // dW = (accumulate ? dW : 0) + w * sum_{s < split} part[s], in split order,
-// from the drain's partial layout (dw_part_index).  One thread per (block,
-// chunk, quarter, lane): it reads each float4 plane of the splits (coalesced
-// across the lanes) and writes its row's 32 columns of the chunk.
-__global__ void dw_split_reduce_kernel(const float4* __restrict__ part, int split, int n_blocks, int nch, int V,
-                                       int d, float w, int accumulate, float* __restrict__ dW) {
-  const long long n = static_cast<long long>(n_blocks) * nch * 4 * 32;
+// from the drain's partial layout (dw_part_index).  One block per (vocab
+// block, 32-column chunk): its 256 threads add the splits' float4 planes
+// (reads coalesced across the lanes) into a shared-memory tile, then write
+// the chunk's 128 rows x 128 bytes of dW (8 threads per row: coalesced).
+__global__ void __launch_bounds__(256) dw_split_reduce_kernel(const float4* __restrict__ part, int split, int n_blocks,
+                                                              int nch, int V, int d, float w, int accumulate,
+                                                              float* __restrict__ dW) {
+  __shared__ float4 tile[4 * 8][33];  // [q * 8 + v][lane], padded against bank conflicts
+  const int blk = blockIdx.x / nch;
+  const int ch = blockIdx.x - blk * nch;
   const long long sstride = static_cast<long long>(n_blocks) * nch * 4 * 256;
-  for (long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; t < n;
-       t += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int lane = static_cast<int>(t & 31);
-    const long long g = t >> 5;  // (blk, ch, q)
-    const int q = static_cast<int>(g & 3);
-    const long long bc = g >> 2;
-    const int ch = static_cast<int>(bc % nch);
-    const int blk = static_cast<int>(bc / nch);
-    const int row = blk * BM + q * 32 + lane;
-    if (row >= V) continue;
-    const float4* src = part + g * 256 + lane;
-    float4* dst = reinterpret_cast<float4*>(dW + static_cast<long long>(row) * d + ch * 32);
-#pragma unroll 2
-    for (int v = 0; v < 8; ++v) {
-      float4 b[MAX_SPLIT];
+  const float4* src = part + dw_part_index(0, blk, ch, 0, 0, 0, n_blocks, nch);
 #pragma unroll
-      for (int k = 0; k < MAX_SPLIT; ++k)
-        if (k < split) b[k] = src[k * sstride + v * 32];
-      float4 s = b[0];
+  for (int it = 0; it < 4; ++it) {
+    const int e = it * 256 + threadIdx.x;  // (q, v, lane) of the chunk's 1024 float4
+    float4 b[MAX_SPLIT];
 #pragma unroll
-      for (int k = 1; k < MAX_SPLIT; ++k) {
-        if (k < split) {
-          s.x += b[k].x;
-          s.y += b[k].y;
-          s.z += b[k].z;
-          s.w += b[k].w;
-        }
+    for (int k = 0; k < MAX_SPLIT; ++k)
+      if (k < split) b[k] = src[k * sstride + e];
+    float4 s = b[0];
+#pragma unroll
+    for (int k = 1; k < MAX_SPLIT; ++k) {
+      if (k < split) {
+        s.x += b[k].x;
+        s.y += b[k].y;
+        s.z += b[k].z;
+        s.w += b[k].w;
       }
-      float4 o = make_float4(w * s.x, w * s.y, w * s.z, w * s.w);
-      if (accumulate) {
-        const float4 a = dst[v];
-        o.x += a.x;
-        o.y += a.y;
-        o.z += a.z;
-        o.w += a.w;
-      }
-      dst[v] = o;
     }
+    tile[e >> 5][e & 31] = make_float4(w * s.x, w * s.y, w * s.z, w * s.w);
+  }
+  __syncthreads();
+#pragma unroll
+  for (int it = 0; it < 4; ++it) {
+    const int e = it * 256 + threadIdx.x;
+    const int r = e >> 3, v = e & 7;  // row of the block, float4 of the chunk
+    const int row = blk * BM + r;
+    if (row >= V) continue;
+    float4 o = tile[(r >> 5) * 8 + v][r & 31];
+    float4* dst = reinterpret_cast<float4*>(dW + static_cast<long long>(row) * d + ch * 32) + v;
+    if (accumulate) {
+      const float4 a = *dst;
+      o.x += a.x;
+      o.y += a.y;
+      o.z += a.z;
+      o.w += a.w;
+    }
+    *dst = o;
   }
 }
 
@@ -1399,8 +1402,7 @@ inline int launch(const uint16_t* h, long long ldh, const uint16_t* W, long long
     const int cl = static_cast<int>(q.n_units < clusters_max ? q.n_units : clusters_max);
     if (int rc = launch_mode<DW>(tm_wx, tm_hy, tm_hs, q, cl, s); rc) return rc;
     if (q.split > 1) {
-      const long long nt = static_cast<long long>(q.n_blocks) * (d / 32) * 4 * 32;
-      const int blocks = static_cast<int>(cdivll(nt, 256) < sms * 8 ? cdivll(nt, 256) : sms * 8);
+      const int blocks = q.n_blocks * static_cast<int>(d / 32);
       count_launches(1);
       dw_split_reduce_kernel<<<blocks, 256, 0, s>>>(reinterpret_cast<const float4*>(scratch), q.split, q.n_blocks,
                                                     static_cast<int>(d / 32), static_cast<int>(V), static_cast<int>(d),
