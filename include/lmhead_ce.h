@@ -249,9 +249,10 @@ LMCE_API int lmhead_ce_fwd_bwd_int4(const lmce_bf16* h, int64_t ldh, const uint8
  * Inputs: ids [N] int64 (the input tokens), g [N, d] bf16 with row stride
  * ldg elements (ldg % 8 == 0, 16-byte aligned).  dW [V, d] fp32 is added to.
  * Deterministic: each token's rows are summed in row order in fp32 (in
- * pieces of at most 64 rows, added in order), then added to dW once.  A row
- * whose id is outside [0, V) is skipped and sets LMCE_EDATA in the status
- * word.  Needs a workspace sized with LMCE_WS_EMBED; d as for the head
+ * pieces of at most 32 rows, then groups of 16 pieces, each added in order),
+ * then added to dW once, by an atomic add that flushes a subnormal operand or
+ * result (below 2^-126 in magnitude) to zero.  A row whose id is outside
+ * [0, V) is skipped and sets LMCE_EDATA in the status word.  Needs a workspace sized with LMCE_WS_EMBED; d as for the head
  * (a multiple of 64, at most 512). */
 LMCE_API int lmhead_tied_embed_bwd(const int64_t* ids, const lmce_bf16* g, int64_t ldg, int64_t N, int64_t V,
                           int64_t d, float* dW, void* ws, size_t ws_bytes, void* stream);

@@ -14,18 +14,20 @@
 // groups of kGroupPieces consecutive pieces (in piece order), then the groups
 // in order -- and the total is added into dW once.  A stable counting sort
 // puts every token's rows together in row order first.
-//   1. count:   per row chunk (chunk_rows(N) rows) and token, the rows (integer
-//               atomics; chunk-major hist[c][v]);
+//   1. count:   per row chunk (chunk_rows(N) rows) and token, the rows
+//               (chunk-major hist[c][v]), and each row's rank among the
+//               chunk's rows with its id (warps walk the chunk's rows in
+//               order; lanes with equal ids take consecutive ranks in lane
+//               order);
 //   2. tokscan: per token (one thread), the exclusive prefix of its counts
 //               over the chunks (in place), its rows, pieces and groups, and
 //               their exclusive scans over all tokens in one pass (256-token
 //               blocks taken in ticket order publish their totals and add
 //               their predecessors': decoupled look-back); each piece's
 //               token recorded, the arrival counters zeroed;
-//   3. place:   per chunk, the cursors of the chunk's tokens are staged in
-//               shared memory, then one warp walks the chunk's rows in order;
-//               lanes holding the same token take consecutive slots in lane
-//               order (stable);
+//   3. place:   per row (one thread), its slot: the token's first position,
+//               plus its rows in earlier chunks, plus the row's rank in its
+//               chunk (stable);
 //   4. pieces:  one warp per piece sums its rows (bf16 -> fp32) in row
 //               order; a token with one piece adds it into dW.  Otherwise the
 //               warp that completes the last piece of a group (an arrival
@@ -34,6 +36,11 @@
 //               and adds the total into dW (a token with one group adds the
 //               group's sum).  Which warp does a sum varies; its order does
 //               not.
+// The additions into dW are vector atomic adds (red.global.add.v4.f32) that
+// need no read round trip.  Each dW element receives exactly one of them per
+// call, so the result is that of a load, add and store, except that the
+// atomic flushes a subnormal (below 2^-126 in magnitude) operand or result
+// to zero.
 // Rows whose id is outside [0, V) raise ST_EDATA and are skipped.
 #pragma once
 #include <cstdint>
@@ -46,7 +53,9 @@ namespace embk {
 constexpr int kPieceRows = 32;     // rows summed by one warp
 constexpr int kGroupPieces = 16;   // pieces summed by one warp
 constexpr int kMaxChunks = 256;    // row chunks of the counting sort
-constexpr int kPlaceSmemV = 32768; // largest V whose chunk cursors the place kernel keeps in shared memory
+constexpr int kCountSmemV = 32768; // largest V whose chunk counts the count kernel keeps in shared memory
+constexpr int kWalkers = 8;         // warps of count8_kernel walking one 1024-row chunk together
+constexpr int kWalkersMaxV = 12288; // largest V whose kWalkers x V 16-bit counts fit in 192 KB of shared memory
 
 // Rows per chunk of the counting sort for N rows (a multiple of 32).
 inline long long chunk_rows(long long N) {
@@ -65,7 +74,7 @@ inline long long max_pieces(long long N, long long V) {
 inline long long max_groups(long long N) { return N / 16 + 64; }
 
 struct Layout {
-  size_t hist, offs, pbase, gbase, perm, part, gpart, pcnt, gcnt, powner, lb, total;
+  size_t hist, lrank, offs, pbase, gbase, perm, part, gpart, pcnt, gcnt, powner, lb, total;
 };
 // Look-back records of the token scan: per 256-token block 8 ints {flag,
 // 3 block totals, 3 inclusive prefixes, unused}, then the block ticket.
@@ -76,6 +85,8 @@ inline Layout layout(long long N, long long V, long long d) {
   size_t o = 0;
   L.hist = o;   // [chunks][V] int: counts, then within-token prefixes (cursors)
   o = up256(o + sizeof(int) * static_cast<size_t>(n_chunks(N)) * static_cast<size_t>(V));
+  L.lrank = o;  // [N] int: rank of each row among its chunk's rows with the same id
+  o = up256(o + sizeof(int) * static_cast<size_t>(N));
   L.offs = o;   // [V + 1] int: first sorted position of each token
   o = up256(o + sizeof(int) * static_cast<size_t>(V + 1));
   L.pbase = o;  // [V + 1] int: first piece of each token
@@ -107,15 +118,87 @@ __device__ __forceinline__ bool id_ok(long long v, int V) { return v >= 0 && v <
 // waits here (griddepcontrol.wait) until the previous kernel has completed
 // and its memory operations are visible before reading what it wrote.
 __device__ __forceinline__ void wait_prior_grid() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// The first three kernels let the next one launch its blocks at once
+// (griddepcontrol.launch_dependents), so that they are resident and waiting
+// in wait_prior_grid when this grid completes.
+__device__ __forceinline__ void allow_next_grid() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// 1. hist[c][v] = rows of chunk c with id v.  With use_smem (V <=
-//    kPlaceSmemV; dynamic shared memory of V ints) block c counts in shared
-//    memory and writes its row out whole; otherwise it zeroes its row and
-//    counts with global atomics.  Also zeroes the token scan's look-back
-//    records.
+__device__ __forceinline__ int ld_shared_s32(const int* p) {
+  int x;
+  asm volatile("ld.shared.s32 %0, [%1];" : "=r"(x) : "r"(smem_u32(p)) : "memory");
+  return x;
+}
+__device__ __forceinline__ void st_shared_s32(int* p, int x) {
+  asm volatile("st.shared.s32 [%0], %1;" ::"r"(smem_u32(p)), "r"(x) : "memory");
+}
+
+// Warp-wide walk over rows i0 .. i1 - 1 of a chunk, in order, 32 at a time:
+// lanes with equal ids (__match_any_sync) take consecutive ranks in lane order
+// after the id's count so far, and the group's lowest lane advances the count
+// in cnt (shared memory when kShared, so no access of the walk waits on a
+// global store; the chunk's hist row otherwise).  The ranks are kept in
+// registers and stored to lrank after each 1024 rows.
+template <bool kShared>
+__device__ __forceinline__ void rank_walk(const int64_t* __restrict__ ids, int i0, int i1, int V, int* cnt,
+                                          int* __restrict__ lrank, unsigned* status, int lane) {
+  constexpr int kSteps = 32;
+  for (int b0 = i0; b0 < i1; b0 += 32 * kSteps) {
+    // The chunk's ids are loaded ahead: lane l holds row b0 + 32 st + l of
+    // step st (-1 for rows that do not count).
+    // The status update comes after all the loads: an atomic between them
+    // made each load wait for the one before it.
+    int tok[kSteps], rk[kSteps];
+    bool bad = false;
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st) {
+      const int i = b0 + 32 * st + lane;
+      const long long v = i < i1 ? ids[i] : 0;
+      bad |= i < i1 && !id_ok(v, V);
+      tok[st] = i < i1 && id_ok(v, V) ? static_cast<int>(v) : -1;
+    }
+    if (bad) atomicOr(status, ST_EDATA);
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st) {
+      const int v = tok[st];
+      const bool ok = v >= 0;
+      const unsigned active = __ballot_sync(0xffffffffu, ok);
+      const unsigned peers = __match_any_sync(0xffffffffu, v) & active;
+      const unsigned below = peers & ((1u << lane) - 1u);
+      int base = 0;
+      if (ok) {
+        if constexpr (kShared)
+          base = ld_shared_s32(cnt + v);
+        else
+          base = cnt[v];
+      }
+      rk[st] = base + __popc(below);
+      __syncwarp();
+      if (ok && below == 0u) {
+        if constexpr (kShared)
+          st_shared_s32(cnt + v, base + __popc(peers));
+        else
+          cnt[v] = base + __popc(peers);
+      }
+      __syncwarp();
+    }
+#pragma unroll
+    for (int st = 0; st < kSteps; ++st)
+      if (tok[st] >= 0) lrank[b0 + 32 * st + lane] = rk[st];
+  }
+}
+
+// 1. hist[c][v] = rows of chunk c with id v, and lrank[i] = the rank of row
+//    i among the chunk's rows with the same id (the number of earlier rows
+//    of the chunk with that id), by one warp's walk (rank_walk).  With
+//    use_smem (V <= kCountSmemV; dynamic shared memory of V ints) the counts
+//    live in shared memory and the block writes its row out whole;
+//    otherwise they live in the block's hist row.  Also zeroes the token
+//    scan's look-back records.
 __global__ void count_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int* __restrict__ hist,
-                             unsigned* status, int use_smem, int* __restrict__ lb, int lb_n) {
+                             int* __restrict__ lrank, unsigned* status, int use_smem, int* __restrict__ lb,
+                             int lb_n) {
   extern __shared__ int s_hist[];
+  allow_next_grid();
   // The token scan's look-back records and ticket start at zero.
   for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < lb_n; k += gridDim.x * blockDim.x) lb[k] = 0;
   const int c = blockIdx.x;
@@ -124,45 +207,113 @@ __global__ void count_kernel(const int64_t* __restrict__ ids, int N, int V, int 
   int* cnt = use_smem ? s_hist : h;
   for (int v = threadIdx.x; v < V; v += blockDim.x) cnt[v] = 0;
   __syncthreads();
-  for (int i = i0 + threadIdx.x; i < i1; i += blockDim.x) {
-    const long long v = ids[i];
-    if (!id_ok(v, V)) {
-      atomicOr(status, ST_EDATA);
-      continue;
-    }
-    atomicAdd(cnt + v, 1);
+  if (threadIdx.x < 32) {
+    if (use_smem)
+      rank_walk<true>(ids, i0, i1, V, s_hist, lrank, status, threadIdx.x);
+    else
+      rank_walk<false>(ids, i0, i1, V, h, lrank, status, threadIdx.x);
   }
   if (!use_smem) return;
   __syncthreads();
   for (int v = threadIdx.x; v < V; v += blockDim.x) h[v] = s_hist[v];
 }
 
-// Block-wide exclusive scan (blockDim.x == 256) of one value per thread;
-// returns the thread's prefix, *total the block's sum.
-__device__ __forceinline__ int block_scan_256(int x, int* s_warp, int* total) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int inc = x;
+// 1b. count_kernel's results for 1024-row chunks and V <= kWalkersMaxV, with
+//     the walk split over the block's 8 warps: warp w walks rows 128 w ..
+//     128 w + 127 of the chunk (as rank_walk) with 16-bit counts of its own
+//     (dynamic shared memory, [kWalkers][V]).  A row's rank is its rank among
+//     its warp's rows with the same id plus that id's counts in the warps
+//     before; the chunk's count of an id is the sum over the warps.
+__global__ void __launch_bounds__(256) count8_kernel(const int64_t* __restrict__ ids, int N, int V,
+                                                     int* __restrict__ hist, int* __restrict__ lrank,
+                                                     unsigned* status, int* __restrict__ lb, int lb_n) {
+  extern __shared__ __align__(16) uint16_t s_cnt[];
+  allow_next_grid();
+  // The token scan's look-back records and ticket start at zero.
+  for (int k = blockIdx.x * blockDim.x + threadIdx.x; k < lb_n; k += gridDim.x * blockDim.x) lb[k] = 0;
+  const int c = blockIdx.x;
+  const int i0 = c * 1024, i1 = min(N, i0 + 1024);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint32_t* s_words = reinterpret_cast<uint32_t*>(s_cnt);
+  for (int k = threadIdx.x; k < kWalkers * V / 2; k += blockDim.x) s_words[k] = 0u;
+  constexpr int kSteps = 1024 / (32 * kWalkers);
+  int tok[kSteps], rk[kSteps];
+  bool bad = false;
 #pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, inc, o);
-    if (lane >= o) inc += y;
+  for (int st = 0; st < kSteps; ++st) {
+    const int i = i0 + 32 * (kSteps * warp + st) + lane;
+    const long long v = i < i1 ? ids[i] : 0;
+    bad |= i < i1 && !id_ok(v, V);
+    tok[st] = i < i1 && id_ok(v, V) ? static_cast<int>(v) : -1;
   }
-  if (lane == 31) s_warp[warp] = inc;
+  if (bad) atomicOr(status, ST_EDATA);
+  __syncthreads();
+  uint16_t* mine = s_cnt + static_cast<size_t>(warp) * V;
+#pragma unroll
+  for (int st = 0; st < kSteps; ++st) {
+    const int v = tok[st];
+    const bool ok = v >= 0;
+    const unsigned active = __ballot_sync(0xffffffffu, ok);
+    const unsigned peers = __match_any_sync(0xffffffffu, v) & active;
+    const unsigned below = peers & ((1u << lane) - 1u);
+    const int base = ok ? static_cast<int>(mine[v]) : 0;
+    rk[st] = base + __popc(below);
+    __syncwarp();
+    if (ok && below == 0u) mine[v] = static_cast<uint16_t>(base + __popc(peers));
+    __syncwarp();
+  }
+  __syncthreads();
+#pragma unroll
+  for (int st = 0; st < kSteps; ++st) {
+    const int v = tok[st];
+    if (v < 0) continue;
+    int b = rk[st];
+    for (int w2 = 0; w2 < warp; ++w2) b += s_cnt[static_cast<size_t>(w2) * V + v];
+    lrank[i0 + 32 * (kSteps * warp + st) + lane] = b;
+  }
+  int* h = hist + static_cast<size_t>(c) * V;
+  for (int v = threadIdx.x; v < V; v += blockDim.x) {
+    int sum = 0;
+#pragma unroll
+    for (int w2 = 0; w2 < kWalkers; ++w2) sum += s_cnt[static_cast<size_t>(w2) * V + v];
+    h[v] = sum;
+  }
+}
+
+// Block-wide exclusive scans (blockDim.x == 256) of three values per thread
+// at once: x[k] <- the thread's prefix of value k, total[k] <- the block's sum.
+__device__ __forceinline__ void block_scan3_256(int (&x)[3], int* s_warp, int (&total)[3]) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  int inc[3];
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    inc[k] = x[k];
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, inc[k], o);
+      if (lane >= o) inc[k] += y;
+    }
+    if (lane == 31) s_warp[8 * k + warp] = inc[k];
+  }
   __syncthreads();
   if (warp == 0) {
-    int w = lane < 8 ? s_warp[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 8; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, w, o);
-      if (lane >= o) w += y;
+    for (int k = 0; k < 3; ++k) {
+      int w = lane < 8 ? s_warp[8 * k + lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 8; o <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, w, o);
+        if (lane >= o) w += y;
+      }
+      if (lane < 8) s_warp[8 * k + lane] = w;  // inclusive over the warps
     }
-    if (lane < 8) s_warp[lane] = w;  // inclusive over the warps
   }
   __syncthreads();
-  const int before = (warp > 0 ? s_warp[warp - 1] : 0) + inc - x;
-  *total = s_warp[7];
-  __syncthreads();
-  return before;
+#pragma unroll
+  for (int k = 0; k < 3; ++k) {
+    x[k] = (warp > 0 ? s_warp[8 * k + warp - 1] : 0) + inc[k] - x[k];
+    total[k] = s_warp[8 * k + 7];
+  }
 }
 
 // 2. Per token v (one thread of 256-thread blocks): hist[c][v] <- rows of v
@@ -181,8 +332,9 @@ __global__ void __launch_bounds__(256) tokscan_kernel(int* __restrict__ hist, in
                                                       int* __restrict__ pbase, int* __restrict__ gbase,
                                                       int* __restrict__ gcnt, int* __restrict__ pcnt,
                                                       int* __restrict__ powner, int* lb, unsigned* status) {
+  allow_next_grid();
   wait_prior_grid();
-  __shared__ int s_warp[8];
+  __shared__ int s_warp[24];
   __shared__ int s_b, s_ex[3];
   const int nb = gridDim.x;
   if (threadIdx.x == 0) s_b = atomicAdd(lb + 8 * nb, 1);
@@ -205,9 +357,9 @@ __global__ void __launch_bounds__(256) tokscan_kernel(int* __restrict__ hist, in
   const int np = (run + kPieceRows - 1) / kPieceRows;
   const int ng = np >= 2 ? (np + kGroupPieces - 1) / kGroupPieces : 0;
   int t[3];
-  const int la = block_scan_256(run, s_warp, &t[0]);
-  const int lpb = block_scan_256(np, s_warp, &t[1]);
-  const int lgb = block_scan_256(ng, s_warp, &t[2]);
+  int pre[3] = {run, np, ng};
+  block_scan3_256(pre, s_warp, t);
+  const int la = pre[0], lpb = pre[1], lgb = pre[2];
   if (threadIdx.x < 32) {
     // Warp 0: publish this block's totals, then read up to 32 predecessors'
     // records at once (lane k: block b - 1 - k - 32 r), adding their totals
@@ -280,74 +432,21 @@ __global__ void __launch_bounds__(256) tokscan_kernel(int* __restrict__ hist, in
   }
 }
 
-// 3. Block c: warp 0 walks the chunk's rows in order, 32 at a time, and
-//    writes each row index at its token's next slot; lanes with equal ids
-//    take consecutive slots in lane order, so each token's rows keep their
-//    row order (stable).  The cursors of the chunk's tokens (offs[v] +
-//    hist[c][v]) are staged in shared memory when V <= kPlaceSmemV (dynamic
-//    shared memory of V ints, of which only the chunk's tokens are written;
-//    threads holding the same token write the same value), else updated in
-//    place in hist.
-__global__ void place_kernel(const int64_t* __restrict__ ids, int N, int V, int R, int* __restrict__ hist,
-                             const int* __restrict__ offs, int* __restrict__ perm, int use_smem) {
-  extern __shared__ int s_cur[];
+// 3. Row i (one thread): its slot offs[v] + hist[c][v] (the rows of v in
+//    chunks before its chunk c, after the token scan) + lrank[i] gets the
+//    row index (perm), so each token's rows keep their row order (stable).
+//    The ids are the caller's input, which no kernel of this call writes, so
+//    they are read before the wait.
+__global__ void __launch_bounds__(256) place_kernel(const int64_t* __restrict__ ids, int N, int V, int R,
+                                                    const int* __restrict__ hist, const int* __restrict__ lrank,
+                                                    const int* __restrict__ offs, int* __restrict__ perm) {
+  allow_next_grid();
+  const int i = blockIdx.x * 256 + threadIdx.x;
+  const long long id = i < N ? ids[i] : -1;
   wait_prior_grid();
-  const int c = blockIdx.x;
-  int* hc = hist + static_cast<size_t>(c) * V;
-  if (use_smem) {
-    const int i0 = c * R, i1 = min(N, i0 + R);
-    for (int b0 = i0; b0 < i1; b0 += 4 * static_cast<int>(blockDim.x)) {
-      int tv[4], cur[4];
-#pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        const int i = b0 + k * blockDim.x + threadIdx.x;
-        const long long id = i < i1 ? ids[i] : -1;
-        tv[k] = id_ok(id, V) ? static_cast<int>(id) : -1;
-      }
-#pragma unroll
-      for (int k = 0; k < 4; ++k) cur[k] = tv[k] >= 0 ? offs[tv[k]] + hc[tv[k]] : 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k)
-        if (tv[k] >= 0) s_cur[tv[k]] = cur[k];
-    }
-    __syncthreads();
-  }
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  const int i0 = c * R, i1 = min(N, i0 + R);
-  // The walk is serial, so the chunk's ids are loaded ahead, 32 steps (1024
-  // rows) at a time, lane l holding row b + 32 s + l of step s (-1 for rows
-  // that do not count).
-  constexpr int kSteps = 32;
-  for (int b0 = i0; b0 < i1; b0 += 32 * kSteps) {
-    int tok[kSteps];
-#pragma unroll
-    for (int st = 0; st < kSteps; ++st) {
-      const int i = b0 + 32 * st + lane;
-      const long long v = i < i1 ? ids[i] : -1;
-      tok[st] = id_ok(v, V) ? static_cast<int>(v) : -1;
-    }
-#pragma unroll
-    for (int st = 0; st < kSteps; ++st) {
-      const int i = b0 + 32 * st + lane;
-      const int v = tok[st];
-      const bool ok = v >= 0;
-      const unsigned active = __ballot_sync(0xffffffffu, ok);
-      const unsigned peers = __match_any_sync(0xffffffffu, v) & active;
-      const unsigned below = peers & ((1u << lane) - 1u);
-      int base = 0;
-      if (ok) base = use_smem ? s_cur[v] : offs[v] + hc[v];
-      if (ok) perm[base + __popc(below)] = i;
-      __syncwarp();
-      if (ok && below == 0u) {  // the group's lowest lane advances the cursor
-        if (use_smem)
-          s_cur[v] = base + __popc(peers);
-        else
-          hc[v] += __popc(peers);
-      }
-      __syncwarp();
-    }
-  }
+  if (!id_ok(id, V)) return;
+  const int v = static_cast<int>(id);
+  perm[offs[v] + hist[static_cast<size_t>(i / R) * V + v] + lrank[i]] = i;
 }
 
 // Token owning entry p of a sorted exclusive-prefix array base[0..V]: the
@@ -361,19 +460,15 @@ __device__ __forceinline__ int owner_of(const int* __restrict__ base, int V, int
   return lo;
 }
 
-// dW[v][:] += s (lane l holds the float4 groups l, l + 32, l + 64, l + 96).
+// dW[v][:] += s (lane l holds the float4 groups l, l + 32, l + 64, l + 96),
+// by vector atomic adds.
 __device__ __forceinline__ void add_row_f4(float* __restrict__ dW, int v, int ng4, const float4 (&s)[4], int lane) {
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const int j = lane + 32 * q;
     if (j < ng4) {
       float4* o = reinterpret_cast<float4*>(dW + static_cast<size_t>(v) * (4 * ng4)) + j;
-      float4 a = *o;
-      a.x += s[q].x;
-      a.y += s[q].y;
-      a.z += s[q].z;
-      a.w += s[q].w;
-      *o = a;
+      atomicAdd(o, s[q]);
     }
   }
 }
@@ -491,9 +586,8 @@ __global__ void __launch_bounds__(256, 2) pieces_kernel(const uint16_t* __restri
       float4* o = reinterpret_cast<float4*>((single ? dW + static_cast<size_t>(v) * d : part + static_cast<size_t>(p) * d) +
                                             8 * j);
       if (single) {
-        float4 a = o[0], b = o[1];
-        o[0] = make_float4(a.x + lo.x, a.y + lo.y, a.z + lo.z, a.w + lo.w);
-        o[1] = make_float4(b.x + hi.x, b.y + hi.y, b.z + hi.z, b.w + hi.w);
+        atomicAdd(o, lo);
+        atomicAdd(o + 1, hi);
       } else {
         o[0] = lo;
         o[1] = hi;

@@ -136,12 +136,13 @@ int dev_info(DevInfo* out) {
       return LMCE_ENOTSUP;
     }
     if ((e = lmce::fwdk::set_attributes()) != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute(fwd)");
-    if ((e = cudaFuncSetAttribute(lmce::embk::place_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(sizeof(int) * lmce::embk::kPlaceSmemV))) != cudaSuccess)
-      return cuda_fail(e, "cudaFuncSetAttribute(place)");
     if ((e = cudaFuncSetAttribute(lmce::embk::count_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                  static_cast<int>(sizeof(int) * lmce::embk::kPlaceSmemV))) != cudaSuccess)
+                                  static_cast<int>(sizeof(int) * lmce::embk::kCountSmemV))) != cudaSuccess)
       return cuda_fail(e, "cudaFuncSetAttribute(count)");
+    if ((e = cudaFuncSetAttribute(lmce::embk::count8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  static_cast<int>(sizeof(uint16_t) * lmce::embk::kWalkers *
+                                                   lmce::embk::kWalkersMaxV))) != cudaSuccess)
+      return cuda_fail(e, "cudaFuncSetAttribute(count8)");
     if (int rc = lmce::bwdk::setup_attributes(); rc != 0) return rc;
     sms[dev] = n;
     ready[dev] = true;
@@ -883,6 +884,7 @@ int lmhead_tied_embed_bwd(const int64_t* ids, const lmce_bf16* g, int64_t ldg, i
   char* e = w + L.embed;
   unsigned* status = reinterpret_cast<unsigned*>(w + L.status);
   int* hist = reinterpret_cast<int*>(e + E.hist);
+  int* lrank = reinterpret_cast<int*>(e + E.lrank);
   int* offs = reinterpret_cast<int*>(e + E.offs);
   int* pbase = reinterpret_cast<int*>(e + E.pbase);
   int* gbase = reinterpret_cast<int*>(e + E.gbase);
@@ -895,20 +897,24 @@ int lmhead_tied_embed_bwd(const int64_t* ids, const lmce_bf16* g, int64_t ldg, i
   const int R = static_cast<int>(ek::chunk_rows(N)), C = static_cast<int>(ek::n_chunks(N));
   const int n = static_cast<int>(N), v = static_cast<int>(V), dd = static_cast<int>(d);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  const int use_smem = V <= ek::kPlaceSmemV ? 1 : 0;
-  const size_t place_smem = use_smem ? sizeof(int) * static_cast<size_t>(V) : 0;
+  const int use_smem = V <= ek::kCountSmemV ? 1 : 0;
+  const size_t count_smem = use_smem ? sizeof(int) * static_cast<size_t>(V) : 0;
   int* lb = reinterpret_cast<int*>(e + E.lb);
   const int nb = static_cast<int>(cdiv(V, 256));
   lmce::count_launches(4);
-  ek::count_kernel<<<C, 256, place_smem, s>>>(ids, n, v, R, hist, status, use_smem, lb,
-                                              static_cast<int>(ek::lb_ints(V)));
+  if (R == 1024 && V <= ek::kWalkersMaxV)
+    ek::count8_kernel<<<C, 256, sizeof(uint16_t) * ek::kWalkers * static_cast<size_t>(V), s>>>(
+        ids, n, v, hist, lrank, status, lb, static_cast<int>(ek::lb_ints(V)));
+  else
+    ek::count_kernel<<<C, 256, count_smem, s>>>(ids, n, v, R, hist, lrank, status, use_smem, lb,
+                                                static_cast<int>(ek::lb_ints(V)));
   cudaError_t err = cudaGetLastError();
   if (err == cudaSuccess)
     err = launch_pdl(ek::tokscan_kernel, nb, 256, 0, s, hist, C, v, offs, pbase, gbase, gcnt, pcnt, powner, lb,
                      status);
   if (err == cudaSuccess)
-    err = launch_pdl(ek::place_kernel, C, 256, place_smem, s, ids, n, v, R, hist, static_cast<const int*>(offs), perm,
-                     use_smem);
+    err = launch_pdl(ek::place_kernel, static_cast<int>(cdiv(N, 256)), 256, 0, s, ids, n, v, R,
+                     static_cast<const int*>(hist), static_cast<const int*>(lrank), static_cast<const int*>(offs), perm);
   if (err == cudaSuccess)
     err = launch_pdl(ek::pieces_kernel, di.sms * 8, 256, 0, s, reinterpret_cast<const uint16_t*>(g),
                      static_cast<long long>(ldg), dd, v, static_cast<const int*>(offs), static_cast<const int*>(pbase),

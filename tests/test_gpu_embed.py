@@ -3,7 +3,8 @@
 
 Each element of the result is an fp32 sum, along a fixed tree, of the token's
 bf16 rows (pieces of at most 32 rows summed in row order, groups of 16 pieces
-added in order, the groups added in order, then one addition into dW).  The classic bound for recursive
+added in order, the groups added in order, then one atomic addition into dW,
+which flushes only subnormal results).  The classic bound for recursive
 summation gives, per element, |gpu - exact| <= (n_v + 1) u (sum |g| + |dW0|)
 with n_v the token's row count and u = 2^-24; the tests hold the GPU to that
 bound, and to bit-identical repeats."""
