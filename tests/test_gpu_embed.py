@@ -64,8 +64,9 @@ def check(oracle_mod, ids, g_bits, V, dW0, dW, valid=None):
     (3000, 1, 128, None),      # one token owns every row (47 pieces)
     (777, 777, 256, None),     # every token once (a permutation below)
     (2500, 400, 192, 256),     # g with a row stride wider than d
-    (30000, 20000, 64, None),  # 79 token blocks: the token scan looks back past one warp's 32 records
-    (20000, 50000, 64, None),  # V above the shared-memory cursor limit: global counts and cursors
+    (30000, 20000, 64, None),  # 79 token blocks: the token scan looks back past one warp's 32 records;
+                               # V above the eight-warp count walk: one warp's walk, counts in shared memory
+    (20000, 50000, 64, None),  # V above the shared-memory count limit: counts in the histogram rows
 ])
 def test_tied_embed_matches_oracle(lm, oracle_mod, N, V, d, ld):
     e = si.make_embed_inputs(N, V, d, seed=3000 + N)
