@@ -114,3 +114,22 @@ def test_tied_embed_training_batch_full(lm, oracle_mod):
     st, dW = run(lm, e["ids"], e["g"], e["V"], dW0)
     assert st == lm.LMCE_OK
     check(oracle_mod, e["ids"], e["g"], e["V"], dW0, dW)
+
+
+def test_tied_embed_count_forms_agree(lm):
+    """The stable sort is unique, so the three forms of the count kernel (eight
+    warps with 16-bit counts for V <= 12288, one warp with counts in shared
+    memory up to V = 32768, counts in the histogram rows above) give the same
+    dW bits for the same ids; the extra vocabulary rows stay untouched."""
+    N, V0, d = 20000, 12288, 128
+    e = si.make_embed_inputs(N, V0, d, seed=3303)
+    dW0 = torch.randn(V0, d, device="cuda") * 1e-2
+    outs = []
+    for V in (V0, V0 + 1, 40000):
+        init = torch.zeros(V, d, device="cuda")
+        init[:V0] = dW0
+        st, dW = run(lm, e["ids"], e["g"], V, init)
+        assert st == lm.LMCE_OK
+        assert torch.equal(dW[V0:], init[V0:])
+        outs.append(dW[:V0])
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[0], outs[2])
