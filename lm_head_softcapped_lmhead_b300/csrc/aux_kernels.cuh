@@ -104,9 +104,9 @@ __global__ void __launch_bounds__(kBpbThreads) bpb_kernel(const float* __restric
   double a = 0.0;
   long long b = 0, c = 0;
   const long long stride = static_cast<long long>(kBpbBlocks) * kBpbThreads;
-  // A thread's rows i0, i0 + stride, ... in that order, four at a time with
-  // their loads issued together.
-  constexpr int kB = 4;
+  // A thread's rows i0, i0 + stride, ... in that order, sixteen at a time
+  // with their loads issued together.
+  constexpr int kB = 16;
   for (long long i0 = static_cast<long long>(blockIdx.x) * kBpbThreads + threadIdx.x; i0 < N; i0 += kB * stride) {
     bool live[kB];
 #pragma unroll
@@ -254,11 +254,16 @@ __global__ void __launch_bounds__(kCompactThreads) compact_write_kernel(
   constexpr int R = kCompactRows / kCompactThreads;
   const int base = blockIdx.x * kCompactRows + threadIdx.x;
   bool m[R];
+  int64_t tv[R];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
     const int i = base + k * kCompactThreads;
     m[k] = i < N && mask[i];
   }
+  // The scored rows' targets are loaded before the scans (whose barriers
+  // would otherwise hold each load back until the one before it returned).
+#pragma unroll
+  for (int k = 0; k < R; ++k) tv[k] = m[k] ? tgt[base + k * kCompactThreads] : 0;
   int pos = block_offset[blockIdx.x];
 #pragma unroll
   for (int k = 0; k < R; ++k) {
@@ -267,7 +272,7 @@ __global__ void __launch_bounds__(kCompactThreads) compact_write_kernel(
     const int ex = block_exclusive_scan(m[k] ? 1 : 0, s_warp, &tot);
     if (m[k]) {
       idx[pos + ex] = i;
-      tgt_c[pos + ex] = tgt[i];
+      tgt_c[pos + ex] = tv[k];
     } else if (i < N) {
       if (nll) nll[i] = 0.f;
       if (lse) lse[i] = 0.f;
@@ -276,16 +281,43 @@ __global__ void __launch_bounds__(kCompactThreads) compact_write_kernel(
   }
 }
 
-// pass 4: h_c[r, :] = h[idx[r], :] for r < n_scored (16-byte vectors).
+// pass 4: h_c[r, :] = h[idx[r], :] for r < n_scored (16-byte vectors, at most
+// 64 per row).  A warp copies four rows at a time: their indices, then all
+// their vectors' loads (non-coherent, not kept in L1, with L2 fetching
+// 256-byte blocks: each row is read once, in an order that is a gather).
+__device__ __forceinline__ uint4 ld_once16(const uint4* p) {
+  uint4 r;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+      : "l"(p));
+  return r;
+}
 __global__ void gather_rows_kernel(const uint4* __restrict__ h, long long ldh_vec, const int* __restrict__ idx,
                                    const int* __restrict__ n_scored, int vec_per_row, uint4* __restrict__ h_c) {
   const int n = *n_scored;
-  const long long total = static_cast<long long>(n) * vec_per_row;
-  for (long long e = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; e < total;
-       e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long r = e / vec_per_row;
-    const int v = static_cast<int>(e % vec_per_row);
-    h_c[r * vec_per_row + v] = h[static_cast<long long>(idx[r]) * ldh_vec + v];
+  const int lane = threadIdx.x & 31;
+  const long long warps = static_cast<long long>(gridDim.x) * (blockDim.x >> 5);
+  for (long long r0 = 4 * (static_cast<long long>(blockIdx.x) * (blockDim.x >> 5) + (threadIdx.x >> 5)); r0 < n;
+       r0 += 4 * warps) {
+    int src[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) src[k] = r0 + k < n ? idx[r0 + k] : -1;
+    uint4 x[4][2];
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int v = lane + 32 * q;
+        x[k][q] = src[k] >= 0 && v < vec_per_row ? ld_once16(h + static_cast<long long>(src[k]) * ldh_vec + v)
+                                                 : make_uint4(0u, 0u, 0u, 0u);
+      }
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+#pragma unroll
+      for (int q = 0; q < 2; ++q) {
+        const int v = lane + 32 * q;
+        if (src[k] >= 0 && v < vec_per_row) h_c[(r0 + k) * vec_per_row + v] = x[k][q];
+      }
   }
 }
 
