@@ -209,11 +209,17 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* s_warp, int* tot
   return before;
 }
 
-// pass 1: scored-row count per block of kCompactRows rows (thread t reads
-// rows base + 256 k + t: coalesced).
+// passes 1 and 2: scored-row count per block of kCompactRows rows (thread t
+// reads rows base + 256 k + t: coalesced); the block that stores the last
+// count (an arrival counter, zero between calls: the workspace's zero-fill,
+// then reset here) turns the counts into exclusive offsets in block order and
+// stores the grand total, the live row count of the compacted problem.
 __global__ void __launch_bounds__(kCompactThreads) compact_count_kernel(const uint8_t* __restrict__ mask, int N,
-                                                                        int* __restrict__ block_count) {
+                                                                        int* __restrict__ block_count,
+                                                                        int* __restrict__ n_scored,
+                                                                        unsigned* __restrict__ arrivals) {
   __shared__ int s_warp[kCompactThreads / 32];
+  __shared__ int s_last;
   const int base = blockIdx.x * kCompactRows + threadIdx.x;
   int c = 0;
 #pragma unroll
@@ -223,24 +229,28 @@ __global__ void __launch_bounds__(kCompactThreads) compact_count_kernel(const ui
   }
   int total;
   block_exclusive_scan(c, s_warp, &total);
-  if (threadIdx.x == 0) block_count[blockIdx.x] = total;
-}
-
-// pass 2 (one block): exclusive scan of the block counts; the grand total is
-// the live row count of the compacted problem.
-__global__ void __launch_bounds__(kCompactThreads) compact_scan_kernel(int* __restrict__ block_count, int nblocks,
-                                                                       int* __restrict__ n_scored) {
-  __shared__ int s_warp[kCompactThreads / 32];
-  int carry = 0;
-  for (int base = 0; base < nblocks; base += kCompactThreads) {
-    const int i = base + threadIdx.x;
-    const int v = (i < nblocks) ? block_count[i] : 0;
-    int total;
-    const int ex = block_exclusive_scan(v, s_warp, &total);
-    if (i < nblocks) block_count[i] = carry + ex;
-    carry += total;
+  if (threadIdx.x == 0) {
+    block_count[blockIdx.x] = total;
+    __threadfence();
+    s_last = atomicAdd(arrivals, 1u) == gridDim.x - 1;
   }
-  if (threadIdx.x == 0) *n_scored = carry;
+  __syncthreads();
+  if (!s_last) return;  // the whole block leaves together
+  __threadfence();      // the other blocks' counts are read after this
+  const int nblocks = static_cast<int>(gridDim.x);
+  int carry = 0;
+  for (int b0 = 0; b0 < nblocks; b0 += kCompactThreads) {
+    const int i = b0 + threadIdx.x;
+    const int v = (i < nblocks) ? __ldcg(block_count + i) : 0;
+    int tot;
+    const int ex = block_exclusive_scan(v, s_warp, &tot);
+    if (i < nblocks) block_count[i] = carry + ex;
+    carry += tot;
+  }
+  if (threadIdx.x == 0) {
+    *n_scored = carry;
+    *arrivals = 0u;
+  }
 }
 
 // pass 3: scored rows get their compacted index (idx[pos] = i, targets

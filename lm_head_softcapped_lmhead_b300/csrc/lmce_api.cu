@@ -72,8 +72,8 @@ Layout make_layout(int64_t N, int64_t V, int64_t d, unsigned flags) {
   if (flags & LMCE_WS_MASKED) {
     L.blkcnt = o;
     o = up(o + sizeof(int) * cdiv(N, lmce::kCompactRows));
-    L.nscored = o;
-    o = up(o + sizeof(int));
+    L.nscored = o;  // the live row count, then the count kernel's arrival counter
+    o = up(o + 2 * sizeof(int));
     L.idx = o;
     o = up(o + sizeof(int) * N);
     L.tgt_c = o;
@@ -360,9 +360,10 @@ int fwd_impl(const lmce_bf16* h, int64_t ldh, const lmce_bf16* W, int64_t N, int
     int* idxp = reinterpret_cast<int*>(w + L.idx);
     int64_t* tgc = reinterpret_cast<int64_t*>(w + L.tgt_c);
     lmce_bf16* hc = reinterpret_cast<lmce_bf16*>(w + L.h_c);
-    lmce::count_launches(4);
-    lmce::compact_count_kernel<<<nblk, lmce::kCompactThreads, 0, s>>>(mask, static_cast<int>(N), blkcnt);
-    lmce::compact_scan_kernel<<<1, lmce::kCompactThreads, 0, s>>>(blkcnt, nblk, nsc);
+    lmce::count_launches(3);
+    // nsc[1] is the count kernel's arrival counter (zero between calls).
+    lmce::compact_count_kernel<<<nblk, lmce::kCompactThreads, 0, s>>>(mask, static_cast<int>(N), blkcnt, nsc,
+                                                                      reinterpret_cast<unsigned*>(nsc + 1));
     lmce::compact_write_kernel<<<nblk, lmce::kCompactThreads, 0, s>>>(mask, static_cast<int>(N), blkcnt, tgt, idxp,
                                                                       tgc, nll, lse);
     const int vec = static_cast<int>(d / 8);
